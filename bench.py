@@ -1,0 +1,417 @@
+#!/usr/bin/env python3
+"""Throughput of the KPool DSA step (one DSA layer: compress + score + top-k +
+sparse MLA) on B300, with the roofline of its dominant kernel and the fp64
+oracle timed on the host cores beside it.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl kpool|reference]
+                    [--workload decode|ragged|prefill|long]
+
+Prints ONE JSON line (rank 0).  Timing: every step is a CUDA-graph replay of
+kp_dsa_forward bracketed by CUDA events on the launching stream; a 256 MB read
+flushes L2 between steps, outside the events.  Under torchrun each rank runs
+its own batch (weak scaling over independent sequences, no collective on the
+data path); value = all ranks' query tokens / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import kpool_inputs as KI  # noqa: E402
+
+METRIC = {"decode": "DSA decode tokens/s per B300", "ragged": "DSA decode tokens/s per B300",
+          "long": "DSA decode tokens/s per B300", "prefill": "DSA prefill tokens/s per B300"}
+DESCR = {
+    "decode": "decode: 32 seqs x ctx 32768, 1 query each, top-k 2048 tokens (512 pools + tail), "
+              "indexer 32x128, MLA 64 heads x 576 latent, bf16",
+    "ragged": "ragged decode + MTP: 8 seqs, ctx U[65537,131071] (not multiples of 4), 2 queries each, top-k 2048",
+    "prefill": "chunked causal prefill: 1 seq, 4096 new queries on 61440 cached (ctx 65536), top-k 2048",
+    "long": "long-context decode: 1 seq, ctx 1,048,575, 4 queries, top-k 2048",
+}
+STAGES = ("kpool_compress", "indexer_score", "topk_select", "sparse_mla_attend")
+KERNEL_FILES = {"kpool_compress": "compress.cu", "indexer_score": "score.cu", "topk_select": "topk.cu",
+                "sparse_mla_attend": "attend.cu"}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="kpool", choices=["kpool", "reference"])
+    ap.add_argument("--workload", default="decode", choices=["decode", "ragged", "prefill", "long"])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the CPU-baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ workload facts
+
+def workload(name: str, rank: int) -> KI.Workload:
+    spec = KI.named(name)
+    spec.seed += 1000 * rank          # each rank its own independent batch
+    return KI.make(spec)
+
+
+def algorithmic_bytes(wl: KI.Workload):
+    """Bytes the method must move per step, by stage (roofline)."""
+    kp = wl.spec.kpool
+    K = wl.k_pools
+    nf = (wl.q_pos.astype(np.int64) + 1) // kp
+    tail = (wl.q_pos.astype(np.int64) + 1) - nf * kp
+    n_tok = np.minimum(nf, K) * kp + tail
+    # pooled keys once per sequence (the largest n_full among its queries), q and w
+    per_seq = {}
+    for q in range(wl.NQ):
+        b = int(wl.q_seq[q])
+        per_seq[b] = max(per_seq.get(b, 0), int(nf[q]))
+    score = sum(per_seq.values()) * 128 * 2 + wl.NQ * (32 * 128 * 2 + 32 * 4)
+    attend = int(n_tok.sum()) * 512 * 2 + wl.NQ * 64 * (512 * 2 + 512 * 2 + 4)
+    n_new = int((wl.lens - wl.prev_len).sum())
+    new_pools = int(sum(int(L) // kp - int(P) // kp for L, P in zip(wl.lens, wl.prev_len)))
+    compress = n_new * 2 * 128 * 2 + new_pools * 128 * 2
+    return {"kpool_compress": compress, "indexer_score": score, "topk_select": 0,
+            "sparse_mla_attend": attend}, int(n_tok.sum())
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6400.0, 1800.0, "fallback"
+
+
+def kernel_traffic(stage: str):
+    """ncu DRAM bytes per launch of this stage's kernel, if the committed summary
+    was taken on the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(stage)
+    if not d:
+        return None
+    src = os.path.join(ROOT, "dsa_indexer_sparse_kpool_b300", "csrc", KERNEL_FILES[stage])
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    return d["bytes_per_launch"] if d.get("source_sha") == sha else None
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.path = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            sel = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        except Exception:
+            sel = []
+        self.cmd = ["nvidia-smi", *sel, "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits", "-lms", "100"]
+
+    def start(self):
+        try:
+            self.out = open(os.devnull, "w")
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            text, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            text = ""
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in text.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ CPU oracle baseline
+
+class OracleStep:
+    """The fp64 oracle doing this workload's step for a batch of queries:
+    compress of the pools the step's new tokens complete, scores over all
+    visible pools, top-k, attention.  The pooled caches of the sequences as they
+    were before the step are built once in the constructor (cache state, not
+    step work)."""
+
+    def __init__(self, wl: KI.Workload, threads: int):
+        import oracle
+        self.oracle, self.wl, self.threads, kp = oracle, wl, threads, wl.spec.kpool
+        pooled, self.pool_off, off = [], np.zeros(wl.B, np.int64), 0
+        for b in range(wl.B):
+            a, e = int(wl.tok_off[b]), int(wl.tok_off[b] + wl.prev_len[b])
+            p, _ = oracle.kpool_compress(KI.bits(wl.keys[a:e]), KI.bits(wl.gates[a:e]), KI.bits(wl.ape), kp)
+            full = np.zeros((int(wl.lens[b]) // kp + 1, 128), np.uint16)
+            full[:p.shape[0]] = p
+            pooled.append(full)
+            self.pool_off[b] = off
+            off += full.shape[0]
+        self.pooled = np.concatenate(pooled)
+        self.lat = KI.bits(wl.latent)
+        self.keys, self.gates, self.ape = KI.bits(wl.keys), KI.bits(wl.gates), KI.bits(wl.ape)
+        self.q_idx, self.q_lat, self.w = KI.bits(wl.q_idx), KI.bits(wl.q_lat), wl.w.numpy()
+
+    def run(self, queries) -> int:
+        wl, kp, o = self.wl, self.wl.spec.kpool, self.oracle
+        bq = np.asarray(queries)
+        for b in sorted({int(wl.q_seq[q]) for q in bq}):
+            p0, p1 = int(wl.prev_len[b]) // kp, int(wl.lens[b]) // kp
+            if p1 > p0:
+                a, e = int(wl.tok_off[b]) + p0 * kp, int(wl.tok_off[b]) + p1 * kp
+                newp, _ = o.kpool_compress(self.keys[a:e], self.gates[a:e], self.ape, kp)
+                self.pooled[self.pool_off[b] + p0: self.pool_off[b] + p1] = newp
+        o.dsa_queries(wl.q_seq[bq], wl.q_pos[bq], self.pool_off, wl.tok_off, kp, wl.k_pools, 1, self.q_idx[bq],
+                      self.w[bq], self.pooled, self.q_lat[bq], self.lat, wl.spec.sm_scale, threads=self.threads)
+        return len(bq)
+
+    def batches(self):
+        qs = list(range(self.wl.NQ))
+        while True:
+            for i in range(0, len(qs), self.threads):
+                yield qs[i:i + self.threads]
+
+    def rate(self, seconds: float):
+        """Query tokens per second over whole batches until `seconds` have passed."""
+        done, t0, it = 0, time.perf_counter(), self.batches()
+        while True:
+            done += self.run(next(it))
+            if time.perf_counter() - t0 >= seconds:
+                break
+        wall = time.perf_counter() - t0
+        return done / wall, done, wall
+
+
+# ------------------------------------------------------------------ reference arm
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    wl = workload(args.workload, 0)
+    threads = os.cpu_count() or 1
+    ob = OracleStep(wl, threads)
+    it = ob.batches()
+    t0 = time.perf_counter()
+    ob.run(next(it))                              # calibration: one batch
+    per_step = time.perf_counter() - t0
+    steps = max(1, min(args.steps, int(120.0 / max(per_step, 1e-6))))
+    for _ in range(min(args.warmup, 2)):
+        ob.run(next(it))
+    t0 = time.perf_counter()
+    n = 0
+    for _ in range(steps):
+        n += ob.run(next(it))
+    wall = time.perf_counter() - t0
+    val = n / wall
+    line = {"impl": "reference", "metric": METRIC[args.workload], "value": val, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": steps, "steps_requested": args.steps, "warmup": args.warmup,
+            "ms_per_step": wall / steps * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic",
+            "config": {"workload": DESCR[args.workload], "queries_per_step": min(threads, wl.NQ)},
+            "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                             "sample": f"each step = {min(threads, wl.NQ)} whole queries of the workload (compress "
+                                       f"of the step's new pools, scores, top-k, attention), OpenMP over queries; "
+                                       f"steps capped so the run ends in about 2 minutes"},
+            "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    import torch.distributed as dist
+    from dsa_indexer_sparse_kpool_b300 import Config
+    from dsa_indexer_sparse_kpool_b300 import build as kbuild
+    from dsa_indexer_sparse_kpool_b300.session import build_session, build_step
+
+    kbuild.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    wl = workload(args.workload, rank)
+    cfg = Config(topk_tokens=wl.spec.topk_tokens, sm_scale=wl.spec.sm_scale)
+    sess = build_session(cfg, wl.lens.tolist(), wl.prev_len.tolist(), wl.tok_off.tolist(), wl.pool_off.tolist(),
+                         wl.pool_rows, wl.latent, wl.keys, wl.gates, wl.ape, device=dev)
+    step = build_step(sess, wl.lens.tolist(), wl.prev_len.tolist(), wl.tok_off.tolist(), wl.keys, wl.gates,
+                      wl.q_seq, wl.q_pos, wl.q_idx, wl.w, wl.q_lat)
+    NQ = wl.NQ
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(256 << 18, dtype=torch.float32, device=dev).fill_(1.0)   # 256 MB > 126 MB L2
+
+    def flush_l2():
+        flush.sum()
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):                      # eager warm-up (lazy init outside capture)
+            step.run()
+        torch.cuda.synchronize()
+        assert int(sess.status.item()) == 0, "device status set during warm-up"
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            step.run()
+        calls, _ = step.stage_calls()
+        for c in calls:
+            c()
+        stage_graphs = []
+        for c in calls:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                c()
+            stage_graphs.append(g)
+        torch.cuda.synchronize()
+
+        def barrier():
+            torch.cuda.synchronize()
+            if world > 1:
+                dist.barrier()
+
+        # ---- headline: K replays of the whole step
+        for _ in range(args.warmup):
+            flush_l2()
+            graph.replay()
+        barrier()
+        sampler = ClockSampler(local)
+        sampler.start()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush_l2()
+            ev[i][0].record(stream)
+            graph.replay()
+            ev[i][1].record(stream)
+        barrier()
+        clocks = sampler.stop()
+        step_ms = [a.elapsed_time(b) for a, b in ev]
+        total_ms = float(sum(step_ms))
+
+        # ---- per-stage breakdown (one graph per stage, events between)
+        ks = max(1, min(args.steps, 500))
+        sev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(ks)]
+        for i in range(ks):
+            flush_l2()
+            sev[i][0].record(stream)
+            for j, g in enumerate(stage_graphs):
+                g.replay()
+                sev[i][j + 1].record(stream)
+        barrier()
+        stage_ms = {STAGES[j]: float(np.mean([sev[i][j].elapsed_time(sev[i][j + 1]) for i in range(ks)]))
+                    for j in range(4)}
+
+        # ---- end to end: pinned host inputs -> step -> host outputs, every step
+        h_in = [(t.detach().cpu().pin_memory(), t) for t in (step.q_idx, step.w, step.q_lat, step.keys, step.gates,
+                                                            step.prev_len, step.new_off, step.queries.q_seq,
+                                                            step.queries.q_pos)]
+        h_out = [(torch.empty_like(t, device="cpu").pin_memory(), t) for t in (step.out, step.lse)]
+        h2d = sum(h.numel() * h.element_size() for h, _ in h_in)
+        d2h = sum(h.numel() * h.element_size() for h, _ in h_out)
+        ke = max(1, min(args.steps, 1000))
+        eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(ke)]
+        for i in range(ke):
+            flush_l2()
+            eev[i][0].record(stream)
+            for h, d in h_in:
+                d.copy_(h, non_blocking=True)
+            graph.replay()
+            for h, d in h_out:
+                h.copy_(d, non_blocking=True)
+            eev[i][1].record(stream)
+        barrier()
+        e2e_ms = float(np.mean([a.elapsed_time(b) for a, b in eev]))
+        status = int(sess.status.item())
+
+    # ---- aggregate over ranks
+    t_step = total_ms / args.steps
+    t_e2e = e2e_ms
+    if world > 1:
+        t = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_step = float(t[0]) / args.steps
+        t_e2e = float(t[1])
+    value = world * NQ / (t_step * 1e-3)
+    e2e_value = world * NQ / (t_e2e * 1e-3)
+
+    if rank == 0:
+        alg, n_tok = algorithmic_bytes(wl)
+        hbm, bf16, src = measured_peaks()
+        dominant = max(("indexer_score", "sparse_mla_attend", "topk_select", "kpool_compress"),
+                       key=lambda s: stage_ms[s])
+        ach = alg[dominant] / (stage_ms[dominant] * 1e-3) / 1e9 if alg[dominant] else 0.0
+        roof = {"bound": "hbm", "kernel": dominant, "achieved": ach, "peak": hbm, "unit": "GB/s",
+                "frac": ach / hbm, "peak_source": src, "traffic": kernel_traffic(dominant),
+                "algorithmic_bytes": alg[dominant], "avg_launch_ms": stage_ms[dominant]}
+        step_bytes = sum(alg.values())
+        cpu = None
+        if not args.no_cpu_baseline:
+            threads = os.cpu_count() or 1
+            rate, done, wall = OracleStep(wl, threads).rate(args.cpu_seconds)
+            cpu = {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                   "sample": f"{done} whole queries of this workload in {wall:.1f} s (compress of the step's new "
+                             f"pools, scores over all visible pools, top-k, attention), OpenMP over queries"}
+        line = {
+            "metric": METRIC[args.workload], "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": DESCR[args.workload], "batch": wl.B, "queries": NQ,
+                       "ctx": int(wl.lens.max()), "topk_tokens": wl.spec.topk_tokens,
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "l2": "flushed between timed steps (256 MB read)", "timing": "CUDA-graph replay, events"},
+            "roofline": roof,
+            "step_roofline": {"algorithmic_bytes": step_bytes, "achieved_GBps": step_bytes / (t_step * 1e-3) / 1e9,
+                              "frac": step_bytes / (t_step * 1e-3) / 1e9 / hbm},
+            "stage_ms": stage_ms,
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": 5 * args.steps,
+            "clocks": clocks,
+            "device_status": status,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

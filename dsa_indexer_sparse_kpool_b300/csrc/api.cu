@@ -1,0 +1,290 @@
+// api.cu -- the extern "C" entry points of libkpool_dsa.so: argument checks,
+// workspace carving and the fused step.  No allocation, no synchronisation
+// (except kp_read_device_status), everything on the caller's stream.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "kp_common.cuh"
+#include "kp_internal.h"
+
+namespace kp {
+
+namespace {
+thread_local std::string g_last_error;
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+kp_status check_config(const kp_config &c) {
+    if (c.kpool != kKpool) return KP_ERR_UNSUPPORTED;
+    if (c.topk_tokens <= 0 || c.topk_tokens % c.kpool != 0) return KP_ERR_INVALID_ARG;
+    if (c.topk_tokens / c.kpool > KP_MAX_TOPK_POOLS) return KP_ERR_UNSUPPORTED;
+    if (c.compress_mode != KP_COMPRESS_LEARNED && c.compress_mode != KP_COMPRESS_MEAN)
+        return KP_ERR_INVALID_ARG;
+    if (c.always_select_tail != 0 && c.always_select_tail != 1) return KP_ERR_INVALID_ARG;
+    if (!std::isfinite(c.sm_scale)) return KP_ERR_INVALID_ARG;
+    return KP_OK;
+}
+
+kp_status check_queries(const kp_queries &q) {
+    if (q.num_queries < 0) return KP_ERR_INVALID_ARG;
+    if (q.num_queries > 0 && (!q.q_seq || !q.q_pos)) return KP_ERR_INVALID_ARG;
+    if (q.max_pools < 0) return KP_ERR_INVALID_ARG;
+    if (q.max_pools > KP_MAX_SCORE_POOLS) return KP_ERR_UNSUPPORTED;
+    if (q.num_queries > (1 << 24)) return KP_ERR_UNSUPPORTED;
+    return KP_OK;
+}
+
+kp_status check_seqs(const kp_seqs &s, bool latent, bool pooled) {
+    if (s.num_seqs < 1 || s.num_seqs > 65535) return KP_ERR_INVALID_ARG;
+    if (latent && (!s.latent_row_off || s.latent_rows <= 0 || s.latent_rows >= (int64_t(1) << 40)))
+        return KP_ERR_INVALID_ARG;
+    if (pooled && (!s.pool_row_off || s.pool_rows <= 0 || s.pool_rows >= (int64_t(1) << 31)))
+        return KP_ERR_INVALID_ARG;
+    return KP_OK;
+}
+
+int64_t score_stride_for(int32_t max_pools) {
+    const int64_t p = max_pools > 0 ? max_pools : 1;
+    return (p + 127) / 128 * 128;
+}
+
+// Forward workspace layout: [scores][pool_idx][n_sel][step scratch].
+struct ForwardLayout {
+    size_t scores, pool_idx, n_sel, scratch, total;
+};
+ForwardLayout forward_layout(const kp_forward_args &a, int sm_count) {
+    ForwardLayout L;
+    const size_t nq = static_cast<size_t>(a.q.num_queries > 0 ? a.q.num_queries : 0);
+    const size_t K = static_cast<size_t>(a.cfg.topk_tokens / (a.cfg.kpool > 0 ? a.cfg.kpool : 1));
+    L.scores = 0;
+    L.pool_idx = L.scores + align_up(nq * score_stride_for(a.q.max_pools) * 4, 256);
+    L.n_sel = L.pool_idx + align_up(nq * K * 4, 256);
+    L.scratch = L.n_sel + align_up(nq * 4, 256);
+    const size_t plan = score_plan_bytes(static_cast<int32_t>(nq));
+    const size_t att = attend_ws_bytes(a.cfg, static_cast<int32_t>(nq),
+                                       attend_splits(a.cfg, static_cast<int32_t>(nq), sm_count));
+    L.total = L.scratch + (plan > att ? plan : att);
+    return L;
+}
+}  // namespace
+
+void record_cuda_error(const char *where, cudaError_t err) {
+    g_last_error = std::string(where) + ": " + cudaGetErrorName(err) + " (" + cudaGetErrorString(err) + ")";
+}
+void record_error_text(const char *text) { g_last_error = text; }
+
+kp_status check_launch(const char *where) {
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        record_cuda_error(where, e);
+        return KP_ERR_CUDA;
+    }
+    return KP_OK;
+}
+
+int device_sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+}  // namespace kp
+
+using namespace kp;
+
+extern "C" {
+
+kp_status kp_kpool_compress(const kp_compress_args *a, kp_stream_t stream) {
+    if (!a) return KP_ERR_INVALID_ARG;
+    kp_status st = check_config(a->cfg);
+    if (st != KP_OK) return st;
+    if (a->num_seqs < 1 || a->num_seqs > 65535 || a->num_new < 0 || a->max_new_per_seq < 0)
+        return KP_ERR_INVALID_ARG;
+    if (a->num_new == 0) return KP_OK;
+    if (a->max_new_per_seq == 0 || a->max_new_per_seq > a->num_new) return KP_ERR_INVALID_ARG;
+    if (!a->prev_len || !a->new_off || !a->keys || !a->tail_keys || !a->pooled || !a->pool_row_off ||
+        a->pool_rows <= 0)
+        return KP_ERR_INVALID_ARG;
+    if (a->cfg.compress_mode == KP_COMPRESS_LEARNED && (!a->gates || !a->ape || !a->tail_gates))
+        return KP_ERR_INVALID_ARG;
+    if (!aligned(a->keys, 8) || !aligned(a->pooled, 8) || !aligned(a->tail_keys, 8) ||
+        (a->gates && !aligned(a->gates, 8)) || (a->ape && !aligned(a->ape, 8)) ||
+        (a->tail_gates && !aligned(a->tail_gates, 8)))
+        return KP_ERR_INVALID_ARG;
+    return launch_compress(*a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t kp_score_workspace_size(int32_t num_queries) {
+    return score_plan_bytes(num_queries > 0 ? num_queries : 0);
+}
+
+kp_status kp_indexer_score(const kp_score_args *a, kp_stream_t stream) {
+    if (!a) return KP_ERR_INVALID_ARG;
+    kp_status st = check_config(a->cfg);
+    if (st != KP_OK) return st;
+    if ((st = check_queries(a->q)) != KP_OK) return st;
+    if ((st = check_seqs(a->seqs, false, true)) != KP_OK) return st;
+    if (a->q.num_queries == 0) return KP_OK;
+    if (!a->q_idx || !a->w || !a->pooled || !a->scores) return KP_ERR_INVALID_ARG;
+    if (!aligned(a->q_idx, 16) || !aligned(a->pooled, 16) || !aligned(a->w, 4) || !aligned(a->scores, 4))
+        return KP_ERR_INVALID_ARG;
+    if (a->score_stride < score_stride_for(a->q.max_pools)) return KP_ERR_INVALID_ARG;
+    if (!a->workspace || a->workspace_bytes < kp_score_workspace_size(a->q.num_queries) ||
+        !aligned(a->workspace, 256))
+        return KP_ERR_WORKSPACE;
+    return launch_score(*a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+kp_status kp_topk_select(const kp_topk_args *a, kp_stream_t stream) {
+    if (!a) return KP_ERR_INVALID_ARG;
+    kp_status st = check_config(a->cfg);
+    if (st != KP_OK) return st;
+    if ((st = check_queries(a->q)) != KP_OK) return st;
+    if (a->q.num_queries == 0) return KP_OK;
+    if (!a->scores || !a->pool_idx || !a->n_sel) return KP_ERR_INVALID_ARG;
+    if (a->score_stride < (a->q.max_pools > 0 ? a->q.max_pools : 1)) return KP_ERR_INVALID_ARG;
+    return launch_topk(*a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t kp_attend_workspace_size(const kp_config *cfg, int32_t num_queries) {
+    if (!cfg || cfg->kpool <= 0 || cfg->topk_tokens <= 0) return 256;
+    int sms = device_sm_count();
+    if (sms <= 0) sms = 148;
+    return attend_ws_bytes(*cfg, num_queries, attend_splits(*cfg, num_queries, sms));
+}
+
+kp_status kp_sparse_mla_attend(const kp_attend_args *a, kp_stream_t stream) {
+    if (!a) return KP_ERR_INVALID_ARG;
+    kp_status st = check_config(a->cfg);
+    if (st != KP_OK) return st;
+    if ((st = check_queries(a->q)) != KP_OK) return st;
+    if ((st = check_seqs(a->seqs, true, false)) != KP_OK) return st;
+    if (a->q.num_queries == 0) return KP_OK;
+    if (!a->q_lat || !a->latent || !a->pool_idx || !a->n_sel || !a->out) return KP_ERR_INVALID_ARG;
+    if (!aligned(a->q_lat, 16) || !aligned(a->latent, 16) || !aligned(a->out, 4)) return KP_ERR_INVALID_ARG;
+    const size_t need = kp_attend_workspace_size(&a->cfg, a->q.num_queries);
+    if (need > 256 && (!a->workspace || a->workspace_bytes < need || !aligned(a->workspace, 256)))
+        return KP_ERR_WORKSPACE;
+    return launch_attend(*a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t kp_workspace_size(const kp_forward_args *a) {
+    if (!a) return 0;
+    int sms = device_sm_count();
+    if (sms <= 0) sms = 148;
+    return forward_layout(*a, sms).total;
+}
+
+kp_status kp_dsa_forward(const kp_forward_args *a, kp_stream_t stream) {
+    if (!a) return KP_ERR_INVALID_ARG;
+    kp_status st = check_config(a->cfg);
+    if (st != KP_OK) return st;
+    if ((st = check_queries(a->q)) != KP_OK) return st;
+    if ((st = check_seqs(a->seqs, true, true)) != KP_OK) return st;
+    if (!a->out) return KP_ERR_INVALID_ARG;
+    const int sms = device_sm_count();
+    if (sms <= 0) {
+        record_error_text("cannot query the current CUDA device");
+        return KP_ERR_CUDA;
+    }
+    const ForwardLayout L = forward_layout(*a, sms);
+    if (!a->workspace || a->workspace_bytes < L.total || !aligned(a->workspace, 256)) return KP_ERR_WORKSPACE;
+    uint8_t *ws = static_cast<uint8_t *>(a->workspace);
+
+    kp_compress_args c;
+    std::memset(&c, 0, sizeof c);
+    c.cfg = a->cfg;
+    c.num_seqs = a->seqs.num_seqs;
+    c.prev_len = a->prev_len;
+    c.new_off = a->new_off;
+    c.num_new = a->num_new;
+    c.max_new_per_seq = a->max_new_per_seq;
+    c.keys = a->keys;
+    c.gates = a->gates;
+    c.ape = a->ape;
+    c.tail_keys = a->tail_keys;
+    c.tail_gates = a->tail_gates;
+    c.pooled = a->pooled;
+    c.pool_row_off = a->seqs.pool_row_off;
+    c.pool_rows = a->seqs.pool_rows;
+    c.d_status = a->d_status;
+
+    kp_score_args sc;
+    std::memset(&sc, 0, sizeof sc);
+    sc.cfg = a->cfg;
+    sc.seqs = a->seqs;
+    sc.q = a->q;
+    sc.q_idx = a->q_idx;
+    sc.w = a->w;
+    sc.pooled = a->pooled;
+    sc.scores = reinterpret_cast<float *>(ws + L.scores);
+    sc.score_stride = score_stride_for(a->q.max_pools);
+    sc.workspace = ws + L.scratch;
+    sc.workspace_bytes = L.total - L.scratch;
+    sc.d_status = a->d_status;
+
+    kp_topk_args tk;
+    std::memset(&tk, 0, sizeof tk);
+    tk.cfg = a->cfg;
+    tk.q = a->q;
+    tk.scores = sc.scores;
+    tk.score_stride = sc.score_stride;
+    tk.pool_idx = a->pool_idx ? a->pool_idx : reinterpret_cast<int32_t *>(ws + L.pool_idx);
+    tk.n_sel = a->n_sel ? a->n_sel : reinterpret_cast<int32_t *>(ws + L.n_sel);
+    tk.d_status = a->d_status;
+
+    kp_attend_args at;
+    std::memset(&at, 0, sizeof at);
+    at.cfg = a->cfg;
+    at.seqs = a->seqs;
+    at.q = a->q;
+    at.q_lat = a->q_lat;
+    at.latent = a->latent;
+    at.pool_idx = tk.pool_idx;
+    at.n_sel = tk.n_sel;
+    at.out = a->out;
+    at.lse = a->lse;
+    at.workspace = ws + L.scratch;
+    at.workspace_bytes = L.total - L.scratch;
+    at.d_status = a->d_status;
+
+    if ((st = kp_kpool_compress(&c, stream)) != KP_OK) return st;
+    if ((st = kp_indexer_score(&sc, stream)) != KP_OK) return st;
+    if ((st = kp_topk_select(&tk, stream)) != KP_OK) return st;
+    return kp_sparse_mla_attend(&at, stream);
+}
+
+const char *kp_status_string(kp_status s) {
+    switch (s) {
+        case KP_OK: return "ok";
+        case KP_ERR_INVALID_ARG: return "invalid argument";
+        case KP_ERR_UNSUPPORTED: return "unsupported shape or option";
+        case KP_ERR_CUDA: return "CUDA error";
+        case KP_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+        case KP_ERR_DEVICE_BOUNDS: return "device index out of range";
+        case KP_ERR_WORKSPACE: return "workspace missing or too small";
+    }
+    return "unknown status";
+}
+
+const char *kp_last_error(void) { return g_last_error.c_str(); }
+
+kp_status kp_read_device_status(const int32_t *d_status, kp_stream_t stream) {
+    if (!d_status) return KP_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int32_t v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, d_status, sizeof v, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) {
+        record_cuda_error("kp_read_device_status", e);
+        return KP_ERR_CUDA;
+    }
+    return static_cast<kp_status>(v);
+}
+
+int kp_version(void) { return 100; }
+
+}  // extern "C"

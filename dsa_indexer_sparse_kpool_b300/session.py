@@ -1,0 +1,187 @@
+"""Device state of one DSA layer for a batch of sequences, driven through the C ABI.
+
+A ``Session`` owns the latent (MLA) cache, the pooled indexer cache, the tail
+rings and the per-sequence bookkeeping on one CUDA device, and runs steps with
+``kp_dsa_forward`` (or the four stage calls).  It moves data and fills the
+argument structs; all arithmetic of the step runs in libkpool_dsa.so.
+"""
+from __future__ import annotations
+
+from typing import Optional, Sequence
+
+import torch
+
+from . import (Config, Queries, Seqs, forward_args, kp_dsa_forward, kp_indexer_score, kp_kpool_compress,
+               kp_score_workspace_size, kp_attend_workspace_size, kp_sparse_mla_attend, kp_topk_select,
+               kp_workspace_size, score_stride, INDEX_DIM, MLA_HEADS, NOPE_DIM)
+
+
+def _dev_i32(x, device):
+    return torch.as_tensor(x, dtype=torch.int32).to(device).contiguous()
+
+
+def _dev_i64(x, device):
+    return torch.as_tensor(x, dtype=torch.int64).to(device).contiguous()
+
+
+class Session:
+    """Caches of B sequences.
+
+    latent       [rows, 576] bf16, sequence b at rows latent_row_off[b] + position
+    keys, gates  [rows, 128] bf16 raw per-token indexer keys / gate logits laid out
+                 like the latent rows (kept on the host side of the caller; only the
+                 rows a step appends are uploaded per step)
+    pool_row_off first pooled-cache row of each sequence; pool_rows = capacity
+    """
+
+    def __init__(self, cfg: Config, lens: Sequence[int], latent_row_off: Sequence[int],
+                 pool_row_off: Sequence[int], pool_rows: int, latent: torch.Tensor, ape: torch.Tensor,
+                 device="cuda"):
+        self.cfg = cfg
+        self.device = torch.device(device)
+        self.B = len(lens)
+        self.lens = [int(x) for x in lens]
+        self.latent_row_off_h = [int(x) for x in latent_row_off]
+        self.pool_row_off_h = [int(x) for x in pool_row_off]
+        self.latent = latent.to(self.device).contiguous()
+        self.ape = ape.to(self.device).contiguous()
+        self.pooled = torch.zeros(pool_rows, INDEX_DIM, dtype=torch.bfloat16, device=self.device)
+        R = cfg.kpool - 1
+        self.tail_keys = torch.zeros(self.B, R, INDEX_DIM, dtype=torch.bfloat16, device=self.device)
+        self.tail_gates = torch.zeros(self.B, R, INDEX_DIM, dtype=torch.bfloat16, device=self.device)
+        self.seq_len = _dev_i32(self.lens, self.device)
+        self.latent_row_off = _dev_i64(self.latent_row_off_h, self.device)
+        self.pool_row_off = _dev_i64(self.pool_row_off_h, self.device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
+
+    def seqs(self) -> Seqs:
+        return Seqs(self.seq_len, self.latent_row_off, self.pool_row_off, self.latent.shape[0],
+                    self.pooled.shape[0])
+
+    def append(self, prev_len: Sequence[int], new_counts: Sequence[int], keys: torch.Tensor,
+               gates: Optional[torch.Tensor], stream=None) -> None:
+        """Appends new tokens' indexer keys (CSR by sequence) through kp_kpool_compress."""
+        new_off = [0]
+        for n in new_counts:
+            new_off.append(new_off[-1] + int(n))
+        keys = keys.to(self.device).contiguous()
+        gates = gates.to(self.device).contiguous() if gates is not None else None
+        kp_kpool_compress(self.cfg, _dev_i32(list(prev_len), self.device), _dev_i32(new_off, self.device),
+                          keys, gates, self.ape, self.tail_keys, self.tail_gates, self.pooled, self.pool_row_off,
+                          max(1, max(int(n) for n in new_counts)), d_status=self.status, stream=stream)
+
+
+class Step:
+    """Device buffers and argument struct of one kp_dsa_forward call."""
+
+    def __init__(self, sess: Session, prev_len: Sequence[int], new_counts: Sequence[int], new_keys: torch.Tensor,
+                 new_gates: torch.Tensor, q_seq: Sequence[int], q_pos: Sequence[int], q_idx: torch.Tensor,
+                 w: torch.Tensor, q_lat: torch.Tensor, max_pools: Optional[int] = None):
+        d = sess.device
+        self.sess = sess
+        cfg = sess.cfg
+        NQ = len(q_seq)
+        self.prev_len = _dev_i32(list(prev_len), d)
+        off = [0]
+        for n in new_counts:
+            off.append(off[-1] + int(n))
+        self.new_off = _dev_i32(off, d)
+        self.max_new = max(1, max(int(n) for n in new_counts)) if len(new_counts) else 1
+        self.keys = new_keys.to(d).contiguous()
+        self.gates = new_gates.to(d).contiguous()
+        if max_pools is None:
+            max_pools = max((int(t) + 1) // cfg.kpool for t in q_pos) if NQ else 0
+        self.queries = Queries(_dev_i32(list(q_seq), d), _dev_i32(list(q_pos), d), int(max_pools))
+        self.q_idx = q_idx.to(d).contiguous()
+        self.w = w.to(d).contiguous()
+        self.q_lat = q_lat.to(d).contiguous()
+        self.out = torch.empty(NQ, MLA_HEADS, NOPE_DIM, dtype=torch.bfloat16, device=d)
+        self.lse = torch.empty(NQ, MLA_HEADS, dtype=torch.float32, device=d)
+        self.pool_idx = torch.empty(NQ, cfg.k_pools, dtype=torch.int32, device=d)
+        self.n_sel = torch.empty(NQ, dtype=torch.int32, device=d)
+        self.seqs = sess.seqs()
+        args = self._args(None)
+        ws = kp_workspace_size(args)
+        self.workspace = torch.empty(ws, dtype=torch.uint8, device=d)
+        self.args = self._args(self.workspace)
+
+    def _args(self, workspace):
+        s = self.sess
+        return forward_args(s.cfg, self.seqs, self.queries, prev_len=self.prev_len, new_off=self.new_off,
+                            max_new_per_seq=self.max_new, keys=self.keys, gates=self.gates, ape=s.ape,
+                            tail_keys=s.tail_keys, tail_gates=s.tail_gates, pooled=s.pooled, q_idx=self.q_idx,
+                            w=self.w, q_lat=self.q_lat, latent=s.latent, out=self.out, lse=self.lse,
+                            pool_idx=self.pool_idx, n_sel=self.n_sel, workspace=workspace, d_status=s.status)
+
+    def run(self, stream=None) -> None:
+        kp_dsa_forward(self.args, stream=stream)
+
+    def stage_calls(self):
+        """The four stage calls on persistent buffers (capturable one by one):
+        [compress, score, topk, attend]; returns (calls, scores tensor)."""
+        s, cfg = self.sess, self.sess.cfg
+        NQ = self.queries.q_seq.numel()
+        if not hasattr(self, "_stage_bufs"):
+            stride = score_stride(self.queries.max_pools)
+            self._stage_bufs = (
+                torch.empty(NQ, stride, dtype=torch.float32, device=s.device),
+                torch.empty(kp_score_workspace_size(NQ), dtype=torch.uint8, device=s.device),
+                torch.empty(max(256, kp_attend_workspace_size(cfg, NQ)), dtype=torch.uint8, device=s.device))
+        scores, ws, aws = self._stage_bufs
+        calls = [
+            lambda: kp_kpool_compress(cfg, self.prev_len, self.new_off, self.keys, self.gates, s.ape, s.tail_keys,
+                                      s.tail_gates, s.pooled, s.pool_row_off, self.max_new, d_status=s.status),
+            lambda: kp_indexer_score(cfg, self.seqs, self.queries, self.q_idx, self.w, s.pooled, scores, ws,
+                                     d_status=s.status),
+            lambda: kp_topk_select(cfg, self.queries, scores, self.pool_idx, self.n_sel, d_status=s.status),
+            lambda: kp_sparse_mla_attend(cfg, self.seqs, self.queries, self.q_lat, s.latent, self.pool_idx,
+                                         self.n_sel, self.out, self.lse, aws, d_status=s.status),
+        ]
+        return calls, scores
+
+    # ---- the four stages one by one (same buffers), for stage-level checks
+    def run_stages(self, stream=None):
+        s, cfg = self.sess, self.sess.cfg
+        kp_kpool_compress(cfg, self.prev_len, self.new_off, self.keys, self.gates, s.ape, s.tail_keys,
+                          s.tail_gates, s.pooled, s.pool_row_off, self.max_new, d_status=s.status, stream=stream)
+        NQ = self.queries.q_seq.numel()
+        stride = score_stride(self.queries.max_pools)
+        scores = torch.empty(NQ, stride, dtype=torch.float32, device=s.device)
+        ws = torch.empty(kp_score_workspace_size(NQ), dtype=torch.uint8, device=s.device)
+        kp_indexer_score(cfg, self.seqs, self.queries, self.q_idx, self.w, s.pooled, scores, ws,
+                         d_status=s.status, stream=stream)
+        kp_topk_select(cfg, self.queries, scores, self.pool_idx, self.n_sel, d_status=s.status, stream=stream)
+        aws = torch.empty(max(256, kp_attend_workspace_size(cfg, NQ)), dtype=torch.uint8, device=s.device)
+        kp_sparse_mla_attend(cfg, self.seqs, self.queries, self.q_lat, s.latent, self.pool_idx, self.n_sel,
+                             self.out, self.lse, aws, d_status=s.status, stream=stream)
+        return scores
+
+
+def _ranges(starts, ends):
+    parts = [torch.arange(int(s), int(e), dtype=torch.int64) for s, e in zip(starts, ends)]
+    return torch.cat(parts) if parts else torch.zeros(0, dtype=torch.int64)
+
+
+def build_session(cfg: Config, lens, prev_len, tok_off, pool_off, pool_rows: int, latent: torch.Tensor,
+                  keys: torch.Tensor, gates: torch.Tensor, ape: torch.Tensor, device="cuda") -> Session:
+    """Session whose caches hold positions [0, prev_len[b]) of each sequence.
+
+    `keys`, `gates` and `latent` are per-token arrays laid out like the latent
+    cache (sequence b at rows tok_off[b] + position).  The pooled cache and the
+    tail rings are built on the device by kp_kpool_compress."""
+    sess = Session(cfg, lens, tok_off, pool_off, pool_rows, latent, ape, device)
+    B = len(lens)
+    idx = _ranges([tok_off[b] for b in range(B)], [tok_off[b] + prev_len[b] for b in range(B)])
+    if idx.numel():
+        sess.append([0] * B, [int(p) for p in prev_len], keys[idx], gates[idx])
+    return sess
+
+
+def build_step(sess: Session, lens, prev_len, tok_off, keys: torch.Tensor, gates: torch.Tensor, q_seq, q_pos,
+               q_idx, w, q_lat, max_pools=None) -> Step:
+    """Step that appends positions [prev_len[b], lens[b]) and runs the queries."""
+    B = len(lens)
+    idx = _ranges([tok_off[b] + prev_len[b] for b in range(B)], [tok_off[b] + lens[b] for b in range(B)])
+    counts = [int(lens[b]) - int(prev_len[b]) for b in range(B)]
+    return Step(sess, [int(p) for p in prev_len], counts, keys[idx], gates[idx], [int(x) for x in q_seq],
+                [int(x) for x in q_pos], q_idx, w, q_lat, max_pools)

@@ -1,0 +1,281 @@
+/*
+ * kpool_dsa.h -- C ABI of the KPool DSA sparse-attention step (sm_103a).
+ *
+ * One DSA layer step of the GLM-5.3-Flash hybrid decoder, in four stages:
+ *
+ *   1. kp_kpool_compress     pool every run of `kpool` (4) consecutive indexer
+ *                            keys into one pooled key and append it to the
+ *                            pooled indexer cache; keep the rows of the
+ *                            still-incomplete pool in a per-sequence tail ring.
+ *                            (MAX docs, max.pipelines.architectures.glm5_next,
+ *                            Glm5NextConfig.index_kpool / index_kpool_compress;
+ *                            llama.cpp PR "add GLM-5.3-Flash (GLM5-Next)
+ *                            support", Overview: pools of 4 consecutive tokens,
+ *                            per-token key | gate.)
+ *   2. kp_indexer_score      lightning-indexer score of every complete pool a
+ *                            query can see: s = sum_h w_h * ReLU(q_h . k_pool),
+ *                            32 heads x 128 dims (llm-atlas GLM-5.3-Flash card,
+ *                            raw config index_n_heads / index_head_dim).
+ *   3. kp_topk_select        the index_topk / kpool best pools per query
+ *                            (2048 tokens = 512 pools; llm-atlas card,
+ *                            index_topk), ascending pool order.
+ *   4. kp_sparse_mla_attend  nope-only MLA in latent space over the selected
+ *                            pools' rows plus the query's incomplete tail pool
+ *                            (MAX docs Glm5NextConfig.index_kpool_always_select_tail,
+ *                            mla_use_nope; Glm5Next.build_layers: 576-wide
+ *                            latent rows whose last 64 columns are zero).
+ *
+ *   kp_dsa_forward runs 1-4 in order on one stream.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every pointer in an args struct is a DEVICE pointer unless marked
+ *    "host".  The args struct itself is read on the host during the call
+ *    and may be freed when the call returns.
+ *  - bf16 tensors are passed as `uint16_t*` holding bf16 bit patterns.
+ *  - The caller owns every buffer.  The library allocates no device or host
+ *    memory per call (a tensor-map descriptor is built on the host stack),
+ *    frees nothing, and never synchronises the stream, except
+ *    kp_read_device_status.
+ *  - All work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) in order.  Calls are graph-capturable.  Calls on different
+ *    streams that share output or workspace buffers race.
+ *  - Host-side validation runs before any launch.  A call that returns an
+ *    error other than KP_ERR_CUDA has enqueued nothing.
+ *  - `d_status` (optional, may be NULL) is a device int32 the kernels set to
+ *    a kp_status code when they detect bad data (an out-of-range pool index
+ *    or cache row); the offending element is skipped, never dereferenced.
+ *    The library never clears it: zero it before the calls you want to check.
+ *  - Fixed shapes (compile-time): indexer 32 heads x 128 dims; MLA 64 heads
+ *    over latent rows of 576 bf16 of which the first 512 are read; kpool 4.
+ *    Anything else returns KP_ERR_UNSUPPORTED.
+ *
+ * Query positions and visibility
+ * ------------------------------
+ *  A query q belongs to sequence q_seq[q] and sits at absolute position
+ *  t = q_pos[q] (0-based, t < seq_len of that sequence).  It sees the
+ *  n_full(t) = floor((t + 1) / kpool) complete pools of its sequence; its tail
+ *  is positions kpool * n_full(t) .. t (empty when (t + 1) % kpool == 0),
+ *  always attended when always_select_tail, and never scored.  Decode, MTP
+ *  verification and chunked causal prefill differ only in these arrays.
+ */
+#ifndef KPOOL_DSA_H
+#define KPOOL_DSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define KP_API __attribute__((visibility("default")))
+#else
+#define KP_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t without including the CUDA headers. */
+typedef struct CUstream_st *kp_stream_t;
+
+typedef enum kp_status {
+    KP_OK = 0,
+    KP_ERR_INVALID_ARG = 1,     /* null pointer, negative size, inconsistent sizes */
+    KP_ERR_UNSUPPORTED = 2,     /* shape or option this build does not implement */
+    KP_ERR_CUDA = 3,            /* a CUDA runtime or driver call failed (see kp_last_error) */
+    KP_ERR_DEVICE_TIMEOUT = 4,  /* a kernel's bounded wait ran out (device status) */
+    KP_ERR_DEVICE_BOUNDS = 5,   /* a kernel met an out-of-range index (device status) */
+    KP_ERR_WORKSPACE = 6        /* workspace missing or smaller than required */
+} kp_status;
+
+enum {
+    KP_INDEX_HEADS = 32,   /* lightning-indexer heads */
+    KP_INDEX_DIM = 128,    /* indexer key / query width */
+    KP_MLA_HEADS = 64,     /* attention heads */
+    KP_LATENT_DIM = 576,   /* latent cache row width (bf16) */
+    KP_NOPE_DIM = 512,     /* latent columns read (kv_lora_rank); 512..575 are zero */
+    KP_KPOOL = 4,          /* tokens per pool */
+    KP_MAX_TOPK_POOLS = 1024,    /* largest supported topk_tokens / kpool */
+    KP_MAX_SCORE_POOLS = 262144  /* largest supported pools per query (1,048,576 tokens) */
+};
+
+enum { KP_COMPRESS_LEARNED = 0, KP_COMPRESS_MEAN = 1 };
+
+/* Method options. */
+typedef struct kp_config {
+    int32_t kpool;              /* tokens per pool; must be 4 */
+    int32_t topk_tokens;        /* token budget of the top-k (index_topk, 2048); a
+                                   positive multiple of kpool, <= 4 * KP_MAX_TOPK_POOLS */
+    int32_t compress_mode;      /* KP_COMPRESS_LEARNED (gate + ape softmax) or _MEAN */
+    int32_t always_select_tail; /* 1: the query's incomplete pool is always attended */
+    float sm_scale;             /* attention logit scale (1/16 = 1/sqrt(qk_head_dim 256)) */
+} kp_config;
+
+/* Per-sequence cache layout.  Sequence b's latent rows are rows
+ * latent_row_off[b] .. + seq_len[b] - 1 of the latent cache (row i = token
+ * position i), and its pooled keys are rows pool_row_off[b] + p of the pooled
+ * cache (p = pool index).  Both caches are single buffers shared by all
+ * sequences. */
+typedef struct kp_seqs {
+    int32_t num_seqs;                /* host: B >= 1 */
+    const int32_t *seq_len;          /* [B] tokens in the caches, after this step's appends */
+    const int64_t *latent_row_off;   /* [B] */
+    const int64_t *pool_row_off;     /* [B] */
+    int64_t latent_rows;             /* host: rows allocated in the latent cache */
+    int64_t pool_rows;               /* host: rows allocated in the pooled cache */
+} kp_seqs;
+
+/* The query tokens of this step, flattened over sequences.  Queries of one
+ * sequence should be adjacent (any order is correct; adjacency lets the
+ * scorer share pooled-key tiles between them). */
+typedef struct kp_queries {
+    int32_t num_queries;        /* host: NQ >= 0 */
+    const int32_t *q_seq;       /* [NQ] sequence of each query */
+    const int32_t *q_pos;       /* [NQ] absolute position of each query */
+    int32_t max_pools;          /* host: an upper bound of n_full(q_pos) over the queries,
+                                   <= KP_MAX_SCORE_POOLS */
+} kp_queries;
+
+/* ---- 1. pooled-key compression (fused into the indexer-cache write) ---- */
+/* For sequence b the new tokens are positions prev_len[b] .. prev_len[b] +
+ * n_b - 1 with n_b = new_off[b+1] - new_off[b]; their raw indexer key and gate
+ * rows are rows new_off[b] .. new_off[b+1]-1 of `keys` / `gates`.  Every pool
+ * the new tokens complete is written to the pooled cache:
+ *   logit_i[d] = gate[kpool*p + i][d] + ape[i][d],  alpha = softmax_i(logit)
+ *   pooled[p][d] = bf16_rne( sum_i alpha_i[d] * key[kpool*p + i][d] )
+ * (mean mode: alpha_i = 1/kpool), fp32 arithmetic.  Rows of a pool that is
+ * still incomplete after the step go to the tail ring, slot = position %
+ * kpool; rows of older positions of a completing pool are read from there.
+ * The ring must hold the rows of positions kpool*floor(prev_len/kpool) ..
+ * prev_len-1 on entry (any content when that range is empty). */
+typedef struct kp_compress_args {
+    kp_config cfg;
+    int32_t num_seqs;             /* host: B */
+    const int32_t *prev_len;      /* [B] tokens already appended before this call */
+    const int32_t *new_off;       /* [B+1] CSR offsets into keys/gates; new_off[0] = 0 */
+    int32_t num_new;              /* host: total new tokens = new_off[B] */
+    int32_t max_new_per_seq;      /* host: an upper bound of n_b */
+    const uint16_t *keys;         /* [num_new][128] bf16 */
+    const uint16_t *gates;        /* [num_new][128] bf16 (unused in mean mode, may be NULL) */
+    const uint16_t *ape;          /* [kpool][128] bf16 (unused in mean mode, may be NULL) */
+    uint16_t *tail_keys;          /* [B][kpool-1][128] bf16, in/out */
+    uint16_t *tail_gates;         /* [B][kpool-1][128] bf16, in/out */
+    uint16_t *pooled;             /* [pool_rows][128] bf16, out (completed pools only) */
+    const int64_t *pool_row_off;  /* [B] */
+    int64_t pool_rows;            /* host */
+    int32_t *d_status;            /* optional */
+} kp_compress_args;
+
+/* ---- 2. indexer scores ---- */
+/* scores[q][p] = sum_h w[q][h] * max(0, sum_d q_idx[q][h][d] * pooled[row(p)][d])
+ * for p < n_full(q_pos[q]), fp32 (bf16 products, fp32 accumulation).  Entries
+ * n_full .. the next multiple of 128 are set to -inf; later entries of the
+ * row are left as they were. */
+typedef struct kp_score_args {
+    kp_config cfg;
+    kp_seqs seqs;                 /* uses num_seqs, pool_row_off, pool_rows */
+    kp_queries q;
+    const uint16_t *q_idx;        /* [NQ][32][128] bf16 */
+    const float *w;               /* [NQ][32] fp32 head weights */
+    const uint16_t *pooled;       /* [pool_rows][128] bf16 */
+    float *scores;                /* [NQ][score_stride] fp32, out */
+    int64_t score_stride;         /* host: >= max_pools rounded up to 128 */
+    void *workspace;              /* >= kp_score_workspace_size(NQ) bytes, 256-aligned */
+    size_t workspace_bytes;
+    int32_t *d_status;
+} kp_score_args;
+
+/* ---- 3. top-k pool selection ---- */
+/* For each query with n = n_full(q_pos[q]) and K = topk_tokens / kpool:
+ * n_sel[q] = min(K, n); pool_idx[q][0 .. n_sel) = the selected pools in
+ * ascending order (all pools when n <= K, else the K largest scores, ties to
+ * the lower index; -0 equals +0; NaN ranks lowest); pool_idx[q][n_sel .. K)
+ * = -1. */
+typedef struct kp_topk_args {
+    kp_config cfg;
+    kp_queries q;
+    const float *scores;          /* [NQ][score_stride] */
+    int64_t score_stride;         /* host */
+    int32_t *pool_idx;            /* [NQ][K] out */
+    int32_t *n_sel;               /* [NQ] out */
+    int32_t *d_status;
+} kp_topk_args;
+
+/* ---- 4. sparse MLA over the selected pools + tail ---- */
+/* Token set of query q: rows kpool*p .. kpool*p + kpool-1 of every selected
+ * pool p, then the tail positions (when always_select_tail).  For head h:
+ *   z_s = sm_scale * sum_{d<512} q_lat[q][h][d] * latent[row_s][d]
+ *   out[q][h][:] = sum_s softmax(z)_s * latent[row_s][0..512)   (bf16, RNE)
+ *   lse[q][h] = ln sum_s exp(z_s)                                (fp32)
+ * An empty token set gives out = 0 and lse = -inf. */
+typedef struct kp_attend_args {
+    kp_config cfg;
+    kp_seqs seqs;                 /* uses latent_row_off, latent_rows */
+    kp_queries q;
+    const uint16_t *q_lat;        /* [NQ][64][576] bf16 (columns 512.. ignored) */
+    const uint16_t *latent;       /* [latent_rows][576] bf16 */
+    const int32_t *pool_idx;      /* [NQ][K] */
+    const int32_t *n_sel;         /* [NQ] */
+    uint16_t *out;                /* [NQ][64][512] bf16 out */
+    float *lse;                   /* [NQ][64] fp32 out (may be NULL) */
+    void *workspace;              /* >= kp_attend_workspace_size(...) bytes */
+    size_t workspace_bytes;
+    int32_t *d_status;
+} kp_attend_args;
+
+/* ---- the whole step ---- */
+typedef struct kp_forward_args {
+    kp_config cfg;
+    kp_seqs seqs;
+    kp_queries q;
+    /* stage 1 inputs (see kp_compress_args) */
+    const int32_t *prev_len;
+    const int32_t *new_off;
+    int32_t num_new;
+    int32_t max_new_per_seq;
+    const uint16_t *keys;
+    const uint16_t *gates;
+    const uint16_t *ape;
+    uint16_t *tail_keys;
+    uint16_t *tail_gates;
+    uint16_t *pooled;             /* pooled cache, in/out */
+    /* stage 2-4 inputs */
+    const uint16_t *q_idx;
+    const float *w;
+    const uint16_t *q_lat;
+    const uint16_t *latent;
+    /* outputs */
+    uint16_t *out;                /* [NQ][64][512] bf16 */
+    float *lse;                   /* [NQ][64] fp32 (may be NULL) */
+    int32_t *pool_idx;            /* [NQ][K] (may be NULL: kept in the workspace) */
+    int32_t *n_sel;               /* [NQ]    (may be NULL: kept in the workspace) */
+    void *workspace;              /* >= kp_workspace_size(args) bytes */
+    size_t workspace_bytes;
+    int32_t *d_status;
+} kp_forward_args;
+
+KP_API kp_status kp_kpool_compress(const kp_compress_args *args, kp_stream_t stream);
+KP_API kp_status kp_indexer_score(const kp_score_args *args, kp_stream_t stream);
+KP_API kp_status kp_topk_select(const kp_topk_args *args, kp_stream_t stream);
+KP_API kp_status kp_sparse_mla_attend(const kp_attend_args *args, kp_stream_t stream);
+KP_API kp_status kp_dsa_forward(const kp_forward_args *args, kp_stream_t stream);
+
+/* Workspace sizes in bytes (0 never returned; sizes depend only on host fields). */
+KP_API size_t kp_score_workspace_size(int32_t num_queries);
+KP_API size_t kp_attend_workspace_size(const kp_config *cfg, int32_t num_queries);
+KP_API size_t kp_workspace_size(const kp_forward_args *args);
+
+/* Static text for a status code. */
+KP_API const char *kp_status_string(kp_status s);
+/* Text of the last KP_ERR_CUDA raised on the calling host thread ("" if none). */
+KP_API const char *kp_last_error(void);
+/* Synchronises `stream`, reads *d_status and returns it as a kp_status
+ * (debug / tests only). */
+KP_API kp_status kp_read_device_status(const int32_t *d_status, kp_stream_t stream);
+/* Library version: major * 10000 + minor * 100 + patch. */
+KP_API int kp_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KPOOL_DSA_H */

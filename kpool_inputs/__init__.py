@@ -19,8 +19,9 @@ last 64 columns are zero):
 Distributions: indexer q and k ~ N(0,1)/sqrt(128); gate ~ N(0,1);
 ape ~ N(0, 0.1^2); head weights w ~ N(0,1)/sqrt(32); MLA q_lat and latent
 columns 0..511 ~ N(0,1)/sqrt(576); latent columns 512..575 = 0; q_lat columns
-512..575 = 0 unless ``q_rope_random``.  All draws come from one seeded
-``torch.Generator`` on the CPU in a fixed order, then round to bf16.
+512..575 = 0 unless ``q_rope_random``.  All draws come from seeded
+numpy PCG64 streams (one SeedSequence per array, chunks spawned from it), then
+round to bf16 (nearest even).
 The queries of a sequence are its last n_q positions and are also the tokens
 appended to the caches in this step (n_new = n_q).
 """
@@ -28,6 +29,8 @@ from __future__ import annotations
 
 import dataclasses
 import math
+import os
+from concurrent.futures import ThreadPoolExecutor
 from typing import List, Optional
 
 import numpy as np
@@ -75,8 +78,42 @@ def named(name: str) -> Spec:
 NAMES = ("tiny", "decode", "ragged", "prefill", "long")
 
 
-def _randn(g: torch.Generator, shape, std: float) -> torch.Tensor:
-    return (torch.randn(*shape, generator=g, dtype=torch.float32) * std).to(torch.bfloat16)
+_THREADS = max(1, min(16, os.cpu_count() or 1))
+_CHUNK = 1 << 22
+
+
+def _normal_bf16_into(out_u16: np.ndarray, seed: int, tag: int, std: float) -> None:
+    """Fills a 2-D uint16 array (or a column slice of one) with bf16 bit patterns of
+    N(0, std^2) draws.  Each chunk of rows has its own PCG64 stream spawned from
+    SeedSequence([seed, tag]), so the values do not depend on the thread count."""
+    rows, cols = out_u16.shape
+    rows_per = max(1, _CHUNK // max(cols, 1))
+    starts = list(range(0, rows, rows_per))
+    kids = np.random.SeedSequence([seed, tag]).spawn(len(starts))
+
+    def work(i):
+        a = starts[i]
+        b = min(rows, a + rows_per)
+        g = np.random.Generator(np.random.PCG64(kids[i]))
+        x = g.standard_normal((b - a, cols), dtype=np.float32)
+        x *= np.float32(std)
+        u = x.view(np.uint32)
+        u += ((u >> 16) & 1) + 0x7FFF          # round to nearest even at bit 16
+        out_u16[a:b] = (u >> 16).astype(np.uint16)
+
+    with ThreadPoolExecutor(_THREADS) as ex:
+        list(ex.map(work, range(len(starts))))
+
+
+def _bf16(u16: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(u16.view(np.int16)).view(torch.bfloat16)
+
+
+def _randn(seed: int, tag: int, shape, std: float) -> torch.Tensor:
+    rows = int(np.prod(shape[:-1])) if len(shape) > 1 else 1
+    u = np.empty((rows, shape[-1]), np.uint16)
+    _normal_bf16_into(u, seed, tag, std)
+    return _bf16(u).reshape(*shape)
 
 
 def _round_up(x: int, m: int) -> int:
@@ -128,11 +165,11 @@ class Workload:
 
 
 def make(spec: Spec) -> Workload:
-    g = torch.Generator().manual_seed(spec.seed)
     if spec.lens is None:
+        g = np.random.Generator(np.random.PCG64(np.random.SeedSequence([spec.seed, 0])))
         lens = []
         while len(lens) < spec.ragged_b:
-            L = int(torch.randint(spec.ragged_lo, spec.ragged_hi + 1, (1,), generator=g).item())
+            L = int(g.integers(spec.ragged_lo, spec.ragged_hi + 1))
             if L % spec.kpool != 0:
                 lens.append(L)
     else:
@@ -157,19 +194,21 @@ def make(spec: Spec) -> Workload:
     total = int(lens_a.astype(np.int64).sum())
     NQ = int(nq_a.sum())
 
-    keys = _randn(g, (total, INDEX_DIM), 1.0 / math.sqrt(INDEX_DIM))
-    gates = _randn(g, (total, INDEX_DIM), 1.0)
-    ape = _randn(g, (spec.kpool, INDEX_DIM), 0.1)
-    latent = torch.zeros(total, LATENT_DIM, dtype=torch.bfloat16)
-    latent[:, :NOPE_DIM] = _randn(g, (total, NOPE_DIM), 1.0 / math.sqrt(LATENT_DIM))
-    q_idx = _randn(g, (NQ, INDEX_HEADS, INDEX_DIM), 1.0 / math.sqrt(INDEX_DIM))
-    w = torch.randn(NQ, INDEX_HEADS, generator=g, dtype=torch.float32) / math.sqrt(INDEX_HEADS)
-    q_lat = torch.zeros(NQ, MLA_HEADS, LATENT_DIM, dtype=torch.bfloat16)
-    q_main = torch.randn(NQ, MLA_HEADS, NOPE_DIM, generator=g, dtype=torch.float32) / math.sqrt(LATENT_DIM)
-    q_lat[:, :, :NOPE_DIM] = (q_main * spec.q_scale).to(torch.bfloat16)
-    rope = _randn(g, (NQ, MLA_HEADS, LATENT_DIM - NOPE_DIM), 1.0 / math.sqrt(LATENT_DIM))
+    sd = spec.seed
+    keys = _randn(sd, 1, (total, INDEX_DIM), 1.0 / math.sqrt(INDEX_DIM))
+    gates = _randn(sd, 2, (total, INDEX_DIM), 1.0)
+    ape = _randn(sd, 3, (spec.kpool, INDEX_DIM), 0.1)
+    lat = np.zeros((total, LATENT_DIM), np.uint16)
+    _normal_bf16_into(lat[:, :NOPE_DIM], sd, 4, 1.0 / math.sqrt(LATENT_DIM))
+    latent = _bf16(lat)
+    q_idx = _randn(sd, 5, (NQ, INDEX_HEADS, INDEX_DIM), 1.0 / math.sqrt(INDEX_DIM))
+    w = torch.from_numpy(np.random.Generator(np.random.PCG64(np.random.SeedSequence([sd, 6])))
+                         .standard_normal((NQ, INDEX_HEADS), dtype=np.float32) / np.float32(math.sqrt(INDEX_HEADS)))
+    ql = np.zeros((NQ * MLA_HEADS, LATENT_DIM), np.uint16)
+    _normal_bf16_into(ql[:, :NOPE_DIM], sd, 7, spec.q_scale / math.sqrt(LATENT_DIM))
     if spec.q_rope_random:
-        q_lat[:, :, NOPE_DIM:] = rope
+        _normal_bf16_into(ql[:, NOPE_DIM:], sd, 8, 1.0 / math.sqrt(LATENT_DIM))
+    q_lat = _bf16(ql).reshape(NQ, MLA_HEADS, LATENT_DIM)
     return Workload(spec=spec, lens=lens_a, prev_len=prev, new_off=new_off, tok_off=tok_off,
                     pool_off=pool_off, pool_rows=pool_rows, q_seq=q_seq, q_pos=q_pos,
                     keys=keys, gates=gates, ape=ape, latent=latent, q_idx=q_idx, w=w, q_lat=q_lat)

@@ -1,0 +1,87 @@
+"""GPU parity of the four stages and the fused step against the fp64 oracle.
+
+Every test calls the library through its C ABI (ctypes binding) on seeded
+synthetic inputs and compares stage by stage (see parity_lib for the rules).
+"""
+import numpy as np
+import pytest
+import torch
+
+import kpool_inputs as KI
+import oracle
+import parity_lib as PL
+from dsa_indexer_sparse_kpool_b300 import COMPRESS_MEAN
+
+pytestmark = pytest.mark.gpu
+
+
+def small_spec(lens, n_q, topk_tokens=256, seed=11, **kw):
+    return KI.Spec("small", list(lens), list(n_q), topk_tokens=topk_tokens, seed=seed, **kw)
+
+
+def test_tiny_all_stages_and_fused():
+    wl = KI.make(KI.named("tiny"))
+    sess, step, rep = PL.full_check(wl)
+    # the fused call on fresh state gives the same bits as the staged calls
+    sess2, step2 = PL.make_gpu(wl)
+    step2.run()
+    torch.cuda.synchronize()
+    assert torch.equal(step2.pool_idx, step.pool_idx) and torch.equal(step2.n_sel, step.n_sel)
+    assert torch.equal(step2.out, step.out)
+    assert torch.equal(step2.lse, step.lse)
+    assert int(sess2.status.item()) == 0
+
+
+def test_tiny_end_to_end_against_oracle_pipeline():
+    wl = KI.make(KI.named("tiny"))
+    sess, step = PL.make_gpu(wl)
+    step.run()
+    torch.cuda.synchronize()
+    pooled, _ = oracle.kpool_compress(KI.bits(wl.keys), KI.bits(wl.gates), KI.bits(wl.ape), 4)
+    ref = oracle.dsa_queries(wl.q_seq, wl.q_pos, np.zeros(1, np.int64), np.zeros(1, np.int64), 4, wl.k_pools, 1,
+                             KI.bits(wl.q_idx), wl.w.numpy(), pooled, KI.bits(wl.q_lat), KI.bits(wl.latent),
+                             wl.spec.sm_scale)
+    g_idx = step.pool_idx.cpu().numpy()
+    assert np.array_equal(step.n_sel.cpu().numpy(), ref["n_sel"])
+    for q in range(wl.NQ):
+        if np.array_equal(g_idx[q], ref["sel"][q]):
+            PL.check_attend(step.out[q].float().cpu().numpy(), step.lse[q].cpu().numpy(), ref["out"][q], ref["lse"][q])
+
+
+@pytest.mark.parametrize("lens,n_q,topk", [
+    ([1000, 1537, 2050], [1, 3, 5], 256),      # several score tiles, ragged tails, active selection
+    ([515, 600], [9, 2], 128),                  # 9 queries of one sequence: two query groups
+    ([130], [4], 2048),                          # budget covers every pool
+    ([4099], [8], 64),                           # K = 16
+])
+def test_multi_tile_ragged(lens, n_q, topk):
+    wl = KI.make(small_spec(lens, n_q, topk))
+    PL.full_check(wl)
+
+
+def test_peaked_softmax_and_rope_columns():
+    spec = small_spec([777, 1203], [2, 3], 256, q_scale=16.0, q_rope_random=True)
+    wl = KI.make(spec)
+    PL.full_check(wl)
+
+
+def test_mean_mode_and_no_tail():
+    wl = KI.make(small_spec([901, 1026], [3, 2], 128))
+    cfg = PL.cfg_of(wl, compress_mode=COMPRESS_MEAN, always_select_tail=False)
+    PL.full_check(wl, cfg=cfg)
+
+
+def test_very_short_sequences():
+    # positions 0..3: n_full 0 or 1, tails of 1..3 tokens
+    wl = KI.make(small_spec([4, 3, 1, 6], [4, 3, 1, 2], 64))
+    PL.full_check(wl)
+
+
+def test_decode_config_sampled():
+    wl = KI.make(KI.named("decode"))
+    PL.full_check(wl, queries=[0, 13, 31], check_all_pooled=False)
+
+
+def test_ragged_config_sampled():
+    wl = KI.make(KI.named("ragged"))
+    PL.full_check(wl, queries=[0, 5, 15], check_all_pooled=False)
