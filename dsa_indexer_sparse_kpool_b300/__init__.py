@@ -20,7 +20,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libkpool_dsa.so")
 
 INDEX_HEADS, INDEX_DIM, MLA_HEADS, LATENT_DIM, NOPE_DIM, KPOOL = 32, 128, 64, 576, 512, 4
-MAX_TOPK_POOLS, MAX_SCORE_POOLS = 1024, 262144
+MAX_TOPK_POOLS, MAX_SCORE_POOLS, NOALLOC_MAX_QUERIES = 1024, 262144, 8192
 COMPRESS_LEARNED, COMPRESS_MEAN = 0, 1
 
 STATUS = {0: "KP_OK", 1: "KP_ERR_INVALID_ARG", 2: "KP_ERR_UNSUPPORTED", 3: "KP_ERR_CUDA",
@@ -77,7 +77,8 @@ class kp_forward_args(ctypes.Structure):
 
 
 EXPORTS = ("kp_kpool_compress", "kp_indexer_score", "kp_topk_select", "kp_sparse_mla_attend",
-           "kp_dsa_forward", "kp_score_workspace_size", "kp_attend_workspace_size", "kp_workspace_size",
+           "kp_dsa_forward", "kp_indexer_score_noalloc", "kp_score_workspace_size", "kp_attend_workspace_size",
+           "kp_workspace_size",
            "kp_status_string", "kp_last_error", "kp_read_device_status", "kp_version")
 
 _lib = None
@@ -91,6 +92,7 @@ def lib() -> ctypes.CDLL:
             raise RuntimeError("libkpool_dsa.so is not built: run `python -m dsa_indexer_sparse_kpool_b300.build`")
         L = ctypes.CDLL(LIB_PATH)
         for name, argt in (("kp_kpool_compress", kp_compress_args), ("kp_indexer_score", kp_score_args),
+                           ("kp_indexer_score_noalloc", kp_score_args),
                            ("kp_topk_select", kp_topk_args), ("kp_sparse_mla_attend", kp_attend_args),
                            ("kp_dsa_forward", kp_forward_args)):
             f = getattr(L, name)
@@ -210,6 +212,17 @@ def kp_indexer_score(cfg: Config, seqs: Seqs, queries: Queries, q_idx, w, pooled
     a = kp_score_args(cfg.c(), seqs.c(), queries.c(), _p(q_idx), _p(w), _p(pooled), _p(scores), scores.shape[1],
                       _p(workspace), workspace.numel() * workspace.element_size(), _p(d_status))
     _check(lib().kp_indexer_score(ctypes.byref(a), _stream(stream)), "kp_indexer_score")
+
+
+def kp_indexer_score_noalloc(cfg: Config, seqs: Seqs, queries: Queries, q_idx, w, pooled, scores,
+                             d_status=None, stream=None) -> None:
+    """kp_indexer_score without a workspace argument, for callers that cannot
+    allocate device memory: the work plan lives in a device array inside the
+    library (at most NOALLOC_MAX_QUERIES queries per call; calls that overlap
+    on the GPU share that array and race)."""
+    a = kp_score_args(cfg.c(), seqs.c(), queries.c(), _p(q_idx), _p(w), _p(pooled), _p(scores), scores.shape[1],
+                      None, 0, _p(d_status))
+    _check(lib().kp_indexer_score_noalloc(ctypes.byref(a), _stream(stream)), "kp_indexer_score_noalloc")
 
 
 def kp_topk_select(cfg: Config, queries: Queries, scores, pool_idx, n_sel, d_status=None, stream=None) -> None:

@@ -96,7 +96,8 @@ enum {
     KP_NOPE_DIM = 512,     /* latent columns read (kv_lora_rank); 512..575 are zero */
     KP_KPOOL = 4,          /* tokens per pool */
     KP_MAX_TOPK_POOLS = 1024,    /* largest supported topk_tokens / kpool */
-    KP_MAX_SCORE_POOLS = 262144  /* largest supported pools per query (1,048,576 tokens) */
+    KP_MAX_SCORE_POOLS = 262144, /* largest supported pools per query (1,048,576 tokens) */
+    KP_NOALLOC_MAX_QUERIES = 8192 /* largest num_queries of kp_indexer_score_noalloc */
 };
 
 enum { KP_COMPRESS_LEARNED = 0, KP_COMPRESS_MEAN = 1 };
@@ -259,6 +260,25 @@ KP_API kp_status kp_indexer_score(const kp_score_args *args, kp_stream_t stream)
 KP_API kp_status kp_topk_select(const kp_topk_args *args, kp_stream_t stream);
 KP_API kp_status kp_sparse_mla_attend(const kp_attend_args *args, kp_stream_t stream);
 KP_API kp_status kp_dsa_forward(const kp_forward_args *args, kp_stream_t stream);
+
+/* ---- scoring without a caller workspace ----
+ * The pages describe no such call: it exists for callers that cannot
+ * allocate device memory when they score (a host framework whose allocator
+ * forbids raw cudaMalloc, a plugin handed only its input and output buffers,
+ * a process whose memory budget is fixed before the first step).
+ * Same contract and results as kp_indexer_score, except that args->workspace
+ * and args->workspace_bytes are ignored: the work plan lives in a device
+ * array compiled into the library (about 128 KB, held by every GPU that loads
+ * the library until the process exits).  The call allocates nothing.
+ *  - num_queries > KP_NOALLOC_MAX_QUERIES returns KP_ERR_UNSUPPORTED and
+ *    launches nothing.
+ *  - The first call on a device looks up the array's device address with
+ *    that device current (cudaGetSymbolAddress) and caches it; make that
+ *    first call before any stream capture on the device.
+ *  - Every call shares the one array: calls whose kernels overlap on the GPU
+ *    (different streams, or different host threads, without ordering between
+ *    them) race and may produce wrong scores.  Calls in one stream are fine. */
+KP_API kp_status kp_indexer_score_noalloc(const kp_score_args *args, kp_stream_t stream);
 
 /* Workspace sizes in bytes (0 never returned; sizes depend only on host fields). */
 KP_API size_t kp_score_workspace_size(int32_t num_queries);

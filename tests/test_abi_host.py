@@ -100,3 +100,13 @@ def test_workspace_size_queries_need_no_gpu(L):
     args.q = kp.kp_queries(32, 0, 0, 8192)
     ws = L.kp_workspace_size(ctypes.byref(args))
     assert ws >= 32 * 8192 * 4 + 32 * 512 * 4
+
+
+def test_noalloc_score_rejects_too_many_queries_before_any_launch(L):
+    a = kp.kp_score_args()
+    a.cfg = _cfg()
+    a.seqs = kp.kp_seqs(1, 0x1000, 0x1000, 0x1000, 100, 100)
+    a.q = kp.kp_queries(kp.NOALLOC_MAX_QUERIES + 1, 0x1000, 0x1000, 64)
+    assert L.kp_indexer_score_noalloc(ctypes.byref(a), None) == 2
+    assert "KP_NOALLOC_MAX_QUERIES" in L.kp_last_error().decode()
+    assert L.kp_indexer_score_noalloc(None, None) == 1
