@@ -1,4 +1,5 @@
-// attend.cu -- nope-only sparse MLA in latent space over the selected pools.
+// attend.cu -- nope-only sparse MLA in latent space over the selected pools,
+// on tcgen05 tensor cores with TMEM accumulators.
 //
 // Method (MAX docs, max.pipelines.architectures.glm5_next: Glm5NextConfig
 // mla_use_nope -- no rotary embedding anywhere in the text decoder;
@@ -11,14 +12,36 @@
 // Only the 512 latent columns are read: the 64 rotary columns are zero by
 // the cache's contract, so they add nothing to the logits.
 //
-// Design (first version, legacy tensor-core path): one CTA = one query x one
-// split of its token list.  64-token tiles of latent rows are gathered with
-// cp.async (16 B chunks, XOR-swizzled rows) into a double-buffered ring;
-// 8 warps = 4 head groups (16 heads) x 2 halves of the 512 latent columns.
-// QK^T partial sums over each half are exchanged through shared memory,
-// online softmax in registers, P.V with the P fragments reused from the QK
-// accumulators.  Splits of one query write (o, lse) partials; the last CTA
-// to finish (atomic ticket, no waiting) merges them.
+// B300 design.  The 64 heads of a query share every latent row (MQA-like),
+// so heads are the natural N of the tensor-core products and the gathered
+// tokens their M:
+//   S^T[tok, h] = C[tok, :512] . Q[h, :512]^T     M = 128 tokens, N = 64, K = 512
+//   O^T[d, h]  += C[tok, d]^T . P[tok, h]          M = 128 latent columns (x4), N = 64, K = 128 tokens
+// One 128-token tile of latent rows (128 KB) is gathered into shared memory
+// in the 128-byte-swizzle layout; the S product reads it K-major, the P.V
+// product reads the same bytes M-major, so each latent row crosses HBM once.
+// S (64 TMEM columns) and O^T (4 x 64 columns) live in TMEM.  Each softmax
+// thread owns one token (one TMEM lane): per-head tile maxima come from one
+// warp redux per head plus a 4-warp exchange; the running max is raised only
+// when a tile's max exceeds it by 2^8 (then O^T and the row sums are rescaled),
+// so the correction pass almost never runs.
+//
+// A query's token list is split over the CTAs of a thread-block cluster
+// (up to 8).  After its tiles, each CTA dumps its unnormalised O^T, running
+// max and row sums to its own shared memory; after a cluster barrier, CTA r
+// merges heads [64r/S, 64(r+1)/S) across the cluster through distributed
+// shared memory, adds the <= 3 tail tokens (computed on CUDA cores, so the
+// tail never costs a tensor-core tile), normalises and writes bf16 out and
+// fp32 lse.  No global scratch, no second launch.
+//
+// Warp roles (384 threads, one CTA per SM):
+//   warps 0-7  softmax: warp w owns TMEM lane quadrant w % 4 (32 tokens) and
+//              heads 32 * (w / 4) .. +31; then the O^T dump
+//   warp 8     TMEM allocation, Q TMA, MMA issue (one lane)
+//   warps 9-11 gather: cp.async 16-byte pieces of the selected rows into the
+//              swizzled tile (each warp instruction moves two whole 256-byte
+//              row segments; warp g takes token pairs g, g+3, g+6, ...)
+//   all        cluster merge and output
 #include "kp_common.cuh"
 #include "kp_internal.h"
 
@@ -26,19 +49,59 @@ namespace kp {
 
 namespace {
 
-constexpr int kAtTile = 64;
-constexpr int kAtThreads = 256;
-constexpr int kAtRowBytes = kNopeDim * 2;             // 1024
-constexpr int kAtQBytes = kMlaHeads * kAtRowBytes;    // 64 KB
-constexpr int kAtKVBytes = kAtTile * kAtRowBytes;     // 64 KB per stage
-constexpr int kAtXBytes = 8 * 32 * 32 * 4;            // QK partial exchange, 32 KB
-constexpr int kAtRowsBytes = 2 * kAtTile * 8;
-constexpr int kAtSmemBytes = kAtQBytes + 2 * kAtKVBytes + kAtXBytes + kAtRowsBytes;
-constexpr float kLn2 = 0.69314718055994530942f;
-constexpr float kLog2e = 1.44269504088896340736f;
+constexpr int kAtTok = 128;                               // tokens per tile
+constexpr int kAtChunks = 4;                              // 128-column chunks of a latent row
+constexpr int kAtBlockBytes = kAtTok * 128;               // [128 rows][64 bf16] swizzle block
+constexpr int kAtChunkBytes = 2 * kAtBlockBytes;          // 32 KB
+constexpr int kAtTileBytes = kAtChunks * kAtChunkBytes;   // 128 KB
+constexpr int kAtQBlockBytes = kMlaHeads * 128;           // [64 heads][64 bf16] = 8 KB
+constexpr int kAtQBytes = 8 * kAtQBlockBytes;             // 64 KB
+constexpr int kAtPBytes = kAtTok * kMlaHeads * 2;         // 16 KB
+constexpr int kAtMaxSplits = 8;
+constexpr int kAtMaxTail = kKpool - 1;
+constexpr int kAtSoftWarps = 8;
+constexpr int kAtSoftThreads = 32 * kAtSoftWarps;
+constexpr int kAtMmaWarp = 8;
+constexpr int kAtProdWarp0 = 9;
+constexpr int kAtProdWarps = 3;
+constexpr int kAtProdThreads = 32 * kAtProdWarps;
+constexpr int kAtThreads = 384;
+constexpr int kAtTmemCols = 512;
+constexpr uint32_t kAtOCol = 0;                           // O^T: chunk c at columns 64c .. 64c+63
+constexpr uint32_t kAtSCol = 256;                         // S^T: 64 columns
+constexpr float kAtRescaleLog2 = 8.f;                     // raise the running max only past 2^8
+
+// Shared memory (offsets from a 1024-aligned base).
+constexpr int kOffQ = 0;
+constexpr int kOffTile = kOffQ + kAtQBytes;               // also the O dump [64][512] fp32
+constexpr int kOffP = kOffTile + kAtTileBytes;
+constexpr int kOffMisc = kOffP + kAtPBytes;
+constexpr int kMiscRed = 0;                               // [4][64] f32
+constexpr int kMiscMUsed = kMiscRed + 4 * 64 * 4;         // [64] f32 running max (log2 units)
+constexpr int kMiscFac = kMiscMUsed + 64 * 4;             // [64] f32 rescale factors of this tile
+constexpr int kMiscLSum = kMiscFac + 64 * 4;              // [64] f32 row sums
+constexpr int kMiscTail = kMiscLSum + 64 * 4;             // [3][512] bf16 tail rows
+constexpr int kMiscZTail = kMiscTail + kAtMaxTail * kNopeDim * 2;   // [64][4] f32 tail logits
+constexpr int kMiscW = kMiscZTail + 64 * 4 * 4;           // [64][16] f32 merge weights
+constexpr int kMiscBars = kMiscW + 64 * 16 * 4;           // mbarriers
+constexpr int kNumBars = 13;
+constexpr int kMiscTmem = kMiscBars + kNumBars * 8;
+constexpr int kMiscAbort = kMiscTmem + 4;
+constexpr int kMiscBytes = kMiscAbort + 12;
+constexpr int kAtSmemBytes = kOffMisc + kMiscBytes + 1024;  // + alignment slack
+static_assert(kAtSmemBytes <= 232448, "attention shared memory over the per-CTA limit");
+static_assert(kAtTileBytes >= kMlaHeads * kNopeDim * 4, "O dump must fit in the tile region");
+
+// mbarrier indices
+constexpr int kBarFull = 0;    // [4] chunk gathered (96 producer arrivals)
+constexpr int kBarFree = 4;    // [4] chunk consumed by P.V (tcgen05.commit)
+constexpr int kBarQ = 8;       // Q landed (TMA)
+constexpr int kBarS = 9;       // S^T ready (commit)
+constexpr int kBarP = 10;      // P written and O^T rescaled (256 softmax arrivals)
+constexpr int kBarO = 11;      // every MMA of the CTA done (commit)
+constexpr int kBarDrain = 12;  // teardown after an abort
 
 struct AttendParams {
-    const uint16_t *q_lat;
     const uint16_t *latent;
     int64_t latent_rows;
     const int32_t *q_seq;
@@ -52,40 +115,70 @@ struct AttendParams {
     float scale_log2;
     uint16_t *out;
     float *lse;
-    float *ws_o;
-    float *ws_lse;
-    int32_t *ws_cnt;
     int splits;
     int32_t *status;
 };
 
-__device__ __forceinline__ uint32_t swz(int row, int chunk) {
-    return static_cast<uint32_t>(row * kAtRowBytes + ((chunk ^ (row & 7)) << 4));
-}
-
 __device__ __forceinline__ void named_bar(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
+// Named barrier that also ANDs a flag over the participating threads, so a
+// failed wait in any of them makes all of them leave together.
+__device__ __forceinline__ bool named_bar_all(int id, int count, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.and.pred p, %2, %3, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
 
-__global__ void __launch_bounds__(kAtThreads, 1) sparse_mla_mma_kernel(AttendParams P) {
-    extern __shared__ __align__(128) uint8_t sm[];
-    __shared__ int s_last;
-    uint8_t *sQ = sm;
-    uint8_t *sKV = sm + kAtQBytes;
-    float *sX = reinterpret_cast<float *>(sm + kAtQBytes + 2 * kAtKVBytes);
-    int64_t *sRows = reinterpret_cast<int64_t *>(sm + kAtQBytes + 2 * kAtKVBytes + kAtXBytes);
+// Byte offset of element (row, col) of a [rows][64 bf16] 128-byte-swizzled block.
+__device__ __forceinline__ uint32_t sw128_off(int row, int col) {
+    return static_cast<uint32_t>(row * 128 + ((((col >> 3) ^ row) & 7) << 4) + (col & 7) * 2);
+}
 
-    const int q = blockIdx.x / P.splits, split = blockIdx.x % P.splits;
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+__global__ void __launch_bounds__(kAtThreads, 1)
+    sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, AttendParams P) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t sQ = sbase + kOffQ, sTile = sbase + kOffTile, sP = sbase + kOffP;
+    uint8_t *misc = smem + kOffMisc;
+    float *red_s = reinterpret_cast<float *>(misc + kMiscRed);
+    float *mused_s = reinterpret_cast<float *>(misc + kMiscMUsed);
+    float *fac_s = reinterpret_cast<float *>(misc + kMiscFac);
+    float *lsum_s = reinterpret_cast<float *>(misc + kMiscLSum);
+    uint16_t *tail_s = reinterpret_cast<uint16_t *>(misc + kMiscTail);
+    float *ztail_s = reinterpret_cast<float *>(misc + kMiscZTail);
+    float *wm_s = reinterpret_cast<float *>(misc + kMiscW);
+    const uint32_t bar0 = sbase + kOffMisc + kMiscBars;
+    auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
+    uint32_t *tmem_s = reinterpret_cast<uint32_t *>(misc + kMiscTmem);
+    int *abort_s = reinterpret_cast<int *>(misc + kMiscAbort);
+    volatile int *abort_flag = abort_s;
+
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int hg = warp & 3, dh = warp >> 2;
-    const int g = lane >> 2, c4 = lane & 3, mi = lane >> 3, rr = lane & 7;
+    const int S = P.splits;
+    const int q = blockIdx.x / S, split = blockIdx.x % S;
 
+    // ---- what this query attends to
     const int b = P.q_seq[q];
     const int t = P.q_pos[q];
-    int n_tok = 0, ns = 0, nf = 0;
+    bool qvalid = true;
+    int nf = 0, ns = 0, n_tail = 0;
     int64_t base_row = 0;
     if (b < 0 || b >= P.num_seqs || t < 0) {
         if (tid == 0) set_status(P.status, KP_ERR_DEVICE_BOUNDS);
+        qvalid = false;
     } else {
         nf = (t + 1) / kKpool;
         ns = P.n_sel[q];
@@ -94,261 +187,462 @@ __global__ void __launch_bounds__(kAtThreads, 1) sparse_mla_mma_kernel(AttendPar
             if (tid == 0) set_status(P.status, KP_ERR_DEVICE_BOUNDS);
             ns = max(0, min(ns, ns_max));
         }
-        const int tail = P.tail ? (t + 1) - nf * kKpool : 0;
-        n_tok = ns * kKpool + tail;
+        n_tail = P.tail ? (t + 1) - nf * kKpool : 0;
         base_row = P.latent_row_off[b];
+        if (base_row < 0 || base_row + t >= P.latent_rows) {
+            if (tid == 0) set_status(P.status, KP_ERR_DEVICE_BOUNDS);
+            qvalid = false;
+            ns = 0;
+            n_tail = 0;
+        }
     }
-    const int n_tiles = (n_tok + kAtTile - 1) / kAtTile;
-    const int tb = n_tiles * split / P.splits, te = n_tiles * (split + 1) / P.splits;
+    const int n_pool_tok = ns * kKpool;
+    const int n_tiles = (n_pool_tok + kAtTok - 1) / kAtTok;
+    const int tb = n_tiles * split / S, te = n_tiles * (split + 1) / S;
+    const int nt = te - tb;
 
-    // Q: 64 heads x 512 columns (the rotary columns 512..575 are never read).
-    for (int i = tid; i < kMlaHeads * 64; i += kAtThreads) {
-        const int h = i >> 6, c = i & 63;
-        cp_async_16(smem_u32(sQ) + swz(h, c),
-                    P.q_lat + (static_cast<int64_t>(q) * kMlaHeads + h) * kLatentDim + c * 8, 16);
+    // ---- set-up
+    if (tid == 0) {
+        for (int c = 0; c < kAtChunks; ++c) {
+            mbar_init(bar(kBarFull + c), kAtProdThreads);
+            mbar_init(bar(kBarFree + c), 1);
+        }
+        mbar_init(bar(kBarQ), 1);
+        mbar_init(bar(kBarS), 1);
+        mbar_init(bar(kBarP), kAtSoftThreads);
+        mbar_init(bar(kBarO), 1);
+        mbar_init(bar(kBarDrain), 1);
+        fence_mbar_init();
+        *abort_s = 0;
+        tma_prefetch_desc(&tm_q);
     }
-    cp_async_commit();
+    if (tid < kMlaHeads) {
+        mused_s[tid] = -INFINITY;
+        lsum_s[tid] = 0.f;
+    }
+    if (warp == kAtMmaWarp) {
+        tmem_alloc(smem_u32(tmem_s), kAtTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_s;
 
-    auto compute_rows = [&](int k, int slot) {
-        if (tid < kAtTile) {
-            const int i = k * kAtTile + tid;
-            int64_t row = -1;
-            if (i < n_tok) {
-                if (i < ns * kKpool) {
-                    const int p = P.pool_idx[static_cast<int64_t>(q) * P.K + i / kKpool];
-                    if (p >= 0 && p < nf) row = base_row + static_cast<int64_t>(p) * kKpool + (i % kKpool);
-                    else set_status(P.status, KP_ERR_DEVICE_BOUNDS);
-                } else {
-                    row = base_row + static_cast<int64_t>(nf) * kKpool + (i - ns * kKpool);
+    if (warp == kAtMmaWarp) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            if (qvalid) {
+                mbar_expect_tx(bar(kBarQ), kAtQBytes);
+                for (int blk = 0; blk < 8; ++blk)
+                    tma_load_2d(sQ + blk * kAtQBlockBytes, &tm_q, bar(kBarQ), blk * 64, q * kMlaHeads);
+            }
+            bool ok = true;
+            if (nt > 0) ok = mbar_wait(bar(kBarQ), 0, abort_flag, P.status);
+            const uint32_t idesc_s = idesc_bf16_f32(kAtTok, kMlaHeads);
+            const uint32_t idesc_pv = idesc_bf16_f32(kAtTok, kMlaHeads, true, true);
+            for (int jj = 0; ok && jj < nt; ++jj) {
+                const uint32_t par = jj & 1;
+                for (int c = 0; ok && c < kAtChunks; ++c) {
+                    if (!(ok = mbar_wait(bar(kBarFull + c), par, abort_flag, P.status))) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const int blk = 2 * c + (kk >> 2);
+                        const uint32_t koff = (kk & 3) * 32;
+                        const uint64_t ad = desc_sw128(sTile + blk * kAtBlockBytes + koff, 16, 1024);
+                        const uint64_t bd = desc_sw128(sQ + blk * kAtQBlockBytes + koff, 16, 1024);
+                        tc_mma_bf16(tmem + kAtSCol, ad, bd, idesc_s, (c | kk) ? 1u : 0u);
+                    }
                 }
-                if (row >= P.latent_rows) {
-                    set_status(P.status, KP_ERR_DEVICE_BOUNDS);
-                    row = -1;
+                if (!ok) break;
+                tc_commit(bar(kBarS));
+                if (!(ok = mbar_wait(bar(kBarP), par, abort_flag, P.status))) break;
+                tc_fence_after();
+                for (int c = 0; c < kAtChunks; ++c) {
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        // A = C^T (latent columns x tokens), M-major: 64-column groups 16 KB
+                        // apart, 8-token groups 1 KB apart.  B = P (tokens x heads), N-major.
+                        const uint64_t ad = desc_sw128(sTile + 2 * c * kAtBlockBytes + kk * 2048,
+                                                       kAtBlockBytes, 1024);
+                        // (B is one 64-head group wide, so its LBO is never stepped.)
+                        const uint64_t bd = desc_sw128(sP + kk * 2048, 8192, 1024);
+                        tc_mma_bf16(tmem + kAtOCol + 64 * c, ad, bd, idesc_pv, (jj | kk) ? 1u : 0u);
+                    }
+                    tc_commit(bar(kBarFree + c));
                 }
             }
-            sRows[slot * kAtTile + tid] = row;
+            if (ok) {
+                if (nt > 0) tc_commit(bar(kBarO));
+                else mbar_arrive(bar(kBarO));
+            } else {
+                // Let every MMA already issued finish before the TMEM is freed.
+                tc_commit(bar(kBarDrain));
+                mbar_wait(bar(kBarDrain), 0, nullptr, P.status);
+                mbar_arrive(bar(kBarO));
+            }
         }
-    };
-    auto issue_tile = [&](int slot) {
-        const int c = tid & 63, r0 = tid >> 6;
-        const uint32_t dst0 = smem_u32(sKV + slot * kAtKVBytes);
-#pragma unroll
-        for (int j = 0; j < kAtTile / 4; ++j) {
-            const int r = r0 + 4 * j;
-            const int64_t row = sRows[slot * kAtTile + r];
-            const uint16_t *src = P.latent + (row < 0 ? 0 : row) * kLatentDim + c * 8;
-            cp_async_16(dst0 + swz(r, c), src, row < 0 ? 0u : 16u);
-        }
-    };
-
-    float O[32][4];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) O[i][0] = O[i][1] = O[i][2] = O[i][3] = 0.f;
-    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-
-    if (tb < te) {
-        compute_rows(tb, 0);
-        __syncthreads();
-        issue_tile(0);
-        cp_async_commit();
-    }
-    for (int k = tb; k < te; ++k) {
-        const int slot = (k - tb) & 1;
-        if (k + 1 < te) {
-            compute_rows(k + 1, slot ^ 1);
-            __syncthreads();
-            issue_tile(slot ^ 1);
-            cp_async_commit();
+    } else if (warp >= kAtProdWarp0) {
+        // ------------------------------------------------------------ gather
+        const int pw = warp - kAtProdWarp0;
+        const int piece = lane & 15, sub = lane >> 4;
+        // Token pairs (2k, 2k+1), k = pw + 3m, m < n_pairs; list index j = 2m + sub.
+        const int n_pairs = (64 - pw + kAtProdWarps - 1) / kAtProdWarps;
+        auto row_of = [&](int tile, int j) -> int64_t {
+            if (j >= 2 * n_pairs) return -1;
+            const int tok = tile * kAtTok + 2 * (pw + kAtProdWarps * (j >> 1)) + (j & 1);
+            if (tok >= n_pool_tok) return -1;
+            const int p = P.pool_idx[static_cast<int64_t>(q) * P.K + tok / kKpool];
+            if (p < 0 || p >= nf) {
+                set_status(P.status, KP_ERR_DEVICE_BOUNDS);
+                return -1;
+            }
+            return base_row + static_cast<int64_t>(p) * kKpool + (tok % kKpool);
+        };
+        for (int jj = 0; jj < nt; ++jj) {
+            const int tile = tb + jj;
+            const int64_t row0 = row_of(tile, lane), row1 = row_of(tile, lane + 32);
+            bool ok = true;
+            for (int c = 0; c < kAtChunks; ++c) {
+                if (jj > 0 && !(ok = mbar_wait(bar(kBarFree + c), (jj - 1) & 1, abort_flag, P.status)))
+                    break;
+                for (int m = 0; m < n_pairs; ++m) {
+                    const int tk = 2 * (pw + kAtProdWarps * m) + sub;
+                    const int64_t r = __shfl_sync(0xffffffffu, m < 16 ? row0 : row1, (2 * m + sub) & 31);
+                    const uint16_t *src = P.latent + (r < 0 ? 0 : r) * kLatentDim + c * 128 + piece * 8;
+                    const uint32_t dst = sTile + (2 * c + (piece >> 3)) * kAtBlockBytes + tk * 128 +
+                                         (((piece & 7) ^ (tk & 7)) << 4);
+                    cp_async_16(dst, src, r < 0 ? 0u : 16u);
+                }
+                cp_async_commit();
+            }
+            if (!ok) {
+                cp_async_wait<0>();
+                break;
+            }
+            // Chunk c is complete once at most 3 - c newer groups are pending.
+            cp_async_wait<3>();
+            fence_proxy_async_smem();
+            mbar_arrive(bar(kBarFull + 0));
+            cp_async_wait<2>();
+            fence_proxy_async_smem();
+            mbar_arrive(bar(kBarFull + 1));
             cp_async_wait<1>();
-        } else {
+            fence_proxy_async_smem();
+            mbar_arrive(bar(kBarFull + 2));
             cp_async_wait<0>();
+            fence_proxy_async_smem();
+            mbar_arrive(bar(kBarFull + 3));
+        }
+    } else {
+        // ------------------------------------------------------------ softmax
+        const int quad = warp & 3, half = warp >> 2;
+        const int i = quad * 32 + lane;  // token lane of the tile
+        const int hb = half * 32;        // this warp's first head
+        const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+        float lp[32];                    // running row-sum partials, heads hb .. hb+31
+#pragma unroll
+        for (int h = 0; h < 32; ++h) lp[h] = 0.f;
+        bool ok = true;
+        for (int jj = 0; jj < nt; ++jj) {
+            ok = named_bar_all(1, kAtSoftThreads, mbar_wait(bar(kBarS), jj & 1, abort_flag, P.status));
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(tmem + lane_base + kAtSCol + hb, r);
+            tmem_ld_wait();
+            const int n_valid = min(kAtTok, n_pool_tok - (tb + jj) * kAtTok);
+            const bool valid = i < n_valid;
+            float x[32];
+#pragma unroll
+            for (int h = 0; h < 32; ++h) {
+                x[h] = valid ? __uint_as_float(r[h]) * P.scale_log2 : -INFINITY;
+                const float m = warp_max_f32(x[h]);
+                if (lane == h) red_s[quad * 64 + hb + h] = m;
+            }
+            named_bar(1, kAtSoftThreads);
+            if (tid < kMlaHeads) {
+                const float mt = fmaxf(fmaxf(red_s[tid], red_s[64 + tid]), fmaxf(red_s[128 + tid], red_s[192 + tid]));
+                const float mo = mused_s[tid];
+                if (mt > mo + kAtRescaleLog2) {
+                    mused_s[tid] = mt;
+                    fac_s[tid] = exp2f(mo - mt);  // 0 on the first tile (mo = -inf)
+                } else {
+                    fac_s[tid] = 1.f;
+                }
+            }
+            named_bar(1, kAtSoftThreads);
+            bool any = false;
+#pragma unroll
+            for (int h = 0; h < 32; h += 4) {
+                const float4 f = *reinterpret_cast<const float4 *>(fac_s + hb + h);
+                lp[h] *= f.x;
+                lp[h + 1] *= f.y;
+                lp[h + 2] *= f.z;
+                lp[h + 3] *= f.w;
+                any |= (f.x != 1.f) | (f.y != 1.f) | (f.z != 1.f) | (f.w != 1.f);
+            }
+            // p = 2^(x - m), row partial sums, bf16 P (token i, heads hb..hb+31), swizzled.
+            uint8_t *prow = smem + kOffP + i * 128;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                uint32_t pk[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int h = 8 * k + 2 * e;
+                    const float2 m2 = *reinterpret_cast<const float2 *>(mused_s + hb + h);
+                    const float p0 = exp2f(x[h] - m2.x);
+                    const float p1 = exp2f(x[h + 1] - m2.y);
+                    lp[h] += p0;
+                    lp[h + 1] += p1;
+                    pk[e] = pack_bf16x2(p0, p1);
+                }
+                const int chunk = 4 * half + k;
+                *reinterpret_cast<uint4 *>(prow + ((chunk ^ (i & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
+            if (any && jj > 0) {
+                // O^T is stable here: every P.V of the previous tile completed before S^T.
+                // (Done after P so that the logits' registers are free.)
+                for (int c = 0; c < kAtChunks; ++c) {
+                    uint32_t o[32];
+                    const uint32_t ta = tmem + lane_base + kAtOCol + 64 * c + hb;
+                    tmem_ld_32x32b_x32(ta, o);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int h = 0; h < 32; ++h) o[h] = __float_as_uint(__uint_as_float(o[h]) * fac_s[hb + h]);
+                    tmem_st_32x32b_x32(ta, o);
+                }
+                tmem_st_wait();
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar(kBarP));
+        }
+        // ---- after the last tile: O^T -> shared memory as O[h][d] (fp32, unnormalised)
+        if (ok) ok = named_bar_all(1, kAtSoftThreads, mbar_wait(bar(kBarO), 0, abort_flag, P.status));
+        if (ok) {
+            tc_fence_after();
+            if (nt > 0) {
+                float *odump = reinterpret_cast<float *>(smem + kOffTile);
+                for (int c = 0; c < kAtChunks; ++c) {
+                    uint32_t o[32];
+                    tmem_ld_32x32b_x32(tmem + lane_base + kAtOCol + 64 * c + hb, o);
+                    tmem_ld_wait();
+                    const int d = c * 128 + i;
+#pragma unroll
+                    for (int h = 0; h < 32; ++h) odump[(hb + h) * kNopeDim + d] = __uint_as_float(o[h]);
+                }
+            }
+            // Row sums: transpose-reduce the 32 per-thread partials over the warp
+            // (lane l ends with head hb + l), then add the 4 quadrants.
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const bool hi = lane & 16;
+                const float send = hi ? lp[j] : lp[j + 16];
+                const float keep = hi ? lp[j + 16] : lp[j];
+                lp[j] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const bool hi = lane & 8;
+                const float send = hi ? lp[j] : lp[j + 8];
+                const float keep = hi ? lp[j + 8] : lp[j];
+                lp[j] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const bool hi = lane & 4;
+                const float send = hi ? lp[j] : lp[j + 4];
+                const float keep = hi ? lp[j + 4] : lp[j];
+                lp[j] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+            }
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const bool hi = lane & 2;
+                const float send = hi ? lp[j] : lp[j + 2];
+                const float keep = hi ? lp[j + 2] : lp[j];
+                lp[j] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+            }
+            {
+                const bool hi = lane & 1;
+                const float send = hi ? lp[0] : lp[1];
+                const float keep = hi ? lp[1] : lp[0];
+                lp[0] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
+            }
+            atomicAdd(lsum_s + hb + lane, lp[0]);
+        }
+    }
+
+    // ---- merge over the cluster, tail tokens, output
+    tc_fence_before();
+    __syncthreads();
+    if (S > 1) cluster_barrier();
+
+    const int h0 = kMlaHeads * split / S, h1 = kMlaHeads * (split + 1) / S, nh = h1 - h0;
+    const bool aborted = *abort_flag != 0;
+    if (qvalid && !aborted) {
+        // tail rows -> shared memory
+        for (int k = tid; k < n_tail * 64; k += kAtThreads) {
+            const int j = k >> 6, piece = k & 63;
+            const int64_t row = base_row + static_cast<int64_t>(nf) * kKpool + j;
+            *reinterpret_cast<uint4 *>(tail_s + j * kNopeDim + piece * 8) =
+                *reinterpret_cast<const uint4 *>(P.latent + row * kLatentDim + piece * 8);
+        }
+        // Q has landed (the tail logits read it; nothing may be in flight at exit).
+        const bool have_q = mbar_wait(bar(kBarQ), 0, abort_flag, P.status);
+        __syncthreads();
+        // tail logits: one warp per (head, tail token)
+        if (have_q) {
+            for (int pr = warp; pr < nh * n_tail; pr += kAtThreads / 32) {
+                const int h = h0 + pr / n_tail, j = pr % n_tail;
+                float acc = 0.f;
+#pragma unroll
+                for (int e = 0; e < 16; e += 2) {
+                    const int d = lane * 16 + e;
+                    const uint32_t qv =
+                        *reinterpret_cast<const uint32_t *>(smem + kOffQ + (d >> 6) * kAtQBlockBytes +
+                                                            sw128_off(h, d & 63));
+                    const uint32_t cv = *reinterpret_cast<const uint32_t *>(tail_s + j * kNopeDim + d);
+                    acc = fmaf(bf16_lo(qv), bf16_lo(cv), acc);
+                    acc = fmaf(bf16_hi(qv), bf16_hi(cv), acc);
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+                if (lane == 0) ztail_s[h * 4 + j] = acc * P.scale_log2;
+            }
         }
         __syncthreads();
-        const uint32_t kv = smem_u32(sKV + slot * kAtKVBytes);
-        const uint32_t qs = smem_u32(sQ);
-
-        // S_partial[16 heads x 64 tokens] over this warp's 256 latent columns.
-        float S[8][4];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) S[i][0] = S[i][1] = S[i][2] = S[i][3] = 0.f;
-#pragma unroll 4
-        for (int ks = 0; ks < 16; ++ks) {
-            const int kc = dh * 32 + ks * 2;
-            uint32_t a0, a1, a2, a3;
-            const int arow = 16 * hg + rr + 8 * (mi & 1);
-            ldsm_x4(qs + swz(arow, kc + (mi >> 1)), a0, a1, a2, a3);
-#pragma unroll
-            for (int nt2 = 0; nt2 < 4; ++nt2) {
-                uint32_t b0, b1, b2, b3;
-                const int brow = 16 * nt2 + rr + 8 * (mi >> 1);
-                ldsm_x4(kv + swz(brow, kc + (mi & 1)), b0, b1, b2, b3);
-                mma_bf16_16816(S[2 * nt2], a0, a1, a2, a3, b0, b1);
-                mma_bf16_16816(S[2 * nt2 + 1], a0, a1, a2, a3, b2, b3);
+        // per-head merge weights
+        if (tid < nh) {
+            const int h = h0 + tid;
+            float M = -INFINITY;
+            for (int s = 0; s < S; ++s) M = fmaxf(M, dsmem_ld_f32(dsmem_addr(smem_u32(mused_s + h), s)));
+            for (int j = 0; j < n_tail; ++j) M = fmaxf(M, ztail_s[h * 4 + j]);
+            float L = 0.f;
+            float *w = wm_s + tid * 16;
+            for (int s = 0; s < kAtMaxSplits; ++s) {
+                float ws = 0.f;
+                if (s < S) {
+                    const float ms = dsmem_ld_f32(dsmem_addr(smem_u32(mused_s + h), s));
+                    if (ms > -INFINITY) {
+                        ws = exp2f(ms - M);
+                        L += ws * dsmem_ld_f32(dsmem_addr(smem_u32(lsum_s + h), s));
+                    }
+                }
+                w[s] = ws;
             }
-        }
-        // Add the other column half's partial sums (same value in both warps).
-        float *myX = sX + warp * 1024;
-        const float *otX = sX + (warp ^ 4) * 1024;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) myX[j * 32 + lane] = S[j >> 2][j & 3];
-        named_bar(1 + hg, 64);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) S[j >> 2][j & 3] += otX[j * 32 + lane];
-
-        // Online softmax (log2 domain).  Row r = 0: head 16hg+g, r = 1: +8.
-        float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int col = 8 * nt + 2 * c4 + (e & 1);
-                const bool valid = sRows[slot * kAtTile + col] >= 0;
-                const float v = valid ? S[nt][e] * P.scale_log2 : -INFINITY;
-                S[nt][e] = v;
-                mx[e >> 1] = fmaxf(mx[e >> 1], v);
+            for (int j = 0; j < kAtMaxTail; ++j) {
+                const float wt = j < n_tail ? exp2f(ztail_s[h * 4 + j] - M) : 0.f;
+                w[8 + j] = wt;
+                L += wt;
             }
-        float alpha[2], rsum[2] = {0.f, 0.f};
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-            mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-            const float m_new = fmaxf(m_run[r], mx[r]);
-            alpha[r] = (m_new == -INFINITY) ? 1.f : exp2f(m_run[r] - m_new);
-            m_run[r] = m_new;
-        }
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int r = e >> 1;
-                const float p = (m_run[r] == -INFINITY) ? 0.f : exp2f(S[nt][e] - m_run[r]);
-                S[nt][e] = p;
-                rsum[r] += p;
-            }
-#pragma unroll
-        for (int r = 0; r < 2; ++r) l_run[r] = l_run[r] * alpha[r] + rsum[r];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            O[i][0] *= alpha[0];
-            O[i][1] *= alpha[0];
-            O[i][2] *= alpha[1];
-            O[i][3] *= alpha[1];
-        }
-        uint32_t pa[4][4];
-#pragma unroll
-        for (int k2 = 0; k2 < 4; ++k2) {
-            pa[k2][0] = pack_bf16x2(S[2 * k2][0], S[2 * k2][1]);
-            pa[k2][1] = pack_bf16x2(S[2 * k2][2], S[2 * k2][3]);
-            pa[k2][2] = pack_bf16x2(S[2 * k2 + 1][0], S[2 * k2 + 1][1]);
-            pa[k2][3] = pack_bf16x2(S[2 * k2 + 1][2], S[2 * k2 + 1][3]);
-        }
-        // O[16 heads x 256 cols] += P[16 x 64] . V[64 x 256]
-#pragma unroll
-        for (int k2 = 0; k2 < 4; ++k2) {
-            const int vrow = 16 * k2 + rr + 8 * (mi & 1);
-#pragma unroll
-            for (int nd2 = 0; nd2 < 16; ++nd2) {
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4_t(kv + swz(vrow, dh * 32 + 2 * nd2 + (mi >> 1)), b0, b1, b2, b3);
-                mma_bf16_16816(O[2 * nd2], pa[k2][0], pa[k2][1], pa[k2][2], pa[k2][3], b0, b1);
-                mma_bf16_16816(O[2 * nd2 + 1], pa[k2][0], pa[k2][1], pa[k2][2], pa[k2][3], b2, b3);
-            }
+            w[12] = L > 0.f ? 1.f / L : 0.f;
+            if (P.lse) P.lse[static_cast<int64_t>(q) * kMlaHeads + h] = L > 0.f ? (M + log2f(L)) * 0.69314718055994530942f : -INFINITY;
         }
         __syncthreads();
-    }
-    cp_async_wait<0>();
-
-    // Finalise this split.
-    float inv[2], lse_v[2];
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-        l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 1);
-        l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 2);
-        if (l_run[r] > 0.f) {
-            inv[r] = 1.f / l_run[r];
-            lse_v[r] = (m_run[r] + log2f(l_run[r])) * kLn2;
-        } else {
-            inv[r] = 0.f;
-            lse_v[r] = -INFINITY;
-        }
-    }
-    const int h0 = 16 * hg + g, h1 = h0 + 8;
-    if (P.splits == 1) {
-        uint16_t *o0 = P.out + (static_cast<int64_t>(q) * kMlaHeads + h0) * kNopeDim;
-        uint16_t *o1 = P.out + (static_cast<int64_t>(q) * kMlaHeads + h1) * kNopeDim;
-#pragma unroll
-        for (int nd = 0; nd < 32; ++nd) {
-            const int d = dh * 256 + 8 * nd + 2 * c4;
-            *reinterpret_cast<uint32_t *>(o0 + d) = pack_bf16x2(O[nd][0] * inv[0], O[nd][1] * inv[0]);
-            *reinterpret_cast<uint32_t *>(o1 + d) = pack_bf16x2(O[nd][2] * inv[1], O[nd][3] * inv[1]);
-        }
-        if (P.lse && dh == 0 && c4 == 0) {
-            P.lse[static_cast<int64_t>(q) * kMlaHeads + h0] = lse_v[0];
-            P.lse[static_cast<int64_t>(q) * kMlaHeads + h1] = lse_v[1];
-        }
-        return;
-    }
-    const int64_t wi = static_cast<int64_t>(q) * P.splits + split;
-    float *wo = P.ws_o + wi * kMlaHeads * kNopeDim;
-#pragma unroll
-    for (int nd = 0; nd < 32; ++nd) {
-        const int d = dh * 256 + 8 * nd + 2 * c4;
-        *reinterpret_cast<float2 *>(wo + h0 * kNopeDim + d) = make_float2(O[nd][0] * inv[0], O[nd][1] * inv[0]);
-        *reinterpret_cast<float2 *>(wo + h1 * kNopeDim + d) = make_float2(O[nd][2] * inv[1], O[nd][3] * inv[1]);
-    }
-    if (dh == 0 && c4 == 0) {
-        P.ws_lse[wi * kMlaHeads + h0] = lse_v[0];
-        P.ws_lse[wi * kMlaHeads + h1] = lse_v[1];
-    }
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) s_last = atomicAdd(&P.ws_cnt[q], 1) == P.splits - 1;
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-    // Last split of this query: merge the partials, lse-weighted.
-    const float *base_o = P.ws_o + static_cast<int64_t>(q) * P.splits * kMlaHeads * kNopeDim;
-    const float *base_l = P.ws_lse + static_cast<int64_t>(q) * P.splits * kMlaHeads;
-    for (int idx = tid; idx < kMlaHeads * (kNopeDim / 2); idx += kAtThreads) {
-        const int h = idx / (kNopeDim / 2), d = 2 * (idx % (kNopeDim / 2));
-        float mx = -INFINITY;
-        for (int s = 0; s < P.splits; ++s) mx = fmaxf(mx, __ldcg(base_l + s * kMlaHeads + h));
-        float a0 = 0.f, a1 = 0.f, den = 0.f;
-        if (mx > -INFINITY) {
-            for (int s = 0; s < P.splits; ++s) {
-                const float wgt = expf(__ldcg(base_l + s * kMlaHeads + h) - mx);
-                const float2 v = __ldcg(reinterpret_cast<const float2 *>(
-                    base_o + (static_cast<int64_t>(s) * kMlaHeads + h) * kNopeDim + d));
-                den += wgt;
-                a0 += wgt * v.x;
-                a1 += wgt * v.y;
+        // out[q][h][d] = (sum_s w_s O_s[h][d] + sum_j w_j c_j[d]) / L
+        const uint32_t odump_addr = sbase + kOffTile;
+        for (int idx = tid; idx < nh * (kNopeDim / 2); idx += kAtThreads) {
+            const int hl = idx / (kNopeDim / 2), d = 2 * (idx % (kNopeDim / 2));
+            const int h = h0 + hl;
+            const float *w = wm_s + hl * 16;
+            float a0 = 0.f, a1 = 0.f;
+            for (int s = 0; s < S; ++s) {
+                if (w[s] > 0.f) {
+                    const float2 v = dsmem_ld_f32x2(dsmem_addr(odump_addr + (h * kNopeDim + d) * 4, s));
+                    a0 = fmaf(w[s], v.x, a0);
+                    a1 = fmaf(w[s], v.y, a1);
+                }
             }
+            for (int j = 0; j < n_tail; ++j) {
+                const uint32_t cv = *reinterpret_cast<const uint32_t *>(tail_s + j * kNopeDim + d);
+                a0 = fmaf(w[8 + j], bf16_lo(cv), a0);
+                a1 = fmaf(w[8 + j], bf16_hi(cv), a1);
+            }
+            *reinterpret_cast<uint32_t *>(P.out + (static_cast<int64_t>(q) * kMlaHeads + h) * kNopeDim + d) =
+                pack_bf16x2(a0 * w[12], a1 * w[12]);
         }
-        const float iv = den > 0.f ? 1.f / den : 0.f;
-        *reinterpret_cast<uint32_t *>(P.out + (static_cast<int64_t>(q) * kMlaHeads + h) * kNopeDim + d) =
-            pack_bf16x2(a0 * iv, a1 * iv);
-        if (P.lse && d == 0) P.lse[static_cast<int64_t>(q) * kMlaHeads + h] = den > 0.f ? mx + logf(den) : -INFINITY;
+    } else if (!qvalid && !aborted) {
+        // Nothing to attend: out = 0, lse = -inf.
+        for (int idx = tid; idx < nh * (kNopeDim / 2); idx += kAtThreads) {
+            const int h = h0 + idx / (kNopeDim / 2), d = 2 * (idx % (kNopeDim / 2));
+            *reinterpret_cast<uint32_t *>(P.out + (static_cast<int64_t>(q) * kMlaHeads + h) * kNopeDim + d) = 0u;
+        }
+        if (P.lse && tid < nh) P.lse[static_cast<int64_t>(q) * kMlaHeads + h0 + tid] = -INFINITY;
     }
-    if (tid == 0) P.ws_cnt[q] = 0;  // ready for the next call
+
+    // Peers may still read this CTA's shared memory until everyone is done.
+    if (S > 1) cluster_barrier();
+    if (aborted && qvalid && tid == 0) mbar_wait(bar(kBarQ), 0, nullptr, P.status);  // no TMA left in flight
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kAtMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kAtTmemCols);
+    }
+}
+
+// Largest cluster size whose clusters, one CTA per SM, all fit at once (cached per device).
+int max_active_clusters(int cluster) {
+    static int cache[64][kAtMaxSplits + 1] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (cache[dev][cluster] != 0) return cache[dev][cluster];
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cluster * 64);
+    cfg.blockDim = dim3(kAtThreads);
+    cfg.dynamicSmemBytes = kAtSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, sparse_mla_tc_kernel, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        n = 0;
+    }
+    cache[dev][cluster] = n > 0 ? n : -1;
+    return n;
+}
+
+bool attend_smem_configured() {
+    static int done[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    if (done[dev]) return true;
+    cudaError_t e = cudaFuncSetAttribute(sparse_mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kAtSmemBytes);
+    if (e != cudaSuccess) {
+        record_cuda_error("cudaFuncSetAttribute(sparse_mla_tc_kernel)", e);
+        return false;
+    }
+    done[dev] = 1;
+    return true;
 }
 
 }  // namespace
 
+// Splits of one query's token list = CTAs of its cluster: as many as keep
+// every cluster resident in one wave, at most 8, at most one per tile.
 int attend_splits(const kp_config &cfg, int32_t num_queries, int sm_count) {
     if (num_queries <= 0) return 1;
-    const int K = cfg.topk_tokens / cfg.kpool;
-    const int max_tiles = (K * cfg.kpool + cfg.kpool - 1 + kAtTile - 1) / kAtTile;
+    const int tiles = (cfg.topk_tokens + kAtTok - 1) / kAtTok;
     int s = sm_count / num_queries;
-    if (s > max_tiles) s = max_tiles;
-    return s < 1 ? 1 : s;
+    if (s > kAtMaxSplits) s = kAtMaxSplits;
+    if (s > tiles) s = tiles;
+    if (s < 1) s = 1;
+    return s;
 }
 
 size_t attend_ws_bytes(const kp_config &cfg, int32_t num_queries, int splits) {
     (void)cfg;
-    if (splits <= 1) return 256;
-    const size_t n = static_cast<size_t>(num_queries) * splits;
-    return align_up(n * kMlaHeads * kNopeDim * 4, 256) + align_up(n * kMlaHeads * 4, 256) +
-           align_up(static_cast<size_t>(num_queries) * 4, 256);
+    (void)num_queries;
+    (void)splits;
+    return 256;  // the cluster merge needs no global scratch
 }
 
 kp_status launch_attend(const kp_attend_args &a, cudaStream_t s) {
@@ -356,9 +650,15 @@ kp_status launch_attend(const kp_attend_args &a, cudaStream_t s) {
     if (nq == 0) return KP_OK;
     const int sms = device_sm_count();
     if (sms <= 0) return KP_ERR_CUDA;
-    const int splits = attend_splits(a.cfg, nq, sms);
+    if (!attend_smem_configured()) return KP_ERR_CUDA;
+    int splits = attend_splits(a.cfg, nq, sms);
+    while (splits > 1 && max_active_clusters(splits) < nq) --splits;
+
+    CUtensorMap tm_q;
+    if (!make_tmap_bf16_sw128(&tm_q, a.q_lat, kLatentDim, static_cast<uint64_t>(nq) * kMlaHeads,
+                              kLatentDim * 2, 64, kMlaHeads))
+        return KP_ERR_CUDA;
     AttendParams P;
-    P.q_lat = a.q_lat;
     P.latent = a.latent;
     P.latent_rows = a.seqs.latent_rows;
     P.q_seq = a.q.q_seq;
@@ -369,36 +669,30 @@ kp_status launch_attend(const kp_attend_args &a, cudaStream_t s) {
     P.n_sel = a.n_sel;
     P.K = a.cfg.topk_tokens / a.cfg.kpool;
     P.tail = a.cfg.always_select_tail ? 1 : 0;
-    P.scale_log2 = a.cfg.sm_scale * kLog2e;
+    P.scale_log2 = a.cfg.sm_scale * 1.44269504088896340736f;
     P.out = a.out;
     P.lse = a.lse;
     P.splits = splits;
     P.status = a.d_status;
-    P.ws_o = nullptr;
-    P.ws_lse = nullptr;
-    P.ws_cnt = nullptr;
-    if (splits > 1) {
-        const size_t n = static_cast<size_t>(nq) * splits;
-        uint8_t *w = static_cast<uint8_t *>(a.workspace);
-        P.ws_o = reinterpret_cast<float *>(w);
-        w += align_up(n * kMlaHeads * kNopeDim * 4, 256);
-        P.ws_lse = reinterpret_cast<float *>(w);
-        w += align_up(n * kMlaHeads * 4, 256);
-        P.ws_cnt = reinterpret_cast<int32_t *>(w);
-        cudaError_t e = cudaMemsetAsync(P.ws_cnt, 0, static_cast<size_t>(nq) * 4, s);
-        if (e != cudaSuccess) {
-            record_cuda_error("cudaMemsetAsync(attend tickets)", e);
-            return KP_ERR_CUDA;
-        }
-    }
-    cudaError_t e = cudaFuncSetAttribute(sparse_mla_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kAtSmemBytes);
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(nq) * splits);
+    cfg.blockDim = dim3(kAtThreads);
+    cfg.dynamicSmemBytes = kAtSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = splits;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, sparse_mla_tc_kernel, tm_q, P);
     if (e != cudaSuccess) {
-        record_cuda_error("cudaFuncSetAttribute(sparse_mla_mma_kernel)", e);
+        record_cuda_error("cudaLaunchKernelEx(sparse_mla_tc_kernel)", e);
         return KP_ERR_CUDA;
     }
-    sparse_mla_mma_kernel<<<static_cast<unsigned>(nq) * splits, kAtThreads, kAtSmemBytes, s>>>(P);
-    return check_launch("sparse_mla_mma_kernel");
+    return check_launch("sparse_mla_tc_kernel");
 }
 
 }  // namespace kp

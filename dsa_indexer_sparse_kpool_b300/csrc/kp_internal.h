@@ -1,6 +1,7 @@
 // kp_internal.h -- host-side declarations shared by the library's .cu files.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -18,6 +19,12 @@ kp_status check_launch(const char *where);
 
 // Number of SMs of the current device (0 on failure).
 int device_sm_count();
+
+// 2-D bf16 tensor map with 128-byte swizzle: `rows` rows of `inner` elements
+// (row pitch `row_bytes`, a multiple of 16), box of box_rows x box_inner
+// elements (box_inner * 2 <= 128).  False (error recorded) on failure.
+bool make_tmap_bf16_sw128(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows,
+                          uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows);
 
 // Byte sizes of the step workspaces.
 size_t score_plan_bytes(int32_t num_queries);

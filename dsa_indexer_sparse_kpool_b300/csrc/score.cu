@@ -311,38 +311,6 @@ __global__ void __launch_bounds__(kScThreads, 1)
     }
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = []() -> EncodeTiledFn {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &q) != cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            return nullptr;
-        return reinterpret_cast<EncodeTiledFn>(p);
-    }();
-    return fn;
-}
-
-// 2-D bf16 tensor [rows][128] (row pitch 256 B), box [box_rows][64] with 128-byte swizzle.
-bool make_map(CUtensorMap *m, const void *base, int64_t rows, int box_rows) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(kIndexDim), static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(kIndexDim * 2)};
-    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
-    cuuint32_t estr[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
-              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace
 
 size_t score_plan_bytes(int32_t num_queries) {
@@ -363,11 +331,11 @@ kp_status launch_score(const kp_score_args &a, cudaStream_t s) {
     if (max_tiles == 0) return KP_OK;
 
     CUtensorMap tm_pool, tm_q;
-    if (!make_map(&tm_pool, a.pooled, a.seqs.pool_rows, kScM) ||
-        !make_map(&tm_q, a.q_idx, static_cast<int64_t>(nq) * kIndexHeads, kIndexHeads)) {
-        record_error_text("cuTensorMapEncodeTiled failed");
+    if (!make_tmap_bf16_sw128(&tm_pool, a.pooled, kIndexDim, static_cast<uint64_t>(a.seqs.pool_rows),
+                              kIndexDim * 2, 64, kScM) ||
+        !make_tmap_bf16_sw128(&tm_q, a.q_idx, kIndexDim, static_cast<uint64_t>(nq) * kIndexHeads,
+                              kIndexDim * 2, 64, kIndexHeads))
         return KP_ERR_CUDA;
-    }
     cudaError_t e = cudaFuncSetAttribute(indexer_score_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kScSmemBytes);
     if (e != cudaSuccess) {

@@ -85,3 +85,29 @@ def test_decode_config_sampled():
 def test_ragged_config_sampled():
     wl = KI.make(KI.named("ragged"))
     PL.full_check(wl, queries=[0, 5, 15], check_all_pooled=False)
+
+
+def test_large_logits_exercise_running_max_rescale():
+    # logits spread over tens of log2 units, so later tiles raise the running
+    # max and the accumulated O and row sums are rescaled
+    spec = small_spec([1000, 1537, 2050], [1, 3, 2], 256, q_scale=64.0)
+    spec.sm_scale = 4.0
+    wl = KI.make(spec)
+    PL.full_check(wl)
+
+
+def test_prefill_chunk_of_64_queries():
+    # 64 consecutive positions of one sequence: per-query causal pool limits,
+    # all four tail lengths, several score query groups
+    wl = KI.make(small_spec([3000], [64], 512, seed=13))
+    PL.full_check(wl)
+
+
+def test_prefill_config_sampled():
+    wl = KI.make(KI.named("prefill"))
+    PL.full_check(wl, queries=[0, 1, 2, 3, 2047, 4095], check_all_pooled=False)
+
+
+def test_long_config_sampled():
+    wl = KI.make(KI.named("long"))
+    PL.full_check(wl, queries=[0, 3], check_all_pooled=False)
