@@ -31,6 +31,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 import kpool_inputs as KI  # noqa: E402
+from dsa_indexer_sparse_kpool_b300 import replicas  # noqa: E402
 
 METRIC = {"decode": "DSA decode tokens/s per B300", "ragged": "DSA decode tokens/s per B300",
           "long": "DSA decode tokens/s per B300", "prefill": "DSA prefill tokens/s per B300"}
@@ -62,12 +63,15 @@ def parse():
 
 def workload(name: str, rank: int) -> KI.Workload:
     spec = KI.named(name)
-    spec.seed += 1000 * rank          # each rank its own independent batch
+    spec.seed = replicas.rank_seed(spec.seed, rank)   # each rank its own independent batch
     return KI.make(spec)
 
 
 def algorithmic_bytes(wl: KI.Workload):
-    """Bytes the method must move per step, by stage (roofline)."""
+    """Bytes the method must move per step, by stage: pooled keys once per
+    sequence plus q and w (score); 1024 B per attended latent row (each row of a
+    sequence counted at most once) plus q_lat, out and lse per query (attend);
+    new key and gate rows plus new pooled rows (compress)."""
     kp = wl.spec.kpool
     K = wl.k_pools
     nf = (wl.q_pos.astype(np.int64) + 1) // kp
@@ -79,7 +83,14 @@ def algorithmic_bytes(wl: KI.Workload):
         b = int(wl.q_seq[q])
         per_seq[b] = max(per_seq.get(b, 0), int(nf[q]))
     score = sum(per_seq.values()) * 128 * 2 + wl.NQ * (32 * 128 * 2 + 32 * 4)
-    attend = int(n_tok.sum()) * 512 * 2 + wl.NQ * 64 * (512 * 2 + 512 * 2 + 4)
+    # latent rows: each query's gathered rows, but never more than the sequence
+    # holds (the queries of a prefill chunk share one cache)
+    tok_per_seq = {}
+    for q in range(wl.NQ):
+        b = int(wl.q_seq[q])
+        tok_per_seq[b] = tok_per_seq.get(b, 0) + int(n_tok[q])
+    rows = sum(min(v, int(wl.lens[b])) for b, v in tok_per_seq.items())
+    attend = rows * 512 * 2 + wl.NQ * 64 * (512 * 2 + 512 * 2 + 4)
     n_new = int((wl.lens - wl.prev_len).sum())
     new_pools = int(sum(int(L) // kp - int(P) // kp for L, P in zip(wl.lens, wl.prev_len)))
     compress = n_new * 2 * 128 * 2 + new_pools * 128 * 2
@@ -87,26 +98,41 @@ def algorithmic_bytes(wl: KI.Workload):
             "sparse_mla_attend": attend}, int(n_tok.sum())
 
 
+def algorithmic_flops(wl: KI.Workload):
+    """Tensor-core flops the method must do per step, by stage: scores over each
+    query's visible pools (32 heads x 128 dims), and Q.K plus P.V over each
+    query's attended tokens (64 heads x 512 latent columns)."""
+    kp = wl.spec.kpool
+    nf = (wl.q_pos.astype(np.int64) + 1) // kp
+    tail = (wl.q_pos.astype(np.int64) + 1) - nf * kp
+    n_tok = np.minimum(nf, wl.k_pools) * kp + tail
+    return {"kpool_compress": 0, "indexer_score": int(nf.sum()) * 32 * 128 * 2, "topk_select": 0,
+            "sparse_mla_attend": int(n_tok.sum()) * 64 * 512 * 2 * 2}
+
+
 def measured_peaks():
+    """(HBM GB/s, bf16 TFLOP/s burst, bf16 TFLOP/s sustained, source)."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         d = json.load(open(p))
-        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
-    return 6400.0, 1800.0, "fallback"
+        return (float(d["hbm_gbs"]), float(d["bf16_tflops"]),
+                float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured")
+    return 6400.0, 1800.0, 1400.0, "fallback"
 
 
 def kernel_traffic(stage: str):
-    """ncu DRAM bytes per launch of this stage's kernel, if the committed summary
-    was taken on the current kernel source (else None)."""
-    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    """ncu DRAM bytes per launch of this stage's kernel (profiles/ncu_traffic.txt),
+    if that capture was taken on the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
     if not os.path.exists(p):
-        return None
-    d = json.load(open(p)).get(stage)
-    if not d:
         return None
     src = os.path.join(ROOT, "dsa_indexer_sparse_kpool_b300", "csrc", KERNEL_FILES[stage])
     sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    return d["bytes_per_launch"] if d.get("source_sha") == sha else None
+    for line in open(p):
+        f = line.split()
+        if len(f) >= 5 and not line.startswith("#") and f[0] == stage and f[4] == sha:
+            return int(f[3])
+    return None
 
 
 # ------------------------------------------------------------------ clocks
@@ -124,7 +150,7 @@ class ClockSampler:
             sel = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
         except Exception:
             sel = []
-        self.cmd = ["nvidia-smi", *sel, "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits", "-lms", "100"]
+        self.cmd = ["nvidia-smi", *sel, "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits", "-lms", "20"]
 
     def start(self):
         try:
@@ -361,26 +387,34 @@ def main():
         e2e_ms = float(np.mean([a.elapsed_time(b) for a, b in eev]))
         status = int(sess.status.item())
 
-    # ---- aggregate over ranks
+    # ---- aggregate over ranks (max of the ranks' times)
+    total_ms, e2e_ms = replicas.max_over_ranks([total_ms, e2e_ms], device=dev)
     t_step = total_ms / args.steps
     t_e2e = e2e_ms
-    if world > 1:
-        t = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_step = float(t[0]) / args.steps
-        t_e2e = float(t[1])
-    value = world * NQ / (t_step * 1e-3)
-    e2e_value = world * NQ / (t_e2e * 1e-3)
+    value = replicas.job_rate(NQ, world, t_step * 1e-3)
+    e2e_value = replicas.job_rate(NQ, world, t_e2e * 1e-3)
 
     if rank == 0:
         alg, n_tok = algorithmic_bytes(wl)
-        hbm, bf16, src = measured_peaks()
+        flops = algorithmic_flops(wl)
+        hbm, bf16, bf16_sus, src = measured_peaks()
         dominant = max(("indexer_score", "sparse_mla_attend", "topk_select", "kpool_compress"),
                        key=lambda s: stage_ms[s])
-        ach = alg[dominant] / (stage_ms[dominant] * 1e-3) / 1e9 if alg[dominant] else 0.0
-        roof = {"bound": "hbm", "kernel": dominant, "achieved": ach, "peak": hbm, "unit": "GB/s",
-                "frac": ach / hbm, "peak_source": src, "traffic": kernel_traffic(dominant),
-                "algorithmic_bytes": alg[dominant], "avg_launch_ms": stage_ms[dominant]}
+        t_dom = stage_ms[dominant] * 1e-3
+        # the stage's bound: whichever of HBM bytes and tensor flops takes longer at peak
+        stage_loop_s = t_dom * ks
+        tpeak = bf16 if stage_loop_s < 1.0 else bf16_sus
+        if flops[dominant] / (tpeak * 1e12) > alg[dominant] / (hbm * 1e9):
+            ach = flops[dominant] / t_dom / 1e12
+            roof = {"bound": "tensor", "kernel": dominant, "achieved": ach, "peak": tpeak, "unit": "TFLOP/s",
+                    "frac": ach / tpeak, "peak_source": src + (" bf16 burst" if tpeak == bf16 else " bf16 sustained"),
+                    "traffic": kernel_traffic(dominant), "algorithmic_flops": flops[dominant],
+                    "algorithmic_bytes": alg[dominant], "avg_launch_ms": stage_ms[dominant]}
+        else:
+            ach = alg[dominant] / t_dom / 1e9
+            roof = {"bound": "hbm", "kernel": dominant, "achieved": ach, "peak": hbm, "unit": "GB/s",
+                    "frac": ach / hbm, "peak_source": src + " HBM copy", "traffic": kernel_traffic(dominant),
+                    "algorithmic_bytes": alg[dominant], "avg_launch_ms": stage_ms[dominant]}
         step_bytes = sum(alg.values())
         cpu = None
         if not args.no_cpu_baseline:

@@ -111,3 +111,20 @@ def test_prefill_config_sampled():
 def test_long_config_sampled():
     wl = KI.make(KI.named("long"))
     PL.full_check(wl, queries=[0, 3], check_all_pooled=False)
+
+
+def test_exact_ties_in_scores():
+    # sequence 0: every pool identical -> all 5000 scores equal (more ties than
+    # the candidate buffer: the radix fallback); sequence 1: pooled keys repeat
+    # every 10 pools -> 75-fold ties at the threshold (candidate sort).  Ties go
+    # to the lower pool index in both.
+    wl = KI.make(small_spec([20000, 3000], [1, 2], 256, seed=17))
+    a, e = int(wl.tok_off[0]), int(wl.tok_off[0] + wl.lens[0])
+    wl.keys[a:e] = wl.keys[a:a + 4].repeat((e - a) // 4, 1)
+    wl.gates[a:e] = wl.gates[a:a + 4].repeat((e - a) // 4, 1)
+    a, e = int(wl.tok_off[1]), int(wl.tok_off[1] + wl.lens[1])
+    wl.keys[a:e] = wl.keys[a:a + 40].repeat((e - a) // 40, 1)
+    wl.gates[a:e] = wl.gates[a:a + 40].repeat((e - a) // 40, 1)
+    sess, step, rep = PL.full_check(wl)
+    sel0 = step.pool_idx[0].cpu().numpy()
+    assert np.array_equal(sel0, np.arange(64)), "equal scores must select the lowest pool indices"
