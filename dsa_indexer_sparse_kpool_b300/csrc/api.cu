@@ -140,7 +140,10 @@ using namespace kp;
 
 extern "C" {
 
-kp_status kp_kpool_compress(const kp_compress_args *a, kp_stream_t stream) {
+namespace {
+// Argument checks of the four stages (no launch).  KP_OK with nothing to do
+// (no new tokens, no queries) is left to the launchers.
+kp_status validate_compress(const kp_compress_args *a) {
     if (!a) return KP_ERR_INVALID_ARG;
     kp_status st = check_config(a->cfg);
     if (st != KP_OK) return st;
@@ -157,14 +160,10 @@ kp_status kp_kpool_compress(const kp_compress_args *a, kp_stream_t stream) {
         (a->gates && !aligned(a->gates, 8)) || (a->ape && !aligned(a->ape, 8)) ||
         (a->tail_gates && !aligned(a->tail_gates, 8)))
         return KP_ERR_INVALID_ARG;
-    return launch_compress(*a, reinterpret_cast<cudaStream_t>(stream));
+    return KP_OK;
 }
 
-size_t kp_score_workspace_size(int32_t num_queries) {
-    return score_plan_bytes(num_queries > 0 ? num_queries : 0);
-}
-
-kp_status kp_indexer_score(const kp_score_args *a, kp_stream_t stream) {
+kp_status validate_score(const kp_score_args *a) {
     if (!a) return KP_ERR_INVALID_ARG;
     kp_status st = check_config(a->cfg);
     if (st != KP_OK) return st;
@@ -175,13 +174,13 @@ kp_status kp_indexer_score(const kp_score_args *a, kp_stream_t stream) {
     if (!aligned(a->q_idx, 16) || !aligned(a->pooled, 16) || !aligned(a->w, 4) || !aligned(a->scores, 4))
         return KP_ERR_INVALID_ARG;
     if (a->score_stride < score_stride_for(a->q.max_pools)) return KP_ERR_INVALID_ARG;
-    if (!a->workspace || a->workspace_bytes < kp_score_workspace_size(a->q.num_queries) ||
+    if (!a->workspace || a->workspace_bytes < score_plan_bytes(a->q.num_queries) ||
         !aligned(a->workspace, 256))
         return KP_ERR_WORKSPACE;
-    return launch_score(*a, reinterpret_cast<cudaStream_t>(stream));
+    return KP_OK;
 }
 
-kp_status kp_topk_select(const kp_topk_args *a, kp_stream_t stream) {
+kp_status validate_topk(const kp_topk_args *a) {
     if (!a) return KP_ERR_INVALID_ARG;
     kp_status st = check_config(a->cfg);
     if (st != KP_OK) return st;
@@ -189,17 +188,17 @@ kp_status kp_topk_select(const kp_topk_args *a, kp_stream_t stream) {
     if (a->q.num_queries == 0) return KP_OK;
     if (!a->scores || !a->pool_idx || !a->n_sel) return KP_ERR_INVALID_ARG;
     if (a->score_stride < (a->q.max_pools > 0 ? a->q.max_pools : 1)) return KP_ERR_INVALID_ARG;
-    return launch_topk(*a, reinterpret_cast<cudaStream_t>(stream));
+    return KP_OK;
 }
 
-size_t kp_attend_workspace_size(const kp_config *cfg, int32_t num_queries) {
-    if (!cfg || cfg->kpool <= 0 || cfg->topk_tokens <= 0) return 256;
+size_t attend_ws_need(const kp_config &cfg, int32_t num_queries) {
+    if (cfg.kpool <= 0 || cfg.topk_tokens <= 0) return 256;
     int sms = device_sm_count();
     if (sms <= 0) sms = 148;
-    return attend_ws_bytes(*cfg, num_queries, attend_splits(*cfg, num_queries, sms));
+    return attend_ws_bytes(cfg, num_queries, attend_splits(cfg, num_queries, sms));
 }
 
-kp_status kp_sparse_mla_attend(const kp_attend_args *a, kp_stream_t stream) {
+kp_status validate_attend(const kp_attend_args *a) {
     if (!a) return KP_ERR_INVALID_ARG;
     kp_status st = check_config(a->cfg);
     if (st != KP_OK) return st;
@@ -208,9 +207,43 @@ kp_status kp_sparse_mla_attend(const kp_attend_args *a, kp_stream_t stream) {
     if (a->q.num_queries == 0) return KP_OK;
     if (!a->q_lat || !a->latent || !a->pool_idx || !a->n_sel || !a->out) return KP_ERR_INVALID_ARG;
     if (!aligned(a->q_lat, 16) || !aligned(a->latent, 16) || !aligned(a->out, 4)) return KP_ERR_INVALID_ARG;
-    const size_t need = kp_attend_workspace_size(&a->cfg, a->q.num_queries);
+    const size_t need = attend_ws_need(a->cfg, a->q.num_queries);
     if (need > 256 && (!a->workspace || a->workspace_bytes < need || !aligned(a->workspace, 256)))
         return KP_ERR_WORKSPACE;
+    return KP_OK;
+}
+}  // namespace
+
+kp_status kp_kpool_compress(const kp_compress_args *a, kp_stream_t stream) {
+    const kp_status st = validate_compress(a);
+    if (st != KP_OK || a->num_new == 0) return st;
+    return launch_compress(*a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t kp_score_workspace_size(int32_t num_queries) {
+    return score_plan_bytes(num_queries > 0 ? num_queries : 0);
+}
+
+kp_status kp_indexer_score(const kp_score_args *a, kp_stream_t stream) {
+    const kp_status st = validate_score(a);
+    if (st != KP_OK || a->q.num_queries == 0) return st;
+    return launch_score(*a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+kp_status kp_topk_select(const kp_topk_args *a, kp_stream_t stream) {
+    const kp_status st = validate_topk(a);
+    if (st != KP_OK || a->q.num_queries == 0) return st;
+    return launch_topk(*a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t kp_attend_workspace_size(const kp_config *cfg, int32_t num_queries) {
+    if (!cfg) return 256;
+    return attend_ws_need(*cfg, num_queries);
+}
+
+kp_status kp_sparse_mla_attend(const kp_attend_args *a, kp_stream_t stream) {
+    const kp_status st = validate_attend(a);
+    if (st != KP_OK || a->q.num_queries == 0) return st;
     return launch_attend(*a, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -294,10 +327,26 @@ kp_status kp_dsa_forward(const kp_forward_args *a, kp_stream_t stream) {
     at.workspace_bytes = L.total - L.scratch;
     at.d_status = a->d_status;
 
-    if ((st = kp_kpool_compress(&c, stream)) != KP_OK) return st;
-    if ((st = kp_indexer_score(&sc, stream)) != KP_OK) return st;
-    if ((st = kp_topk_select(&tk, stream)) != KP_OK) return st;
-    return kp_sparse_mla_attend(&at, stream);
+    if ((st = validate_compress(&c)) != KP_OK) return st;
+    if ((st = validate_score(&sc)) != KP_OK) return st;
+    if ((st = validate_topk(&tk)) != KP_OK) return st;
+    if ((st = validate_attend(&at)) != KP_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const bool queries = a->q.num_queries > 0;
+    // The scorer's plan is built by an extra CTA of the compression launch
+    // (one launch fewer), except when there is nothing to compress or no room
+    // for one more row of CTAs in gridDim.y.
+    if (c.num_new > 0 && queries && c.num_seqs < 65535) {
+        const ScorePlanArgs pa = score_plan_args(sc);
+        if ((st = launch_compress(c, s, &pa)) != KP_OK) return st;
+        if ((st = launch_score(sc, s, true)) != KP_OK) return st;
+    } else {
+        if (c.num_new > 0 && (st = launch_compress(c, s)) != KP_OK) return st;
+        if (queries && (st = launch_score(sc, s)) != KP_OK) return st;
+    }
+    if (!queries) return KP_OK;
+    if ((st = launch_topk(tk, s)) != KP_OK) return st;
+    return launch_attend(at, s);
 }
 
 const char *kp_status_string(kp_status s) {

@@ -15,16 +15,17 @@
 // B300 design.  The 64 heads of a query share every latent row (MQA-like),
 // so heads are the natural N of the tensor-core products and the gathered
 // tokens their M:
-//   S^T[tok, h] = C[tok, :512] . Q[h, :512]^T     M = 128 tokens, N = 64, K = 512
-//   O^T[d, h]  += C[tok, d]^T . P[tok, h]          M = 128 latent columns (x4), N = 64, K = 128 tokens
-// One 128-token tile of latent rows (128 KB) is gathered into shared memory
-// in the 128-byte-swizzle layout; the S product reads it K-major, the P.V
-// product reads the same bytes M-major, so each latent row crosses HBM once.
-// S (64 TMEM columns) and O^T (4 x 64 columns) live in TMEM.  Each softmax
-// thread owns one token (one TMEM lane): per-head tile maxima come from one
-// warp redux per head plus a 4-warp exchange; the running max is raised only
-// when a tile's max exceeds it by 2^8 (then O^T and the row sums are rescaled),
-// so the correction pass almost never runs.
+//   S^T[tok, h] = C[tok, :512] . Q[h, :512]^T     M = 64 tokens, N = 64, K = 512
+//   O^T[d, h]  += C[tok, d]^T . P[tok, h]          M = 128 latent columns (x4), N = 64, K = 64 tokens
+// 64-token tiles of latent rows (64 KB) are gathered into two shared-memory
+// slots in the 128-byte-swizzle layout, so the next tile streams in while
+// this one is computed; the S product reads a tile K-major, the P.V product
+// reads the same bytes M-major, so each latent row crosses HBM once.  S^T
+// (M = 64: token r in TMEM lane 32*(r/16) + r%16) and O^T (4 x 64 columns)
+// live in TMEM.  Each softmax thread owns one token: per-head tile maxima come
+// from one warp redux per head plus a 4-warp exchange; the running max is
+// raised only when a tile's max exceeds it by 2^8 (then O^T and the row sums
+// are rescaled), so the correction pass almost never runs.
 //
 // A query's token list is split over the CTAs of a thread-block cluster
 // (up to 8).  After its tiles, each CTA dumps its unnormalised O^T, running
@@ -35,12 +36,13 @@
 // fp32 lse.  No global scratch, no second launch.
 //
 // Warp roles (384 threads, one CTA per SM):
-//   warps 0-7  softmax: warp w owns TMEM lane quadrant w % 4 (32 tokens) and
-//              heads 32 * (w / 4) .. +31; then the O^T dump
+//   warps 0-7  softmax: warp w owns TMEM lane quadrant w % 4 (tokens 16(w%4) ..
+//              +15 in lanes 0-15) and heads 32 * (w / 4) .. +31; then the O^T dump
 //   warp 8     TMEM allocation, Q TMA, MMA issue (one lane)
 //   warps 9-11 gather: cp.async 16-byte pieces of the selected rows into the
 //              swizzled tile (each warp instruction moves two whole 256-byte
-//              row segments; warp g takes token pairs g, g+3, g+6, ...)
+//              row segments; warp g takes token pairs g, g+3, g+6, ...), up to
+//              two tiles in flight
 //   all        cluster merge and output
 #include "kp_common.cuh"
 #include "kp_internal.h"
@@ -49,14 +51,15 @@ namespace kp {
 
 namespace {
 
-constexpr int kAtTok = 128;                               // tokens per tile
+constexpr int kAtTok = 64;                                // tokens per tile
+constexpr int kAtSlots = 2;                               // tiles resident in shared memory
 constexpr int kAtChunks = 4;                              // 128-column chunks of a latent row
-constexpr int kAtBlockBytes = kAtTok * 128;               // [128 rows][64 bf16] swizzle block
-constexpr int kAtChunkBytes = 2 * kAtBlockBytes;          // 32 KB
-constexpr int kAtTileBytes = kAtChunks * kAtChunkBytes;   // 128 KB
+constexpr int kAtBlockBytes = kAtTok * 128;               // [64 rows][64 bf16] swizzle block, 8 KB
+constexpr int kAtChunkBytes = 2 * kAtBlockBytes;          // 16 KB
+constexpr int kAtTileBytes = kAtChunks * kAtChunkBytes;   // 64 KB
 constexpr int kAtQBlockBytes = kMlaHeads * 128;           // [64 heads][64 bf16] = 8 KB
 constexpr int kAtQBytes = 8 * kAtQBlockBytes;             // 64 KB
-constexpr int kAtPBytes = kAtTok * kMlaHeads * 2;         // 16 KB
+constexpr int kAtPBytes = kAtTok * kMlaHeads * 2;         // 8 KB per buffer (two buffers)
 constexpr int kAtMaxSplits = 8;
 constexpr int kAtMaxTail = kKpool - 1;
 constexpr int kAtSoftWarps = 8;
@@ -68,38 +71,48 @@ constexpr int kAtProdThreads = 32 * kAtProdWarps;
 constexpr int kAtThreads = 384;
 constexpr int kAtTmemCols = 512;
 constexpr uint32_t kAtOCol = 0;                           // O^T: chunk c at columns 64c .. 64c+63
-constexpr uint32_t kAtSCol = 256;                         // S^T: 64 columns
+constexpr uint32_t kAtSCol = 256;                         // S^T: two buffers of 64 columns
 constexpr float kAtRescaleLog2 = 8.f;                     // raise the running max only past 2^8
 
 // Shared memory (offsets from a 1024-aligned base).
 constexpr int kOffQ = 0;
-constexpr int kOffTile = kOffQ + kAtQBytes;               // also the O dump [64][512] fp32
-constexpr int kOffP = kOffTile + kAtTileBytes;
-constexpr int kOffMisc = kOffP + kAtPBytes;
-constexpr int kMiscRed = 0;                               // [4][64] f32
+constexpr int kOffTile = kOffQ + kAtQBytes;               // slots; also the O dump [64][512] fp32
+constexpr int kOffP = kOffTile + kAtSlots * kAtTileBytes;
+constexpr int kOffMisc = kOffP + 2 * kAtPBytes;
+constexpr int kMiscRed = 0;                               // [4][64] f32 per-quadrant tile maxima
 constexpr int kMiscMUsed = kMiscRed + 4 * 64 * 4;         // [64] f32 running max (log2 units)
 constexpr int kMiscFac = kMiscMUsed + 64 * 4;             // [64] f32 rescale factors of this tile
 constexpr int kMiscLSum = kMiscFac + 64 * 4;              // [64] f32 row sums
-constexpr int kMiscTail = kMiscLSum + 64 * 4;             // [3][512] bf16 tail rows
+constexpr int kMiscLPart = kMiscLSum + 64 * 4;            // [4][64] f32 row sums per lane quadrant
+constexpr int kMiscRecvM = kMiscLPart + 4 * 64 * 4;       // [8][64] f32 running max pushed by each split
+constexpr int kMiscRecvL = kMiscRecvM + 8 * 64 * 4;       // [8][64] f32 row sums pushed by each split
+constexpr int kMiscTail = kMiscRecvL + 8 * 64 * 4;        // [3][512] bf16 tail rows
 constexpr int kMiscZTail = kMiscTail + kAtMaxTail * kNopeDim * 2;   // [64][4] f32 tail logits
 constexpr int kMiscW = kMiscZTail + 64 * 4 * 4;           // [64][16] f32 merge weights
+constexpr int kMaxCtaPools = KP_MAX_TOPK_POOLS;          // selected pools one CTA can cover
+// [kMaxCtaPools] i32 this CTA's selected pools: read only during the tile loop,
+// so it shares bytes with the tail rows / tail logits / merge weights, which are
+// written only after it.
+constexpr int kMiscPools = kMiscTail;
+static_assert(kMaxCtaPools * 4 <= kMiscW + 64 * 16 * 4 - kMiscTail, "pool list overlaps past the merge buffers");
 constexpr int kMiscBars = kMiscW + 64 * 16 * 4;           // mbarriers
-constexpr int kNumBars = 13;
+constexpr int kNumBars = 23;
 constexpr int kMiscTmem = kMiscBars + kNumBars * 8;
 constexpr int kMiscAbort = kMiscTmem + 4;
 constexpr int kMiscBytes = kMiscAbort + 12;
 constexpr int kAtSmemBytes = kOffMisc + kMiscBytes + 1024;  // + alignment slack
 static_assert(kAtSmemBytes <= 232448, "attention shared memory over the per-CTA limit");
-static_assert(kAtTileBytes >= kMlaHeads * kNopeDim * 4, "O dump must fit in the tile region");
+static_assert(kAtSlots * kAtTileBytes >= kMlaHeads * kNopeDim * 4, "the merge buffer must fit in the tile slots");
 
 // mbarrier indices
-constexpr int kBarFull = 0;    // [4] chunk gathered (96 producer arrivals)
-constexpr int kBarFree = 4;    // [4] chunk consumed by P.V (tcgen05.commit)
-constexpr int kBarQ = 8;       // Q landed (TMA)
-constexpr int kBarS = 9;       // S^T ready (commit)
-constexpr int kBarP = 10;      // P written and O^T rescaled (256 softmax arrivals)
-constexpr int kBarO = 11;      // every MMA of the CTA done (commit)
-constexpr int kBarDrain = 12;  // teardown after an abort
+constexpr int kBarFull = 0;    // [slot][4] chunk gathered (96 producer arrivals)
+constexpr int kBarFree = 8;    // [slot][4] chunk consumed by P.V (tcgen05.commit)
+constexpr int kBarQ = 16;      // Q landed (TMA)
+constexpr int kBarS = 17;      // [2] S^T buffer ready (commit)
+constexpr int kBarP = 19;      // P written and O^T rescaled (256 softmax arrivals)
+constexpr int kBarO = 20;      // every MMA of the CTA done (commit)
+constexpr int kBarDrain = 21;  // teardown after an abort
+constexpr int kBarPV = 22;     // P.V of a tile done (commit): O^T is stable
 
 struct AttendParams {
     const uint16_t *latent;
@@ -137,6 +150,24 @@ __device__ __forceinline__ bool named_bar_all(int id, int count, bool v) {
     return r != 0;
 }
 
+// Named barrier that ORs a flag over the participating threads.
+__device__ __forceinline__ bool named_bar_any(int id, int count, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.or.pred p, %2, %3, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
 // Byte offset of element (row, col) of a [rows][64 bf16] 128-byte-swizzled block.
 __device__ __forceinline__ uint32_t sw128_off(int row, int col) {
     return static_cast<uint32_t>(row * 128 + ((((col >> 3) ^ row) & 7) << 4) + (col & 7) * 2);
@@ -157,6 +188,9 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     float *mused_s = reinterpret_cast<float *>(misc + kMiscMUsed);
     float *fac_s = reinterpret_cast<float *>(misc + kMiscFac);
     float *lsum_s = reinterpret_cast<float *>(misc + kMiscLSum);
+    float *lpart_s = reinterpret_cast<float *>(misc + kMiscLPart);
+    float *recvm_s = reinterpret_cast<float *>(misc + kMiscRecvM);
+    float *recvl_s = reinterpret_cast<float *>(misc + kMiscRecvL);
     uint16_t *tail_s = reinterpret_cast<uint16_t *>(misc + kMiscTail);
     float *ztail_s = reinterpret_cast<float *>(misc + kMiscZTail);
     float *wm_s = reinterpret_cast<float *>(misc + kMiscW);
@@ -169,46 +203,20 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int S = P.splits;
     const int q = blockIdx.x / S, split = blockIdx.x % S;
+    const int nh = kMlaHeads / S;   // heads this CTA merges (S divides 64)
+    const int h0 = nh * split;
 
-    // ---- what this query attends to
-    const int b = P.q_seq[q];
-    const int t = P.q_pos[q];
-    bool qvalid = true;
-    int nf = 0, ns = 0, n_tail = 0;
-    int64_t base_row = 0;
-    if (b < 0 || b >= P.num_seqs || t < 0) {
-        if (tid == 0) set_status(P.status, KP_ERR_DEVICE_BOUNDS);
-        qvalid = false;
-    } else {
-        nf = (t + 1) / kKpool;
-        ns = P.n_sel[q];
-        const int ns_max = min(P.K, nf);
-        if (ns < 0 || ns > ns_max) {
-            if (tid == 0) set_status(P.status, KP_ERR_DEVICE_BOUNDS);
-            ns = max(0, min(ns, ns_max));
-        }
-        n_tail = P.tail ? (t + 1) - nf * kKpool : 0;
-        base_row = P.latent_row_off[b];
-        if (base_row < 0 || base_row + t >= P.latent_rows) {
-            if (tid == 0) set_status(P.status, KP_ERR_DEVICE_BOUNDS);
-            qvalid = false;
-            ns = 0;
-            n_tail = 0;
-        }
-    }
-    const int n_pool_tok = ns * kKpool;
-    const int n_tiles = (n_pool_tok + kAtTok - 1) / kAtTok;
-    const int tb = n_tiles * split / S, te = n_tiles * (split + 1) / S;
-    const int nt = te - tb;
-
-    // ---- set-up
+    // ---- set-up, and what this query is: inputs no earlier kernel of the step
+    // writes, so they are read before the grid dependency resolves.
     if (tid == 0) {
-        for (int c = 0; c < kAtChunks; ++c) {
+        for (int c = 0; c < kAtSlots * kAtChunks; ++c) {
             mbar_init(bar(kBarFull + c), kAtProdThreads);
             mbar_init(bar(kBarFree + c), 1);
         }
         mbar_init(bar(kBarQ), 1);
         mbar_init(bar(kBarS), 1);
+        mbar_init(bar(kBarS + 1), 1);
+        mbar_init(bar(kBarPV), 1);
         mbar_init(bar(kBarP), kAtSoftThreads);
         mbar_init(bar(kBarO), 1);
         mbar_init(bar(kBarDrain), 1);
@@ -224,53 +232,105 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         tmem_alloc(smem_u32(tmem_s), kAtTmemCols);
         tmem_relinquish();
     }
+    const int b = P.q_seq[q];
+    const int t = P.q_pos[q];
+    bool qvalid = b >= 0 && b < P.num_seqs && t >= 0;
+    int64_t base_row = qvalid ? P.latent_row_off[b] : 0;
+    if (qvalid && (base_row < 0 || base_row + t >= P.latent_rows)) qvalid = false;
+    if (!qvalid && tid == 0) set_status(P.status, KP_ERR_DEVICE_BOUNDS);
+    const int nf = qvalid ? (t + 1) / kKpool : 0;
+    const int n_tail = (qvalid && P.tail) ? (t + 1) - nf * kKpool : 0;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_s;
+    if (tid == 32 * kAtMmaWarp && qvalid) {  // Q: 64 heads x 512 columns, 8 swizzled blocks
+        mbar_expect_tx(bar(kBarQ), kAtQBytes);
+        for (int blk = 0; blk < 8; ++blk)
+            tma_load_2d(sQ + blk * kAtQBlockBytes, &tm_q, bar(kBarQ), blk * 64, q * kMlaHeads);
+    }
+
+    // ---- the selection comes from the previous kernel
+    pdl_wait_then_release();
+    int ns = 0;
+    if (qvalid) {
+        ns = P.n_sel[q];
+        const int ns_max = min(P.K, nf);
+        if (ns < 0 || ns > ns_max) {
+            if (tid == 0) set_status(P.status, KP_ERR_DEVICE_BOUNDS);
+            ns = max(0, min(ns, ns_max));
+        }
+    }
+    const int n_pool_tok = ns * kKpool;
+    const int n_tiles = (n_pool_tok + kAtTok - 1) / kAtTok;
+    const int tb = n_tiles * split / S, te = n_tiles * (split + 1) / S;
+    const int nt = te - tb;
 
     if (warp == kAtMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
+        // Event-driven: S of the next tile, chunk by chunk as it lands, and P.V of
+        // the oldest softmaxed tile, whichever is ready first.
         if (lane == 0) {
-            if (qvalid) {
-                mbar_expect_tx(bar(kBarQ), kAtQBytes);
-                for (int blk = 0; blk < 8; ++blk)
-                    tma_load_2d(sQ + blk * kAtQBlockBytes, &tm_q, bar(kBarQ), blk * 64, q * kMlaHeads);
-            }
-            bool ok = true;
-            if (nt > 0) ok = mbar_wait(bar(kBarQ), 0, abort_flag, P.status);
-            const uint32_t idesc_s = idesc_bf16_f32(kAtTok, kMlaHeads);
-            const uint32_t idesc_pv = idesc_bf16_f32(kAtTok, kMlaHeads, true, true);
-            for (int jj = 0; ok && jj < nt; ++jj) {
-                const uint32_t par = jj & 1;
-                for (int c = 0; ok && c < kAtChunks; ++c) {
-                    if (!(ok = mbar_wait(bar(kBarFull + c), par, abort_flag, P.status))) break;
-                    tc_fence_after();
+            bool ok = nt == 0 || mbar_wait(bar(kBarQ), 0, abort_flag, P.status);
+            const uint32_t idesc_s = idesc_bf16_f32(kAtTok, kMlaHeads);             // M = 64
+            const uint32_t idesc_pv = idesc_bf16_f32(128, kMlaHeads, true, true);   // M = 128 columns
+            // Descriptors are built once; a step along K or to another block adds
+            // (bytes >> 4) to the start-address field (addresses stay < 256 KB).
+            const uint64_t dq0 = desc_sw128(sQ, 16, 1024);
+            const uint64_t dt0 = desc_sw128(sTile, 16, 1024);
+            // A of P.V = C^T, M-major: 64-column groups 8 KB apart, 8-token groups 1 KB apart.
+            const uint64_t dv0 = desc_sw128(sTile, kAtBlockBytes, 1024);
+            // B of P.V = P (tokens x heads), N-major, one 64-head group wide.
+            const uint64_t dp0 = desc_sw128(sP, 4096, 1024);
+            int next_s = 0, s_chunk = 0, next_pv = 0;
+            unsigned long long idle_since = 0;
+            while (ok && next_pv < nt) {
+                bool progressed = false;
+                if (next_s < nt && next_s < next_pv + 2) {
+                    const int slot = next_s & 1;
+                    if (mbar_try_wait(bar(kBarFull + slot * kAtChunks + s_chunk), (next_s >> 1) & 1)) {
+                        tc_fence_after();
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const int blk = 2 * c + (kk >> 2);
-                        const uint32_t koff = (kk & 3) * 32;
-                        const uint64_t ad = desc_sw128(sTile + blk * kAtBlockBytes + koff, 16, 1024);
-                        const uint64_t bd = desc_sw128(sQ + blk * kAtQBlockBytes + koff, 16, 1024);
-                        tc_mma_bf16(tmem + kAtSCol, ad, bd, idesc_s, (c | kk) ? 1u : 0u);
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint32_t blk = 2 * s_chunk + (kk >> 2), koff = (kk & 3) * 32;
+                            const uint64_t ad = dt0 + ((slot * kAtTileBytes + blk * kAtBlockBytes + koff) >> 4);
+                            const uint64_t bd = dq0 + ((blk * kAtQBlockBytes + koff) >> 4);
+                            tc_mma_bf16(tmem + kAtSCol + 64 * slot, ad, bd, idesc_s, (s_chunk | kk) ? 1u : 0u);
+                        }
+                        if (++s_chunk == kAtChunks) {
+                            tc_commit(bar(kBarS + slot));
+                            s_chunk = 0;
+                            ++next_s;
+                        }
+                        progressed = true;
                     }
                 }
-                if (!ok) break;
-                tc_commit(bar(kBarS));
-                if (!(ok = mbar_wait(bar(kBarP), par, abort_flag, P.status))) break;
-                tc_fence_after();
-                for (int c = 0; c < kAtChunks; ++c) {
+                if (next_pv < next_s && mbar_try_wait(bar(kBarP), next_pv & 1)) {
+                    const int slot = next_pv & 1;
+                    tc_fence_after();
+                    for (int c = 0; c < kAtChunks; ++c) {
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        // A = C^T (latent columns x tokens), M-major: 64-column groups 16 KB
-                        // apart, 8-token groups 1 KB apart.  B = P (tokens x heads), N-major.
-                        const uint64_t ad = desc_sw128(sTile + 2 * c * kAtBlockBytes + kk * 2048,
-                                                       kAtBlockBytes, 1024);
-                        // (B is one 64-head group wide, so its LBO is never stepped.)
-                        const uint64_t bd = desc_sw128(sP + kk * 2048, 8192, 1024);
-                        tc_mma_bf16(tmem + kAtOCol + 64 * c, ad, bd, idesc_pv, (jj | kk) ? 1u : 0u);
+                        for (int kk = 0; kk < kAtTok / 16; ++kk) {
+                            const uint64_t ad = dv0 + ((slot * kAtTileBytes + 2 * c * kAtBlockBytes + kk * 2048) >> 4);
+                            const uint64_t bd = dp0 + ((slot * kAtPBytes + kk * 2048) >> 4);
+                            tc_mma_bf16(tmem + kAtOCol + 64 * c, ad, bd, idesc_pv, (next_pv | kk) ? 1u : 0u);
+                        }
+                        tc_commit(bar(kBarFree + slot * kAtChunks + c));
                     }
-                    tc_commit(bar(kBarFree + c));
+                    tc_commit(bar(kBarPV));
+                    ++next_pv;
+                    progressed = true;
+                }
+                if (progressed) {
+                    idle_since = 0;
+                } else {
+                    const unsigned long long now = globaltimer_ns();
+                    if (idle_since == 0) idle_since = now;
+                    if (*abort_flag || now - idle_since > KP_WAIT_NS) {
+                        set_status(P.status, KP_ERR_DEVICE_TIMEOUT);
+                        *abort_flag = 1;
+                        ok = false;
+                    }
                 }
             }
             if (ok) {
@@ -287,123 +347,159 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         // ------------------------------------------------------------ gather
         const int pw = warp - kAtProdWarp0;
         const int piece = lane & 15, sub = lane >> 4;
-        // Token pairs (2k, 2k+1), k = pw + 3m, m < n_pairs; list index j = 2m + sub.
-        const int n_pairs = (64 - pw + kAtProdWarps - 1) / kAtProdWarps;
-        auto row_of = [&](int tile, int j) -> int64_t {
-            if (j >= 2 * n_pairs) return -1;
-            const int tok = tile * kAtTok + 2 * (pw + kAtProdWarps * (j >> 1)) + (j & 1);
-            if (tok >= n_pool_tok) return -1;
-            const int p = P.pool_idx[static_cast<int64_t>(q) * P.K + tok / kKpool];
-            if (p < 0 || p >= nf) {
-                set_status(P.status, KP_ERR_DEVICE_BOUNDS);
-                return -1;
-            }
-            return base_row + static_cast<int64_t>(p) * kKpool + (tok % kKpool);
-        };
-        for (int jj = 0; jj < nt; ++jj) {
-            const int tile = tb + jj;
-            const int64_t row0 = row_of(tile, lane), row1 = row_of(tile, lane + 32);
-            bool ok = true;
-            for (int c = 0; c < kAtChunks; ++c) {
-                if (jj > 0 && !(ok = mbar_wait(bar(kBarFree + c), (jj - 1) & 1, abort_flag, P.status)))
-                    break;
-                for (int m = 0; m < n_pairs; ++m) {
-                    const int tk = 2 * (pw + kAtProdWarps * m) + sub;
-                    const int64_t r = __shfl_sync(0xffffffffu, m < 16 ? row0 : row1, (2 * m + sub) & 31);
-                    const uint16_t *src = P.latent + (r < 0 ? 0 : r) * kLatentDim + c * 128 + piece * 8;
-                    const uint32_t dst = sTile + (2 * c + (piece >> 3)) * kAtBlockBytes + tk * 128 +
-                                         (((piece & 7) ^ (tk & 7)) << 4);
-                    cp_async_16(dst, src, r < 0 ? 0u : 16u);
+        // Token pairs (2k, 2k+1) of a tile, k = pw + 3m, m < n_pairs; list index j = 2m + sub.
+        constexpr int kPairs = kAtTok / 2;
+        const int n_pairs = (kPairs - pw + kAtProdWarps - 1) / kAtProdWarps;
+        bool ok = true;
+        // This CTA's selected pools, once, into shared memory (no global read
+        // sits between a freed slot and its refill).
+        int32_t *pools_s = reinterpret_cast<int32_t *>(misc + kMiscPools);
+        const int pool0 = tb * (kAtTok / kKpool);
+        const int npools = min(nt * (kAtTok / kKpool), ns - pool0);
+        for (int k = tid - 32 * kAtProdWarp0; k < npools; k += kAtProdThreads)
+            pools_s[k] = P.pool_idx[static_cast<int64_t>(q) * P.K + pool0 + k];
+        named_bar(2, kAtProdThreads);
+        // Issues the 4 chunk groups of tile jj into its slot (waiting for the
+        // slot's previous tile to be consumed by P.V).
+        auto issue = [&](int jj) {
+            const int tile = tb + jj, slot = jj & 1;
+            int64_t row = -1;
+            if (lane < 2 * n_pairs) {
+                const int tok = tile * kAtTok + 2 * (pw + kAtProdWarps * (lane >> 1)) + (lane & 1);
+                if (tok < n_pool_tok) {
+                    const int p = pools_s[tok / kKpool - pool0];
+                    if (p >= 0 && p < nf) row = base_row + static_cast<int64_t>(p) * kKpool + (tok % kKpool);
+                    else set_status(P.status, KP_ERR_DEVICE_BOUNDS);
                 }
-                cp_async_commit();
             }
-            if (!ok) {
-                cp_async_wait<0>();
-                break;
+            const uint32_t dst0 = sTile + slot * kAtTileBytes;
+            for (int c = 0; c < kAtChunks; ++c) {
+                if (ok && jj >= 2)
+                    ok = mbar_wait(bar(kBarFree + slot * kAtChunks + c), ((jj >> 1) - 1) & 1, abort_flag, P.status);
+                if (ok) {
+                    for (int m = 0; m < n_pairs; ++m) {
+                        const int tk = 2 * (pw + kAtProdWarps * m) + sub;
+                        const int64_t r = __shfl_sync(0xffffffffu, row, 2 * m + sub);
+                        const uint16_t *src = P.latent + (r < 0 ? 0 : r) * kLatentDim + c * 128 + piece * 8;
+                        const uint32_t dst = dst0 + (2 * c + (piece >> 3)) * kAtBlockBytes + tk * 128 +
+                                             (((piece & 7) ^ (tk & 7)) << 4);
+                        cp_async_16(dst, src, r < 0 ? 0u : 16u);
+                    }
+                }
+                cp_async_commit();  // always 4 groups per tile, so the counts below hold
             }
-            // Chunk c is complete once at most 3 - c newer groups are pending.
-            cp_async_wait<3>();
-            fence_proxy_async_smem();
-            mbar_arrive(bar(kBarFull + 0));
-            cp_async_wait<2>();
-            fence_proxy_async_smem();
-            mbar_arrive(bar(kBarFull + 1));
-            cp_async_wait<1>();
-            fence_proxy_async_smem();
-            mbar_arrive(bar(kBarFull + 2));
-            cp_async_wait<0>();
-            fence_proxy_async_smem();
-            mbar_arrive(bar(kBarFull + 3));
+        };
+        // Signals each chunk of tile jj once it has landed; `newer` = 4 when the
+        // next tile's 4 groups were issued after it.
+        auto complete = [&](int jj, bool newer) {
+            const uint32_t fb = bar(kBarFull + (jj & 1) * kAtChunks);
+            if (newer) {
+                cp_async_wait<7>(); fence_proxy_async_smem(); if (ok) mbar_arrive(fb);
+                cp_async_wait<6>(); fence_proxy_async_smem(); if (ok) mbar_arrive(fb + 8);
+                cp_async_wait<5>(); fence_proxy_async_smem(); if (ok) mbar_arrive(fb + 16);
+                cp_async_wait<4>(); fence_proxy_async_smem(); if (ok) mbar_arrive(fb + 24);
+            } else {
+                cp_async_wait<3>(); fence_proxy_async_smem(); if (ok) mbar_arrive(fb);
+                cp_async_wait<2>(); fence_proxy_async_smem(); if (ok) mbar_arrive(fb + 8);
+                cp_async_wait<1>(); fence_proxy_async_smem(); if (ok) mbar_arrive(fb + 16);
+                cp_async_wait<0>(); fence_proxy_async_smem(); if (ok) mbar_arrive(fb + 24);
+            }
+        };
+        // Both slots are filled up front; afterwards tile jj+2 is issued as soon
+        // as P.V of tile jj frees its slot, and signalled as soon as it lands.
+        if (nt > 0) issue(0);
+        if (nt > 1) issue(1);
+        if (nt > 0) complete(0, nt > 1);
+        if (nt > 1) complete(1, false);
+        for (int jj = 0; ok && jj + 2 < nt; ++jj) {
+            issue(jj + 2);
+            complete(jj + 2, false);
         }
+        cp_async_wait<0>();
     } else {
         // ------------------------------------------------------------ softmax
         const int quad = warp & 3, half = warp >> 2;
-        const int i = quad * 32 + lane;  // token lane of the tile
-        const int hb = half * 32;        // this warp's first head
+        const bool has_tok = lane < 16;              // M = 64: lanes 0-15 of each quadrant
+        const int i = quad * 16 + (lane & 15);       // token of the tile
+        const int hb = half * 32;                    // this warp's first head
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-        float lp[32];                    // running row-sum partials, heads hb .. hb+31
+        float lp[32];  // row-sum partials, heads hb .. hb+31 (the running max is in mused_s)
 #pragma unroll
         for (int h = 0; h < 32; ++h) lp[h] = 0.f;
         bool ok = true;
         for (int jj = 0; jj < nt; ++jj) {
-            ok = named_bar_all(1, kAtSoftThreads, mbar_wait(bar(kBarS), jj & 1, abort_flag, P.status));
+            ok = named_bar_all(1, kAtSoftThreads,
+                               mbar_wait(bar(kBarS + (jj & 1)), (jj >> 1) & 1, abort_flag, P.status));
             if (!ok) break;
             tc_fence_after();
             uint32_t r[32];
-            tmem_ld_32x32b_x32(tmem + lane_base + kAtSCol + hb, r);
+            tmem_ld_32x32b_x32(tmem + lane_base + kAtSCol + 64 * (jj & 1) + hb, r);
             tmem_ld_wait();
             const int n_valid = min(kAtTok, n_pool_tok - (tb + jj) * kAtTok);
-            const bool valid = i < n_valid;
+            const bool valid = has_tok && i < n_valid;
             float x[32];
-#pragma unroll
-            for (int h = 0; h < 32; ++h) {
-                x[h] = valid ? __uint_as_float(r[h]) * P.scale_log2 : -INFINITY;
-                const float m = warp_max_f32(x[h]);
-                if (lane == h) red_s[quad * 64 + hb + h] = m;
-            }
-            named_bar(1, kAtSoftThreads);
-            if (tid < kMlaHeads) {
-                const float mt = fmaxf(fmaxf(red_s[tid], red_s[64 + tid]), fmaxf(red_s[128 + tid], red_s[192 + tid]));
-                const float mo = mused_s[tid];
-                if (mt > mo + kAtRescaleLog2) {
-                    mused_s[tid] = mt;
-                    fac_s[tid] = exp2f(mo - mt);  // 0 on the first tile (mo = -inf)
-                } else {
-                    fac_s[tid] = 1.f;
-                }
-            }
-            named_bar(1, kAtSoftThreads);
-            bool any = false;
+            bool high = false;  // a logit more than 2^8 above the running max
 #pragma unroll
             for (int h = 0; h < 32; h += 4) {
-                const float4 f = *reinterpret_cast<const float4 *>(fac_s + hb + h);
-                lp[h] *= f.x;
-                lp[h + 1] *= f.y;
-                lp[h + 2] *= f.z;
-                lp[h + 3] *= f.w;
-                any |= (f.x != 1.f) | (f.y != 1.f) | (f.z != 1.f) | (f.w != 1.f);
+                const float4 m4 = *reinterpret_cast<const float4 *>(mused_s + hb + h);
+                x[h] = valid ? __uint_as_float(r[h]) * P.scale_log2 : -INFINITY;
+                x[h + 1] = valid ? __uint_as_float(r[h + 1]) * P.scale_log2 : -INFINITY;
+                x[h + 2] = valid ? __uint_as_float(r[h + 2]) * P.scale_log2 : -INFINITY;
+                x[h + 3] = valid ? __uint_as_float(r[h + 3]) * P.scale_log2 : -INFINITY;
+                high |= (x[h] > m4.x + kAtRescaleLog2) | (x[h + 1] > m4.y + kAtRescaleLog2) |
+                        (x[h + 2] > m4.z + kAtRescaleLog2) | (x[h + 3] > m4.w + kAtRescaleLog2);
+            }
+            bool rescale = false;
+            if (named_bar_any(1, kAtSoftThreads, high)) {
+                // Slow path (the first tile, and whenever a head's max jumps): exact
+                // per-head tile max, raise the running max, rescale O^T and row sums.
+#pragma unroll
+                for (int h = 0; h < 32; ++h) {
+                    const float m = warp_max_f32(x[h]);
+                    if (lane == h) red_s[quad * 64 + hb + h] = m;
+                }
+                named_bar(1, kAtSoftThreads);
+                if (tid < kMlaHeads) {
+                    const float mt = fmaxf(fmaxf(red_s[tid], red_s[64 + tid]), fmaxf(red_s[128 + tid], red_s[192 + tid]));
+                    const float mo = mused_s[tid];
+                    if (mt > mo + kAtRescaleLog2) {
+                        mused_s[tid] = mt;
+                        fac_s[tid] = exp2f(mo - mt);  // 0 when mo = -inf
+                    } else {
+                        fac_s[tid] = 1.f;
+                    }
+                }
+                named_bar(1, kAtSoftThreads);
+#pragma unroll
+                for (int h = 0; h < 32; ++h) lp[h] *= fac_s[hb + h];
+                rescale = jj > 0;
             }
             // p = 2^(x - m), row partial sums, bf16 P (token i, heads hb..hb+31), swizzled.
-            uint8_t *prow = smem + kOffP + i * 128;
+            if (has_tok) {
+                uint8_t *prow = smem + kOffP + (jj & 1) * kAtPBytes + i * 128;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                uint32_t pk[4];
+                for (int k = 0; k < 4; ++k) {
+                    uint32_t pk[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int h = 8 * k + 2 * e;
-                    const float2 m2 = *reinterpret_cast<const float2 *>(mused_s + hb + h);
-                    const float p0 = exp2f(x[h] - m2.x);
-                    const float p1 = exp2f(x[h + 1] - m2.y);
-                    lp[h] += p0;
-                    lp[h + 1] += p1;
-                    pk[e] = pack_bf16x2(p0, p1);
+                    for (int e = 0; e < 4; ++e) {
+                        const int h = 8 * k + 2 * e;
+                        const float2 m2 = *reinterpret_cast<const float2 *>(mused_s + hb + h);
+                        const float p0 = exp2f(x[h] - m2.x);
+                        const float p1 = exp2f(x[h + 1] - m2.y);
+                        lp[h] += p0;
+                        lp[h + 1] += p1;
+                        pk[e] = pack_bf16x2(p0, p1);
+                    }
+                    const int chunk = 4 * half + k;
+                    *reinterpret_cast<uint4 *>(prow + ((chunk ^ (i & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
                 }
-                const int chunk = 4 * half + k;
-                *reinterpret_cast<uint4 *>(prow + ((chunk ^ (i & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
             }
-            if (any && jj > 0) {
-                // O^T is stable here: every P.V of the previous tile completed before S^T.
-                // (Done after P so that the logits' registers are free.)
+            if (rescale) {
+                // O^T must hold P.V of the previous tile before it is rescaled; P.V of
+                // this tile waits for our arrival below.  (After P, so that the
+                // logits' registers are free.)
+                mbar_wait(bar(kBarPV), (jj - 1) & 1, abort_flag, P.status);
+                tc_fence_after();
                 for (int c = 0; c < kAtChunks; ++c) {
                     uint32_t o[32];
                     const uint32_t ta = tmem + lane_base + kAtOCol + 64 * c + hb;
@@ -419,23 +515,11 @@ __global__ void __launch_bounds__(kAtThreads, 1)
             tc_fence_before();
             mbar_arrive(bar(kBarP));
         }
-        // ---- after the last tile: O^T -> shared memory as O[h][d] (fp32, unnormalised)
         if (ok) ok = named_bar_all(1, kAtSoftThreads, mbar_wait(bar(kBarO), 0, abort_flag, P.status));
         if (ok) {
             tc_fence_after();
-            if (nt > 0) {
-                float *odump = reinterpret_cast<float *>(smem + kOffTile);
-                for (int c = 0; c < kAtChunks; ++c) {
-                    uint32_t o[32];
-                    tmem_ld_32x32b_x32(tmem + lane_base + kAtOCol + 64 * c + hb, o);
-                    tmem_ld_wait();
-                    const int d = c * 128 + i;
-#pragma unroll
-                    for (int h = 0; h < 32; ++h) odump[(hb + h) * kNopeDim + d] = __uint_as_float(o[h]);
-                }
-            }
             // Row sums: transpose-reduce the 32 per-thread partials over the warp
-            // (lane l ends with head hb + l), then add the 4 quadrants.
+            // (lane l ends with head hb + l); the quadrants are added in order below.
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const bool hi = lane & 16;
@@ -470,17 +554,49 @@ __global__ void __launch_bounds__(kAtThreads, 1)
                 const float keep = hi ? lp[1] : lp[0];
                 lp[0] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
             }
-            atomicAdd(lsum_s + hb + lane, lp[0]);
+            lpart_s[quad * 64 + hb + lane] = lp[0];
         }
     }
 
-    // ---- merge over the cluster, tail tokens, output
+    // ---- merge over the cluster: every CTA pushes its unnormalised O^T, running
+    // max and row sums into the shared memory of the CTA that owns each head,
+    // then every CTA merges its own heads from local memory.
     tc_fence_before();
     __syncthreads();
-    if (S > 1) cluster_barrier();
-
-    const int h0 = kMlaHeads * split / S, h1 = kMlaHeads * (split + 1) / S, nh = h1 - h0;
+    if (tid < kMlaHeads && nt > 0)  // row sums in a fixed order: repeated calls give the same bits
+        lsum_s[tid] = (lpart_s[tid] + lpart_s[64 + tid]) + (lpart_s[128 + tid] + lpart_s[192 + tid]);
+    if (S > 1) cluster_barrier();  // every CTA is done with its tile slots, which receive the pushes
+    else __syncthreads();
     const bool aborted = *abort_flag != 0;
+    const uint32_t recv_o = sbase + kOffTile;  // [S][nh][512] f32
+    if (!aborted) {
+        if (tid < kMlaHeads) {
+            const int owner = tid / nh, hl = tid % nh;
+            st_cluster_f32(dsmem_addr(smem_u32(recvm_s + split * 64 + hl), owner), nt > 0 ? mused_s[tid] : -INFINITY);
+            st_cluster_f32(dsmem_addr(smem_u32(recvl_s + split * 64 + hl), owner), nt > 0 ? lsum_s[tid] : 0.f);
+        }
+        if (warp < kAtSoftWarps && nt > 0) {
+            tc_fence_after();
+            const int quad = warp & 3, hb = (warp >> 2) * 32;
+            const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+            const int lg = 31 - __clz(nh);
+            for (int c = 0; c < kAtChunks; ++c) {
+                uint32_t o[32];
+                tmem_ld_32x32b_x32(tmem + lane_base + kAtOCol + 64 * c + hb, o);
+                tmem_ld_wait();
+                const int d = c * 128 + quad * 32 + lane;  // O^T rows are latent columns
+#pragma unroll
+                for (int h = 0; h < 32; ++h) {
+                    const int hg = hb + h, owner = hg >> lg, hl = hg & (nh - 1);
+                    st_cluster_f32(dsmem_addr(recv_o + ((split * nh + hl) * kNopeDim + d) * 4, owner),
+                                   __uint_as_float(o[h]));
+                }
+            }
+        }
+    }
+    if (S > 1) cluster_barrier();  // every push has landed
+    else __syncthreads();
+
     if (qvalid && !aborted) {
         // tail rows -> shared memory
         for (int k = tid; k < n_tail * 64; k += kAtThreads) {
@@ -517,20 +633,15 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         if (tid < nh) {
             const int h = h0 + tid;
             float M = -INFINITY;
-            for (int s = 0; s < S; ++s) M = fmaxf(M, dsmem_ld_f32(dsmem_addr(smem_u32(mused_s + h), s)));
+            for (int s2 = 0; s2 < S; ++s2) M = fmaxf(M, recvm_s[s2 * 64 + tid]);
             for (int j = 0; j < n_tail; ++j) M = fmaxf(M, ztail_s[h * 4 + j]);
             float L = 0.f;
             float *w = wm_s + tid * 16;
-            for (int s = 0; s < kAtMaxSplits; ++s) {
-                float ws = 0.f;
-                if (s < S) {
-                    const float ms = dsmem_ld_f32(dsmem_addr(smem_u32(mused_s + h), s));
-                    if (ms > -INFINITY) {
-                        ws = exp2f(ms - M);
-                        L += ws * dsmem_ld_f32(dsmem_addr(smem_u32(lsum_s + h), s));
-                    }
-                }
-                w[s] = ws;
+            for (int s2 = 0; s2 < kAtMaxSplits; ++s2) {
+                const float ms = s2 < S ? recvm_s[s2 * 64 + tid] : -INFINITY;
+                const float ws = ms > -INFINITY ? exp2f(ms - M) : 0.f;
+                w[s2] = ws;
+                if (ws > 0.f) L += ws * recvl_s[s2 * 64 + tid];
             }
             for (int j = 0; j < kAtMaxTail; ++j) {
                 const float wt = j < n_tail ? exp2f(ztail_s[h * 4 + j] - M) : 0.f;
@@ -538,30 +649,38 @@ __global__ void __launch_bounds__(kAtThreads, 1)
                 L += wt;
             }
             w[12] = L > 0.f ? 1.f / L : 0.f;
-            if (P.lse) P.lse[static_cast<int64_t>(q) * kMlaHeads + h] = L > 0.f ? (M + log2f(L)) * 0.69314718055994530942f : -INFINITY;
+            if (P.lse)
+                P.lse[static_cast<int64_t>(q) * kMlaHeads + h] =
+                    L > 0.f ? (M + log2f(L)) * 0.69314718055994530942f : -INFINITY;
         }
         __syncthreads();
-        // out[q][h][d] = (sum_s w_s O_s[h][d] + sum_j w_j c_j[d]) / L
-        const uint32_t odump_addr = sbase + kOffTile;
-        for (int idx = tid; idx < nh * (kNopeDim / 2); idx += kAtThreads) {
-            const int hl = idx / (kNopeDim / 2), d = 2 * (idx % (kNopeDim / 2));
-            const int h = h0 + hl;
+        // out[q][h][d] = (sum_s w_s O_s[h][d] + sum_j w_j c_j[d]) / L, 4 columns per item
+        const float *recv = reinterpret_cast<const float *>(smem + kOffTile);
+        for (int idx = tid; idx < nh * (kNopeDim / 4); idx += kAtThreads) {
+            const int hl = idx / (kNopeDim / 4), d = 4 * (idx % (kNopeDim / 4));
             const float *w = wm_s + hl * 16;
-            float a0 = 0.f, a1 = 0.f;
-            for (int s = 0; s < S; ++s) {
-                if (w[s] > 0.f) {
-                    const float2 v = dsmem_ld_f32x2(dsmem_addr(odump_addr + (h * kNopeDim + d) * 4, s));
-                    a0 = fmaf(w[s], v.x, a0);
-                    a1 = fmaf(w[s], v.y, a1);
+            float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int s2 = 0; s2 < S; ++s2) {
+                const float ws = w[s2];
+                if (ws > 0.f) {
+                    const float4 v = *reinterpret_cast<const float4 *>(recv + (s2 * nh + hl) * kNopeDim + d);
+                    a.x = fmaf(ws, v.x, a.x);
+                    a.y = fmaf(ws, v.y, a.y);
+                    a.z = fmaf(ws, v.z, a.z);
+                    a.w = fmaf(ws, v.w, a.w);
                 }
             }
             for (int j = 0; j < n_tail; ++j) {
-                const uint32_t cv = *reinterpret_cast<const uint32_t *>(tail_s + j * kNopeDim + d);
-                a0 = fmaf(w[8 + j], bf16_lo(cv), a0);
-                a1 = fmaf(w[8 + j], bf16_hi(cv), a1);
+                const uint2 cv = *reinterpret_cast<const uint2 *>(tail_s + j * kNopeDim + d);
+                const float wt = w[8 + j];
+                a.x = fmaf(wt, bf16_lo(cv.x), a.x);
+                a.y = fmaf(wt, bf16_hi(cv.x), a.y);
+                a.z = fmaf(wt, bf16_lo(cv.y), a.z);
+                a.w = fmaf(wt, bf16_hi(cv.y), a.w);
             }
-            *reinterpret_cast<uint32_t *>(P.out + (static_cast<int64_t>(q) * kMlaHeads + h) * kNopeDim + d) =
-                pack_bf16x2(a0 * w[12], a1 * w[12]);
+            const float il = w[12];
+            *reinterpret_cast<uint2 *>(P.out + (static_cast<int64_t>(q) * kMlaHeads + h0 + hl) * kNopeDim + d) =
+                make_uint2(pack_bf16x2(a.x * il, a.y * il), pack_bf16x2(a.z * il, a.w * il));
         }
     } else if (!qvalid && !aborted) {
         // Nothing to attend: out = 0, lse = -inf.
@@ -572,9 +691,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         if (P.lse && tid < nh) P.lse[static_cast<int64_t>(q) * kMlaHeads + h0 + tid] = -INFINITY;
     }
 
-    // Peers may still read this CTA's shared memory until everyone is done.
-    if (S > 1) cluster_barrier();
-    if (aborted && qvalid && tid == 0) mbar_wait(bar(kBarQ), 0, nullptr, P.status);  // no TMA left in flight
+    if (qvalid && aborted && tid == 0) mbar_wait(bar(kBarQ), 0, nullptr, P.status);  // no TMA left in flight
     tc_fence_before();
     __syncthreads();
     if (warp == kAtMmaWarp) {
@@ -626,15 +743,14 @@ bool attend_smem_configured() {
 
 }  // namespace
 
-// Splits of one query's token list = CTAs of its cluster: as many as keep
-// every cluster resident in one wave, at most 8, at most one per tile.
+// Splits of one query's token list = CTAs of its cluster: a power of two (the
+// merge gives each CTA 64 / splits heads), at most 8, at most one per tile, and
+// no more than keep the grid within the SMs.
 int attend_splits(const kp_config &cfg, int32_t num_queries, int sm_count) {
     if (num_queries <= 0) return 1;
     const int tiles = (cfg.topk_tokens + kAtTok - 1) / kAtTok;
-    int s = sm_count / num_queries;
-    if (s > kAtMaxSplits) s = kAtMaxSplits;
-    if (s > tiles) s = tiles;
-    if (s < 1) s = 1;
+    int s = 1;
+    while (s * 2 <= kAtMaxSplits && s * 2 <= tiles && static_cast<int64_t>(num_queries) * s * 2 <= sm_count) s *= 2;
     return s;
 }
 
@@ -652,7 +768,7 @@ kp_status launch_attend(const kp_attend_args &a, cudaStream_t s) {
     if (sms <= 0) return KP_ERR_CUDA;
     if (!attend_smem_configured()) return KP_ERR_CUDA;
     int splits = attend_splits(a.cfg, nq, sms);
-    while (splits > 1 && max_active_clusters(splits) < nq) --splits;
+    while (splits > 1 && max_active_clusters(splits) < nq) splits /= 2;
 
     CUtensorMap tm_q;
     if (!make_tmap_bf16_sw128(&tm_q, a.q_lat, kLatentDim, static_cast<uint64_t>(nq) * kMlaHeads,
@@ -675,24 +791,9 @@ kp_status launch_attend(const kp_attend_args &a, cudaStream_t s) {
     P.splits = splits;
     P.status = a.d_status;
 
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(nq) * splits);
-    cfg.blockDim = dim3(kAtThreads);
-    cfg.dynamicSmemBytes = kAtSmemBytes;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = splits;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, sparse_mla_tc_kernel, tm_q, P);
-    if (e != cudaSuccess) {
-        record_cuda_error("cudaLaunchKernelEx(sparse_mla_tc_kernel)", e);
-        return KP_ERR_CUDA;
-    }
-    return check_launch("sparse_mla_tc_kernel");
+    return launch_kernel("sparse_mla_tc_kernel", sparse_mla_tc_kernel,
+                         LaunchCfg(dim3(static_cast<unsigned>(nq) * splits), dim3(kAtThreads), kAtSmemBytes, s, splits),
+                         tm_q, P);
 }
 
 }  // namespace kp

@@ -22,6 +22,7 @@
 // ring rows; it reads before it writes, so no other warp can race with it.
 #include "kp_common.cuh"
 #include "kp_internal.h"
+#include "score_plan.cuh"
 
 namespace kp {
 
@@ -49,8 +50,16 @@ __global__ void __launch_bounds__(kCompressWarps * 32)
                           const uint16_t *__restrict__ gates, const uint16_t *__restrict__ ape,
                           uint16_t *__restrict__ tail_keys, uint16_t *__restrict__ tail_gates,
                           uint16_t *__restrict__ pooled, const int64_t *__restrict__ pool_row_off,
-                          int64_t pool_rows, int32_t *status) {
+                          int64_t pool_rows, int32_t *status, ScorePlanArgs plan) {
     constexpr int R = kKpool - 1;  // ring slots per sequence
+    __shared__ int scratch[33];
+    pdl_wait_then_release();
+    if (plan.plan && blockIdx.y == gridDim.y - 1) {  // the extra row of CTAs: the scorer's plan
+        if (blockIdx.x == 0)
+            build_score_plan(plan.nq, plan.num_seqs, plan.q_seq, plan.q_pos, plan.max_tiles, plan.plan,
+                             plan.status, scratch);
+        return;
+    }
     const int b = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int item = blockIdx.x * kCompressWarps + warp;
@@ -144,14 +153,16 @@ __global__ void __launch_bounds__(kCompressWarps * 32)
 
 }  // namespace
 
-kp_status launch_compress(const kp_compress_args &a, cudaStream_t s) {
+kp_status launch_compress(const kp_compress_args &a, cudaStream_t s, const ScorePlanArgs *plan) {
     if (a.num_new == 0) return KP_OK;
     const int max_items = (a.max_new_per_seq + kKpool - 1) / kKpool + 1;
-    dim3 grid((max_items + kCompressWarps - 1) / kCompressWarps, a.num_seqs);
-    kpool_compress_kernel<<<grid, kCompressWarps * 32, 0, s>>>(
-        a.cfg.compress_mode, a.prev_len, a.new_off, a.keys, a.gates, a.ape, a.tail_keys,
-        a.tail_gates, a.pooled, a.pool_row_off, a.pool_rows, a.d_status);
-    return check_launch("kpool_compress_kernel");
+    ScorePlanArgs pa{};
+    if (plan) pa = *plan;
+    dim3 grid((max_items + kCompressWarps - 1) / kCompressWarps, a.num_seqs + (pa.plan ? 1 : 0));
+    return launch_kernel("kpool_compress_kernel", kpool_compress_kernel,
+                         LaunchCfg(grid, dim3(kCompressWarps * 32), 0, s), a.cfg.compress_mode, a.prev_len,
+                         a.new_off, a.keys, a.gates, a.ape, a.tail_keys, a.tail_gates, a.pooled, a.pool_row_off,
+                         a.pool_rows, a.d_status, pa);
 }
 
 }  // namespace kp

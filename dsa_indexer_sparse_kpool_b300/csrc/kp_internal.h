@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "kpool_dsa.h"
 
 namespace kp {
@@ -26,14 +28,68 @@ int device_sm_count();
 bool make_tmap_bf16_sw128(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows,
                           uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows);
 
+// Launch configuration with programmatic stream serialisation (the kernel
+// may start while the previous kernel of the stream drains; it waits in
+// pdl_wait_then_release before touching memory) and, when cluster_x > 1, a
+// 1-D thread-block cluster.  `attrs` must outlive the launch call.
+struct LaunchCfg {
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attrs[2];
+    LaunchCfg(dim3 grid, dim3 block, size_t smem, cudaStream_t s, int cluster_x = 1) {
+        cfg = cudaLaunchConfig_t{};
+        cfg.gridDim = grid;
+        cfg.blockDim = block;
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = s;
+        int n = 0;
+        attrs[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attrs[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+        if (cluster_x > 1) {
+            attrs[n].id = cudaLaunchAttributeClusterDimension;
+            attrs[n].val.clusterDim.x = static_cast<unsigned>(cluster_x);
+            attrs[n].val.clusterDim.y = 1;
+            attrs[n].val.clusterDim.z = 1;
+            ++n;
+        }
+        cfg.attrs = attrs;
+        cfg.numAttrs = n;
+    }
+};
+
+// Launches a kernel with LaunchCfg; KP_ERR_CUDA (error recorded) on failure.
+template <typename... KArgs, typename... Args>
+kp_status launch_kernel(const char *name, void (*kernel)(KArgs...), const LaunchCfg &lc, Args &&...args) {
+    const cudaError_t e = cudaLaunchKernelEx(&lc.cfg, kernel, std::forward<Args>(args)...);
+    if (e != cudaSuccess) {
+        record_cuda_error(name, e);
+        return KP_ERR_CUDA;
+    }
+    return check_launch(name);
+}
+
 // Byte sizes of the step workspaces.
 size_t score_plan_bytes(int32_t num_queries);
 int attend_splits(const kp_config &cfg, int32_t num_queries, int sm_count);
 size_t attend_ws_bytes(const kp_config &cfg, int32_t num_queries, int splits);
 
-// Launchers (arguments already validated).
-kp_status launch_compress(const kp_compress_args &a, cudaStream_t s);
-kp_status launch_score(const kp_score_args &a, cudaStream_t s);
+// Inputs of the scorer's work plan, for building it inside another launch.
+struct ScorePlanArgs {
+    int nq;
+    int num_seqs;
+    const int32_t *q_seq;
+    const int32_t *q_pos;
+    int max_tiles;
+    int32_t *plan;     // nullptr: no plan to build
+    int32_t *status;
+};
+ScorePlanArgs score_plan_args(const kp_score_args &a);
+
+// Launchers (arguments already validated).  launch_compress with a plan also
+// builds the scorer's plan (one extra CTA); launch_score with plan_ready then
+// skips its own plan kernel.
+kp_status launch_compress(const kp_compress_args &a, cudaStream_t s, const ScorePlanArgs *plan = nullptr);
+kp_status launch_score(const kp_score_args &a, cudaStream_t s, bool plan_ready = false);
 kp_status launch_topk(const kp_topk_args &a, cudaStream_t s);
 kp_status launch_attend(const kp_attend_args &a, cudaStream_t s);
 

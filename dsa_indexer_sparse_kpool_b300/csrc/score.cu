@@ -28,13 +28,12 @@
 
 #include "kp_common.cuh"
 #include "kp_internal.h"
+#include "score_plan.cuh"
 
 namespace kp {
 
 namespace {
 
-constexpr int kScM = 128;                                 // pools per tile (MMA M)
-constexpr int kScMaxQ = 8;                                // queries per group
 constexpr int kScMaxN = kScMaxQ * kIndexHeads;            // 256 (MMA N max)
 constexpr int kScStages = 4;
 constexpr int kScABlockBytes = kScM * 128;                // [128 rows][64 bf16] = 16 KB
@@ -48,80 +47,15 @@ constexpr int kScAccCols = 256;
 constexpr int kScNumBars = 2 * kScStages + 4 + 2;
 constexpr int kScSmemBytes = kScStages * kScAStageBytes + kScBBytes + kScNumBars * 8 + 1024;
 
-// Plan layout (int32 words) inside the score workspace.
-struct PlanView {
-    int32_t *hdr;      // [0] groups, [1] units
-    int32_t *q0;       // [NQ] first query of each group
-    int32_t *nq;       // [NQ] queries in each group
-    int32_t *seq;      // [NQ] sequence of each group
-    int32_t *unit0;    // [NQ + 1] first unit of each group (exclusive scan of tiles)
-    __host__ __device__ PlanView(int32_t *base, int n)
-        : hdr(base), q0(base + 4), nq(base + 4 + n), seq(base + 4 + 2 * n), unit0(base + 4 + 3 * n) {}
-};
-
-// Groups runs of up to 8 adjacent queries of the same sequence and counts the
-// 128-pool tiles each group needs (the largest n_full among its queries).
+// The plan as its own one-CTA kernel (the standalone scoring call).
 __global__ void __launch_bounds__(1024) score_plan_kernel(int nq, int num_seqs,
                                                           const int32_t *__restrict__ q_seq,
                                                           const int32_t *__restrict__ q_pos,
                                                           int max_tiles, int32_t *plan_base,
                                                           int32_t *status) {
     __shared__ int scratch[33];
-    PlanView plan(plan_base, nq);
-    int carry_run = -1, carry_groups = 0;
-    for (int base = 0; base < nq; base += blockDim.x) {
-        const int i = base + threadIdx.x;
-        const bool in = i < nq;
-        const int sq = in ? q_seq[i] : 0;
-        const bool run_start = in && (i == 0 || q_seq[i - 1] != sq);
-        int tot;
-        int rs = block_inclusive_scan<1>(run_start ? i : -1, scratch, &tot);
-        rs = max(rs, carry_run);
-        carry_run = max(carry_run, tot);
-        const bool gs = in && ((i - rs) % kScMaxQ == 0);
-        const int incl = block_inclusive_scan<0>(gs ? 1 : 0, scratch, &tot);
-        if (gs) {
-            const int gid = carry_groups + incl - 1;
-            plan.q0[gid] = i;
-            plan.seq[gid] = sq;
-        }
-        carry_groups += tot;
-    }
-    __syncthreads();
-    const int ng = carry_groups;
-    for (int g = threadIdx.x; g < ng; g += blockDim.x) {
-        const int q0 = plan.q0[g];
-        const int q1 = (g + 1 < ng) ? plan.q0[g + 1] : nq;
-        int mx = 0;
-        for (int q = q0; q < q1; ++q) mx = max(mx, (q_pos[q] + 1) / kKpool);
-        int tiles = (mx + kScM - 1) / kScM;
-        const int sq = plan.seq[g];
-        if (sq < 0 || sq >= num_seqs) {
-            set_status(status, KP_ERR_DEVICE_BOUNDS);
-            tiles = 0;
-        }
-        if (tiles > max_tiles) {
-            set_status(status, KP_ERR_DEVICE_BOUNDS);
-            tiles = max_tiles;
-        }
-        plan.nq[g] = q1 - q0;
-        plan.unit0[g] = tiles;
-    }
-    __syncthreads();
-    int carry_units = 0;
-    for (int base = 0; base < ng; base += blockDim.x) {
-        const int g = base + threadIdx.x;
-        const int v = g < ng ? plan.unit0[g] : 0;
-        int tot;
-        const int incl = block_inclusive_scan<0>(v, scratch, &tot);
-        if (g < ng) plan.unit0[g] = carry_units + incl - v;
-        carry_units += tot;
-    }
-    if (threadIdx.x == 0) {
-        plan.unit0[ng] = carry_units;
-        plan.hdr[0] = ng;
-        plan.hdr[1] = carry_units;
-    }
+    pdl_wait_then_release();
+    build_score_plan(nq, num_seqs, q_seq, q_pos, max_tiles, plan_base, status, scratch);
 }
 
 struct ScoreParams {
@@ -133,6 +67,45 @@ struct ScoreParams {
     float *scores;
     int64_t stride;
     int32_t *status;
+};
+
+// Barrier over the 4 epilogue warps (named barrier 1) that also ANDs a flag,
+// so a failed wait in any of them makes all of them leave together.
+__device__ __forceinline__ bool epi_bar_all(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.and.pred p, 1, 128, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(v))
+        : "memory");
+    return r != 0;
+}
+
+// Walks the plan's groups alongside a CTA's units: one global read per group
+// change instead of several dependent reads per unit.
+struct GroupCursor {
+    const int32_t *unit0;
+    int g, u0, u1;
+    __device__ void init(const int32_t *unit0_, int g0) {
+        unit0 = unit0_;
+        g = g0;
+        u0 = unit0[g];
+        u1 = unit0[g + 1];
+    }
+    // Advances to the group containing unit u; true when the group changed.
+    __device__ bool seek(int u) {
+        bool moved = false;
+        while (u >= u1) {
+            ++g;
+            u0 = u1;
+            u1 = unit0[g + 1];
+            moved = true;
+        }
+        return moved;
+    }
 };
 
 // Largest group whose first unit is <= u (skips empty groups correctly).
@@ -152,7 +125,10 @@ __global__ void __launch_bounds__(kScThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint32_t tmem_base_s;
     __shared__ int abort_s;
+    __shared__ __align__(16) float w_s[kScMaxQ * kIndexHeads];  // head weights of the current group
+    __shared__ int nf_s[kScMaxQ];                                 // complete pools each query sees
 
+    pdl_wait_then_release();
     PlanView plan(const_cast<int32_t *>(P.plan), P.nq);
     const int ng = plan.hdr[0];
     const long long n_units = plan.hdr[1];
@@ -201,27 +177,29 @@ __global__ void __launch_bounds__(kScThreads, 1)
 
     if (warp == 0) {
         if (lane == 0) {
-            int g = find_group(plan.unit0, ng, u_begin), cur_g = -1, b_loads = 0, stage = 0;
+            GroupCursor gc;
+            gc.init(plan.unit0, find_group(plan.unit0, ng, u_begin));
+            int b_loads = 0, stage = 0;
+            int64_t row_base = 0;
             uint32_t phase = 0;
             for (int u = u_begin; u < u_end; ++u) {
-                while (plan.unit0[g + 1] <= u) ++g;
-                if (g != cur_g) {
+                if (gc.seek(u) || b_loads == 0) {
+                    const int g = gc.g;
                     if (b_loads > 0 &&
                         !mbar_wait(bempty_bar, (b_loads - 1) & 1, abort_flag, P.status))
                         break;
                     const int q0 = plan.q0[g], nq = plan.nq[g];
+                    row_base = P.pool_row_off[plan.seq[g]];
                     mbar_expect_tx(bfull_bar, nq * 2 * kScQBoxBytes);
                     for (int qi = 0; qi < nq; ++qi)
                         for (int kb = 0; kb < 2; ++kb)
                             tma_load_2d(sB + kb * kScBBlockBytes + qi * kScQBoxBytes, &tm_q,
                                         bfull_bar, kb * 64, (q0 + qi) * kIndexHeads);
                     ++b_loads;
-                    cur_g = g;
                 }
                 if (!mbar_wait(empty_bar(stage), phase ^ 1, abort_flag, P.status)) break;
                 mbar_expect_tx(full_bar(stage), kScAStageBytes);
-                const int row = static_cast<int>(P.pool_row_off[plan.seq[g]] +
-                                                 static_cast<int64_t>(u - plan.unit0[g]) * kScM);
+                const int row = static_cast<int>(row_base + static_cast<int64_t>(u - gc.u0) * kScM);
                 const uint32_t dst = sA + stage * kScAStageBytes;
                 tma_load_2d(dst, &tm_pool, full_bar(stage), 0, row);
                 tma_load_2d(dst + kScABlockBytes, &tm_pool, full_bar(stage), 64, row);
@@ -233,16 +211,16 @@ __global__ void __launch_bounds__(kScThreads, 1)
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            int g = find_group(plan.unit0, ng, u_begin), cur_g = -1, b_loads = 0, stage = 0, acc = 0;
+            GroupCursor gc;
+            gc.init(plan.unit0, find_group(plan.unit0, ng, u_begin));
+            int b_loads = 0, stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0, idesc = 0;
             for (int u = u_begin; u < u_end; ++u) {
-                while (plan.unit0[g + 1] <= u) ++g;
-                if (g != cur_g) {
+                if (gc.seek(u) || b_loads == 0) {
                     if (b_loads > 0) tc_commit(bempty_bar);
                     if (!mbar_wait(bfull_bar, b_loads & 1, abort_flag, P.status)) break;
                     ++b_loads;
-                    cur_g = g;
-                    idesc = idesc_bf16_f32(kScM, kIndexHeads * plan.nq[g]);
+                    idesc = idesc_bf16_f32(kScM, kIndexHeads * plan.nq[gc.g]);
                 }
                 if (!mbar_wait(acce_bar(acc), acc_phase ^ 1, abort_flag, P.status)) break;
                 if (!mbar_wait(full_bar(stage), phase, abort_flag, P.status)) break;
@@ -269,30 +247,47 @@ __global__ void __launch_bounds__(kScThreads, 1)
             }
         }
     } else {
-        // Epilogue: warp w may only touch TMEM lanes 32*(w%4) .. +31.
-        const int quad = warp & 3;
-        int g = find_group(plan.unit0, ng, u_begin), acc = 0;
+        // Epilogue: warp w may only touch TMEM lanes 32*(w%4) .. +31.  The head
+        // weights and causal limits of the current query group are staged in
+        // shared memory when the group changes.
+        const int quad = warp & 3, et = threadIdx.x - 64;
+        GroupCursor gc;
+        gc.init(plan.unit0, find_group(plan.unit0, ng, u_begin));
+        int acc = 0, q0 = 0, nq = 0;
+        bool first = true;
         uint32_t acc_phase = 0;
         for (int u = u_begin; u < u_end; ++u) {
-            while (plan.unit0[g + 1] <= u) ++g;
-            if (!mbar_wait(accf_bar(acc), acc_phase, abort_flag, P.status)) break;
+            const bool moved = gc.seek(u) || first;
+            // every epilogue thread leaves together if any wait failed
+            if (!epi_bar_all(mbar_wait(accf_bar(acc), acc_phase, abort_flag, P.status))) break;
             tc_fence_after();
-            const int p = (u - plan.unit0[g]) * kScM + quad * 32 + lane;
-            const int q0 = plan.q0[g], nq = plan.nq[g];
+            if (moved) {
+                q0 = plan.q0[gc.g];
+                nq = plan.nq[gc.g];
+                for (int k = et; k < nq * kIndexHeads; k += 128) w_s[k] = P.w[static_cast<int64_t>(q0) * kIndexHeads + k];
+                if (et < nq) nf_s[et] = (P.q_pos[q0 + et] + 1) / kKpool;
+                epi_bar_all(true);
+                first = false;
+            }
+            const int p = (u - gc.u0) * kScM + quad * 32 + lane;
             for (int qi = 0; qi < nq; ++qi) {
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(tmem + acc * kScAccCols + qi * kIndexHeads +
                                        (static_cast<uint32_t>(quad * 32) << 16),
                                    r);
                 tmem_ld_wait();
-                const int q = q0 + qi;
-                const float *wq = P.w + static_cast<int64_t>(q) * kIndexHeads;
-                float s = 0.f;
+                const float4 *wq = reinterpret_cast<const float4 *>(w_s + qi * kIndexHeads);
+                float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-                for (int h = 0; h < kIndexHeads; ++h)
-                    s = fmaf(__ldg(wq + h), fmaxf(__uint_as_float(r[h]), 0.f), s);
-                const int nf = (P.q_pos[q] + 1) / kKpool;
-                if (p < P.stride) P.scores[static_cast<int64_t>(q) * P.stride + p] = p < nf ? s : -INFINITY;
+                for (int h4 = 0; h4 < kIndexHeads / 4; ++h4) {
+                    const float4 wv = wq[h4];
+                    s0 = fmaf(wv.x, fmaxf(__uint_as_float(r[4 * h4]), 0.f), s0);
+                    s1 = fmaf(wv.y, fmaxf(__uint_as_float(r[4 * h4 + 1]), 0.f), s1);
+                    s0 = fmaf(wv.z, fmaxf(__uint_as_float(r[4 * h4 + 2]), 0.f), s0);
+                    s1 = fmaf(wv.w, fmaxf(__uint_as_float(r[4 * h4 + 3]), 0.f), s1);
+                }
+                const int q = q0 + qi;
+                if (p < P.stride) P.scores[static_cast<int64_t>(q) * P.stride + p] = p < nf_s[qi] ? s0 + s1 : -INFINITY;
             }
             tc_fence_before();
             mbar_arrive(acce_bar(acc));
@@ -317,17 +312,31 @@ size_t score_plan_bytes(int32_t num_queries) {
     return align_up(sizeof(int32_t) * (4 + 4 * static_cast<size_t>(num_queries) + 1), 256);
 }
 
-kp_status launch_score(const kp_score_args &a, cudaStream_t s) {
+ScorePlanArgs score_plan_args(const kp_score_args &a) {
+    ScorePlanArgs p;
+    p.nq = a.q.num_queries;
+    p.num_seqs = a.seqs.num_seqs;
+    p.q_seq = a.q.q_seq;
+    p.q_pos = a.q.q_pos;
+    p.max_tiles = (a.q.max_pools + kScM - 1) / kScM;
+    p.plan = static_cast<int32_t *>(a.workspace);
+    p.status = a.d_status;
+    return p;
+}
+
+kp_status launch_score(const kp_score_args &a, cudaStream_t s, bool plan_ready) {
     const int nq = a.q.num_queries;
     if (nq == 0) return KP_OK;
     const int sms = device_sm_count();
     if (sms <= 0) return KP_ERR_CUDA;
     int32_t *plan = static_cast<int32_t *>(a.workspace);
     const int max_tiles = (a.q.max_pools + kScM - 1) / kScM;
-    score_plan_kernel<<<1, 1024, 0, s>>>(nq, a.seqs.num_seqs, a.q.q_seq, a.q.q_pos, max_tiles, plan,
-                                         a.d_status);
-    kp_status st = check_launch("score_plan_kernel");
-    if (st != KP_OK) return st;
+    if (!plan_ready) {
+        const kp_status st = launch_kernel("score_plan_kernel", score_plan_kernel,
+                                           LaunchCfg(dim3(1), dim3(1024), 0, s), nq, a.seqs.num_seqs, a.q.q_seq,
+                                           a.q.q_pos, max_tiles, plan, a.d_status);
+        if (st != KP_OK) return st;
+    }
     if (max_tiles == 0) return KP_OK;
 
     CUtensorMap tm_pool, tm_q;
@@ -351,8 +360,8 @@ kp_status launch_score(const kp_score_args &a, cudaStream_t s) {
     P.scores = a.scores;
     P.stride = a.score_stride;
     P.status = a.d_status;
-    indexer_score_kernel<<<sms, kScThreads, kScSmemBytes, s>>>(tm_pool, tm_q, P);
-    return check_launch("indexer_score_kernel");
+    return launch_kernel("indexer_score_kernel", indexer_score_kernel,
+                         LaunchCfg(dim3(sms), dim3(kScThreads), kScSmemBytes, s), tm_pool, tm_q, P);
 }
 
 }  // namespace kp

@@ -114,8 +114,14 @@ __global__ void __launch_bounds__(kTkThreads, 1)
     __shared__ TopkShared sh;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    pdl_wait_then_release();
     const uint32_t rank = cluster_ctarank(), C = cluster_size();
     const int q = blockIdx.x / C;
+    // A one-CTA row needs only block barriers.
+    auto cbar = [&]() {
+        if (C > 1) cluster_barrier();
+        else __syncthreads();
+    };
     const int t = q_pos[q];
     const int n = t >= 0 ? (t + 1) / kKpool : 0;
     int32_t *out = pool_idx + static_cast<int64_t>(q) * K;
@@ -172,7 +178,7 @@ __global__ void __launch_bounds__(kTkThreads, 1)
         atomicMin(&sh.kmin, kmin);
         atomicMax(&sh.kmax, kmax);
     }
-    cluster_barrier();
+    cbar();
     uint32_t gmin = 0xffffffffu, gmax = 0u;
     for (uint32_t r = 0; r < C; ++r) {
         gmin = min(gmin, ld_cluster_u32(dsmem_addr(smem_u32(&sh.kmin), r)));
@@ -198,7 +204,7 @@ __global__ void __launch_bounds__(kTkThreads, 1)
             }
         }
     }
-    cluster_barrier();
+    cbar();
 
     // ---- threshold bin: the K-th largest key lies in bin B
     if (rank != 0) {  // local copy of the cluster totals
@@ -261,40 +267,58 @@ __global__ void __launch_bounds__(kTkThreads, 1)
                 }
             }
         }
-        cluster_barrier();
+        cbar();
         if (rank == 0) {
             const int m = static_cast<int>(min(sh.n_cand, static_cast<uint32_t>(kTkCandMax)));
-            int m2 = 1;
-            while (m2 < m) m2 <<= 1;
-            for (int i = m + tid; i < m2; i += kTkThreads) sh.cand[i] = 0ull;  // sorts last
-            __syncthreads();
-            // bitonic sort, descending
-            for (int kk = 2; kk <= m2; kk <<= 1) {
-                for (int j = kk >> 1; j > 0; j >>= 1) {
-                    for (int i = tid; i < (m2 >> 1); i += kTkThreads) {
-                        const int lo = 2 * i - (i & (j - 1));
-                        const int hi = lo + j;
-                        const bool desc = (lo & kk) == 0;
-                        const uint64_t a = sh.cand[lo], b = sh.cand[hi];
-                        if ((a < b) == desc) {
-                            sh.cand[lo] = b;
-                            sh.cand[hi] = a;
+            const bool need_ok = need >= 1 && need <= m;
+            if (!need_ok && tid == 0) set_status(status, KP_ERR_DEVICE_BOUNDS);
+            const int nd = need_ok ? need : (m > 0 ? m : 1);
+            if (m <= kTkThreads) {
+                // Rank every candidate against all others (values are distinct: the
+                // low half holds the inverted index); the one of rank nd-1 is T.
+                uint64_t v = 0;
+                int rk = m;
+                if (tid < m) {
+                    v = sh.cand[tid];
+                    rk = 0;
+                    for (int j = 0; j < m; ++j) rk += sh.cand[j] > v;
+                    if (rk == nd - 1) sh.thr_key = static_cast<uint32_t>(v >> 32);
+                }
+                __syncthreads();
+                const uint32_t tk = sh.thr_key;
+                const int e = __syncthreads_count(tid < m && rk < nd && static_cast<uint32_t>(v >> 32) == tk);
+                if (tid == 0) sh.eq_take = static_cast<uint32_t>(e);
+            } else {
+                int m2 = 1;
+                while (m2 < m) m2 <<= 1;
+                for (int i = m + tid; i < m2; i += kTkThreads) sh.cand[i] = 0ull;  // sorts last
+                __syncthreads();
+                // bitonic sort, descending
+                for (int kk = 2; kk <= m2; kk <<= 1) {
+                    for (int j = kk >> 1; j > 0; j >>= 1) {
+                        for (int i = tid; i < (m2 >> 1); i += kTkThreads) {
+                            const int lo = 2 * i - (i & (j - 1));
+                            const int hi = lo + j;
+                            const bool desc = (lo & kk) == 0;
+                            const uint64_t a = sh.cand[lo], b = sh.cand[hi];
+                            if ((a < b) == desc) {
+                                sh.cand[lo] = b;
+                                sh.cand[hi] = a;
+                            }
                         }
+                        __syncthreads();
                     }
-                    __syncthreads();
+                }
+                if (tid == 0) {
+                    const uint32_t tk = static_cast<uint32_t>(sh.cand[nd - 1] >> 32);
+                    uint32_t e = 0;
+                    for (int j = nd - 1; j >= 0 && static_cast<uint32_t>(sh.cand[j] >> 32) == tk; --j) ++e;
+                    sh.thr_key = tk;
+                    sh.eq_take = e;
                 }
             }
-            if (tid == 0) {
-                const int nd = need >= 1 && need <= m ? need : (m > 0 ? m : 1);
-                if (!(need >= 1 && need <= m)) set_status(status, KP_ERR_DEVICE_BOUNDS);
-                const uint32_t tk = static_cast<uint32_t>(sh.cand[nd - 1] >> 32);
-                uint32_t e = 0;
-                for (int j = nd - 1; j >= 0 && static_cast<uint32_t>(sh.cand[j] >> 32) == tk; --j) ++e;
-                sh.thr_key = tk;
-                sh.eq_take = e;
-            }
         }
-        cluster_barrier();
+        cbar();
         T = ld_cluster_u32(dsmem_addr(smem_u32(&sh.thr_key), 0));
         eq_take = ld_cluster_u32(dsmem_addr(smem_u32(&sh.eq_take), 0));
     } else {
@@ -303,16 +327,16 @@ __global__ void __launch_bounds__(kTkThreads, 1)
         int krem = need;
         for (int pass = 0; pass < 4; ++pass) {
             const int shift = 24 - 8 * pass;
-            cluster_barrier();  // every CTA is done reading the leader's previous totals
+            cbar();  // every CTA is done reading the leader's previous totals
             for (int i = tid; i < 256; i += kTkThreads) sh.hist[i] = 0u;
-            cluster_barrier();  // ... and every histogram is cleared
+            cbar();  // ... and every histogram is cleared
             for (int i = tid; i < len; i += kTkThreads) {
                 const uint32_t k = keys[i];
                 if (bin_of(k) == B && (k & mask) == prefix) atomicAdd(&sh.hist[(k >> shift) & 255u], 1u);
             }
             __syncthreads();
             if (rank != 0 && tid < 256 && sh.hist[tid]) red_add_cluster(dsmem_addr(smem_u32(&sh.hist[tid]), 0), sh.hist[tid]);
-            cluster_barrier();
+            cbar();
             if (warp == 0) {
                 uint32_t c[8], sum = 0;
 #pragma unroll
@@ -376,7 +400,7 @@ __global__ void __launch_bounds__(kTkThreads, 1)
             atomicAdd(&sh.cnt_eq, e);
         }
     }
-    cluster_barrier();
+    cbar();
     uint32_t out_base = 0, eq_before = 0;
     for (uint32_t r = 0; r < rank; ++r) {
         const uint32_t gt_r = ld_cluster_u32(dsmem_addr(smem_u32(&sh.cnt_gt), r));
@@ -406,7 +430,7 @@ __global__ void __launch_bounds__(kTkThreads, 1)
         }
     }
     if (rank == 0 && tid == 0) n_sel[q] = K;
-    cluster_barrier();  // keep this CTA's shared memory alive until every peer is done reading it
+    cbar();  // keep this CTA's shared memory alive until every peer is done reading it
 }
 
 }  // namespace
@@ -434,25 +458,9 @@ kp_status launch_topk(const kp_topk_args &a, cudaStream_t s) {
         record_cuda_error("cudaFuncSetAttribute(topk_select_kernel)", e);
         return KP_ERR_CUDA;
     }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(nq) * C);
-    cfg.blockDim = dim3(kTkThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = C;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, topk_select_kernel, a.scores, a.score_stride, a.q.q_pos, K,
-                           a.pool_idx, a.n_sel, chunk_cap, a.d_status);
-    if (e != cudaSuccess) {
-        record_cuda_error("cudaLaunchKernelEx(topk_select_kernel)", e);
-        return KP_ERR_CUDA;
-    }
-    return check_launch("topk_select_kernel");
+    return launch_kernel("topk_select_kernel", topk_select_kernel,
+                         LaunchCfg(dim3(static_cast<unsigned>(nq) * C), dim3(kTkThreads), smem, s, C), a.scores,
+                         a.score_stride, a.q.q_pos, K, a.pool_idx, a.n_sel, chunk_cap, a.d_status);
 }
 
 }  // namespace kp

@@ -128,3 +128,34 @@ def test_exact_ties_in_scores():
     sess, step, rep = PL.full_check(wl)
     sel0 = step.pool_idx[0].cpu().numpy()
     assert np.array_equal(sel0, np.arange(64)), "equal scores must select the lowest pool indices"
+
+
+def test_forward_without_new_tokens():
+    # every token is already cached: the step only queries, so there is no
+    # compression launch and the scorer builds its own plan
+    from dsa_indexer_sparse_kpool_b300.session import Step, build_session
+    wl = KI.make(small_spec([1000, 1537], [2, 3], 256, seed=23))
+    cfg = PL.cfg_of(wl)
+    lens = wl.lens.tolist()
+    sess = build_session(cfg, lens, lens, wl.tok_off.tolist(), wl.pool_off.tolist(), wl.pool_rows, wl.latent,
+                         wl.keys, wl.gates, wl.ape)
+    empty = torch.zeros(0, 128, dtype=torch.bfloat16)
+    step = Step(sess, lens, [0] * wl.B, empty, empty, wl.q_seq.tolist(), wl.q_pos.tolist(), wl.q_idx, wl.w,
+                wl.q_lat)
+    step.run()
+    torch.cuda.synchronize()
+    assert int(sess.status.item()) == 0
+    PL.check_pooled(sess, wl)
+    g_idx, g_nsel = step.pool_idx.cpu().numpy(), step.n_sel.cpu().numpy()
+    for qi in range(wl.NQ):
+        b = int(wl.q_seq[qi])
+        o_sc = PL.oracle_scores_on(PL.gpu_pooled_of_seq(sess, wl, b), wl, qi)
+        ref = oracle.topk_select(o_sc, cfg.k_pools)
+        ns = int(g_nsel[qi])
+        assert ns == ref.size
+        diff = np.setxor1d(g_idx[qi][:ns], ref)
+        if diff.size:
+            sK = np.sort(o_sc)[::-1][cfg.k_pools - 1]
+            assert (np.abs(o_sc[diff] - sK) <= PL.NEAR_TIE * abs(sK)).all()
+        o_out, o_lse = PL.oracle_attend_on_selection(wl, qi, g_idx[qi][:ns])
+        PL.check_attend(step.out[qi].float().cpu().numpy(), step.lse[qi].cpu().numpy(), o_out, o_lse)
