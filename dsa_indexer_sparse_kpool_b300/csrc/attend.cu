@@ -269,7 +269,8 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     if (warp == kAtMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         // Event-driven: S of the next tile, chunk by chunk as it lands, and P.V of
-        // the oldest softmaxed tile, whichever is ready first.
+        // the oldest softmaxed tile, whichever is ready first (non-blocking tests:
+        // a blocking wait on one would stall the other).
         if (lane == 0) {
             bool ok = nt == 0 || mbar_wait(bar(kBarQ), 0, abort_flag, P.status);
             const uint32_t idesc_s = idesc_bf16_f32(kAtTok, kMlaHeads);             // M = 64
@@ -288,7 +289,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
                 bool progressed = false;
                 if (next_s < nt && next_s < next_pv + 2) {
                     const int slot = next_s & 1;
-                    if (mbar_try_wait(bar(kBarFull + slot * kAtChunks + s_chunk), (next_s >> 1) & 1)) {
+                    if (mbar_test(bar(kBarFull + slot * kAtChunks + s_chunk), (next_s >> 1) & 1)) {
                         tc_fence_after();
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk) {
@@ -305,7 +306,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
                         progressed = true;
                     }
                 }
-                if (next_pv < next_s && mbar_try_wait(bar(kBarP), next_pv & 1)) {
+                if (next_pv < next_s && mbar_test(bar(kBarP), next_pv & 1)) {
                     const int slot = next_pv & 1;
                     tc_fence_after();
                     for (int c = 0; c < kAtChunks; ++c) {
@@ -464,7 +465,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
                     const float mo = mused_s[tid];
                     if (mt > mo + kAtRescaleLog2) {
                         mused_s[tid] = mt;
-                        fac_s[tid] = exp2f(mo - mt);  // 0 when mo = -inf
+                        fac_s[tid] = fast_exp2(mo - mt);  // 0 when mo = -inf
                     } else {
                         fac_s[tid] = 1.f;
                     }
@@ -484,8 +485,8 @@ __global__ void __launch_bounds__(kAtThreads, 1)
                     for (int e = 0; e < 4; ++e) {
                         const int h = 8 * k + 2 * e;
                         const float2 m2 = *reinterpret_cast<const float2 *>(mused_s + hb + h);
-                        const float p0 = exp2f(x[h] - m2.x);
-                        const float p1 = exp2f(x[h + 1] - m2.y);
+                        const float p0 = fast_exp2(x[h] - m2.x);
+                        const float p1 = fast_exp2(x[h + 1] - m2.y);
                         lp[h] += p0;
                         lp[h + 1] += p1;
                         pk[e] = pack_bf16x2(p0, p1);
@@ -639,19 +640,19 @@ __global__ void __launch_bounds__(kAtThreads, 1)
             float *w = wm_s + tid * 16;
             for (int s2 = 0; s2 < kAtMaxSplits; ++s2) {
                 const float ms = s2 < S ? recvm_s[s2 * 64 + tid] : -INFINITY;
-                const float ws = ms > -INFINITY ? exp2f(ms - M) : 0.f;
+                const float ws = ms > -INFINITY ? fast_exp2(ms - M) : 0.f;
                 w[s2] = ws;
                 if (ws > 0.f) L += ws * recvl_s[s2 * 64 + tid];
             }
             for (int j = 0; j < kAtMaxTail; ++j) {
-                const float wt = j < n_tail ? exp2f(ztail_s[h * 4 + j] - M) : 0.f;
+                const float wt = j < n_tail ? fast_exp2(ztail_s[h * 4 + j] - M) : 0.f;
                 w[8 + j] = wt;
                 L += wt;
             }
             w[12] = L > 0.f ? 1.f / L : 0.f;
             if (P.lse)
                 P.lse[static_cast<int64_t>(q) * kMlaHeads + h] =
-                    L > 0.f ? (M + log2f(L)) * 0.69314718055994530942f : -INFINITY;
+                    L > 0.f ? (M + fast_log2(L)) * 0.69314718055994530942f : -INFINITY;
         }
         __syncthreads();
         // out[q][h][d] = (sum_s w_s O_s[h][d] + sum_j w_j c_j[d]) / L, 4 columns per item

@@ -76,6 +76,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// Non-blocking test of the same condition (try_wait may suspend the thread for
+// a while when the phase is not complete; polling several barriers needs this).
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 // Waits for the phase of parity `parity` to complete.  Returns false (and
 // records a timeout in *status) after KP_WAIT_NS, or early when *abort is
 // set by another thread of the CTA.
@@ -182,6 +195,18 @@ __device__ __forceinline__ void tmem_st_wait() {
 // proxy (TMA, tcgen05.mma operand reads) once the thread synchronises.
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// 2^x and log2(x) as single approximate hardware instructions (relative error
+// about 2^-22; denormal results flush to zero, 2^-inf = 0).
+__device__ __forceinline__ float fast_exp2(float x) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+__device__ __forceinline__ float fast_log2(float x) {
+    float r;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
 }
 // Warp-wide max of a float (every lane gets the result).
 __device__ __forceinline__ float warp_max_f32(float v) {

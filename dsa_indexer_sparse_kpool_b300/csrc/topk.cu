@@ -1,5 +1,5 @@
-// topk.cu -- top-k pool selection: one histogram pass, exact resolution of
-// the threshold bin, order-preserving compaction.
+// topk.cu -- top-k pool selection: exact radix select on order-preserving
+// keys, then an order-preserving compaction.
 //
 // Method: each query keeps index_topk / kpool pools (2048 tokens / 4 = 512;
 // llm-atlas GLM-5.3-Flash card, raw config index_topk / index_kpool); when it
@@ -8,20 +8,22 @@
 //
 // B300 design.  A query's row of n = n_full(t) scores is split over a
 // thread-block cluster of C CTAs (C = 1 up to 16K pools; up to 8 for the
-// 262,143-pool rows of a 1M-token context), each holding its slice as
-// order-preserving uint32 keys.
-//  1. The cluster's smallest and largest keys fix up to 2048 bins of equal
-//     width (a power of two) in key space (monotone, so the K-th largest key
-//     lies in exactly one bin, B).  One histogram pass, summed into the leader CTA through
-//     distributed shared memory, gives B and how many of its keys are needed.
-//  2. The keys of bin B (typically a few dozen) are gathered into the
-//     leader, sorted (key descending, index ascending) and give the exact
-//     threshold key T and how many keys equal to T are taken.  If bin B holds
-//     more than 4096 keys (heavy ties), 8-bit radix passes restricted to bin B
-//     find T instead.
-//  3. Every CTA counts its keys above / equal to T; one packed block scan
-//     turns the counts into output positions, so the selected pools are
-//     written in ascending order with no sort.
+// 262,143-pool rows of a 1M-token context), each holding its slice in shared
+// memory as order-preserving uint32 keys.
+//  1. The cluster's smallest key and key span fix a shift s with at most 2048
+//     bins of width 2^s.  Each level histograms the keys inside the current
+//     range into its bins, finds the bin holding the K-th largest key and
+//     narrows the range to that bin, split next into bins of width
+//     2^max(0, s - 11).  After at most three
+//     levels the range is one key value: the threshold T, with the number of
+//     keys equal to T that are taken (the lowest indices first).  A level
+//     costs one pass over the keys and one cluster barrier: every CTA reads
+//     every peer's histogram through distributed shared memory (two buffers,
+//     so a level never waits for the previous one to be read).
+//  2. Counts of keys above / equal to T, per warp and per CTA, give every
+//     selected key its output position; each warp walks its own contiguous
+//     range of keys with lanes interleaved (no shared-memory bank conflicts),
+//     so the selection is written in ascending pool order with no sort.
 // Cluster barriers are hardware barriers (all CTAs of a cluster are
 // co-resident): no spin loop anywhere.
 #include "kp_common.cuh"
@@ -32,32 +34,30 @@ namespace kp {
 namespace {
 
 constexpr int kTkThreads = 512;
-constexpr int kTkChunkMax = 32768;  // keys per CTA (128 KB of shared memory)
+constexpr int kTkWarps = kTkThreads / 32;
+constexpr int kTkChunkMax = 32768;    // keys per CTA (128 KB of shared memory)
 constexpr int kTkMaxCluster = 8;
 constexpr int kTkBins = 2048;
-constexpr int kTkCandMax = 4096;
-constexpr int kTkKeysPerCta = 16384;  // preferred largest slice per CTA
+constexpr int kTkDigit = 11;           // log2(kTkBins)
+constexpr int kTkKeysPerCta = 16384;   // preferred largest slice per CTA
 
 __device__ __forceinline__ uint32_t cluster_size() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
     return r;
 }
-__device__ __forceinline__ void red_add_cluster(uint32_t addr, uint32_t v) {
-    asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-__device__ __forceinline__ uint32_t atom_add_cluster(uint32_t addr, uint32_t v) {
-    uint32_t old;
-    asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(addr), "r"(v) : "memory");
-    return old;
-}
 __device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr) {
     uint32_t v;
     asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
     return v;
 }
-__device__ __forceinline__ void st_cluster_u64(uint32_t addr, uint64_t v) {
-    asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
+__device__ __forceinline__ uint4 ld_cluster_u32x4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
 }
 
 // Order-preserving key: larger float -> larger key; -0 == +0; NaN lowest.
@@ -96,13 +96,11 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *warp_t
 }
 
 struct TopkShared {
-    uint32_t hist[kTkBins];           // leader: cluster totals
-    uint64_t cand[kTkCandMax];        // leader: (key << 32) | ~index of bin-B keys
+    uint32_t hist[2][kTkBins];        // this CTA's histogram of a level (two buffers)
     uint32_t warp_tot[32];
+    uint32_t wgt[kTkWarps], weq[kTkWarps];  // per-warp counts above / equal to T
     uint32_t kmin, kmax;              // this CTA's key range
-    uint32_t n_cand;                  // leader: candidates gathered
-    uint32_t thr_key, eq_take;        // leader: threshold key and how many of its ties to take
-    uint32_t cnt_gt, cnt_eq;          // this CTA's keys above / equal to the threshold
+    uint32_t cnt_gt, cnt_eq;          // this CTA's keys above / equal to T
     int pick_bin, pick_need;
 };
 
@@ -111,7 +109,7 @@ __global__ void __launch_bounds__(kTkThreads, 1)
                        const int32_t *__restrict__ q_pos, int K, int32_t *__restrict__ pool_idx,
                        int32_t *__restrict__ n_sel, int chunk_cap, int32_t *status) {
     extern __shared__ uint32_t keys[];
-    __shared__ TopkShared sh;
+    __shared__ __align__(16) TopkShared sh;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     pdl_wait_then_release();
@@ -170,9 +168,8 @@ __global__ void __launch_bounds__(kTkThreads, 1)
     if (tid == 0) {
         sh.kmin = 0xffffffffu;
         sh.kmax = 0u;
-        sh.n_cand = 0u;
     }
-    for (int i = tid; i < kTkBins; i += kTkThreads) sh.hist[i] = 0u;
+    for (int i = tid; i < kTkBins; i += kTkThreads) sh.hist[0][i] = 0u;
     __syncthreads();
     if (lane == 0) {
         atomicMin(&sh.kmin, kmin);
@@ -184,221 +181,94 @@ __global__ void __launch_bounds__(kTkThreads, 1)
         gmin = min(gmin, ld_cluster_u32(dsmem_addr(smem_u32(&sh.kmin), r)));
         gmax = max(gmax, ld_cluster_u32(dsmem_addr(smem_u32(&sh.kmax), r)));
     }
-    // bin(k) = (k - gmin) >> sh with the smallest sh that maps the key span into
-    // 2048 bins: monotone in k, one shift per key.
+
+    // ---- radix select: the range [base, base + 2^wb) holds the K-th largest key;
+    // a level splits it into bins of width 2^s (at most 2048 of them).
     const uint64_t span = static_cast<uint64_t>(gmax) - gmin + 1;
-    int bsh = 0;
-    while ((span - 1) >> bsh >= static_cast<uint64_t>(kTkBins)) ++bsh;
-    auto bin_of = [&](uint32_t k) -> uint32_t { return (k - gmin) >> bsh; };
-
-    // ---- histogram into the leader
-    {
-        // Private per-CTA histogram first (in this CTA's own hist, zeroed above),
-        // then one remote add per non-empty bin.
-        for (int i = tid; i < len; i += kTkThreads) atomicAdd(&sh.hist[bin_of(keys[i])], 1u);
-        __syncthreads();
-        if (rank != 0) {
-            for (int i = tid; i < kTkBins; i += kTkThreads) {
-                const uint32_t v = sh.hist[i];
-                if (v) red_add_cluster(dsmem_addr(smem_u32(&sh.hist[i]), 0), v);
-            }
+    int s = 0;
+    while (((span - 1) >> s) >= static_cast<uint64_t>(kTkBins)) ++s;
+    int wb = s + kTkDigit;
+    uint32_t base = gmin;
+    int need = K;
+    constexpr int kPer = kTkBins / kTkThreads;  // bins per thread in the scan
+    static_assert(kPer == 4, "the histogram scan reads four bins per thread");
+    for (int level = 0;; ++level) {
+        uint32_t *hist = sh.hist[level & 1];
+        if (level > 0) {  // this buffer was last read by peers two levels ago
+            for (int i = tid; i < kTkBins; i += kTkThreads) hist[i] = 0u;
+            __syncthreads();
         }
-    }
-    cbar();
-
-    // ---- threshold bin: the K-th largest key lies in bin B
-    if (rank != 0) {  // local copy of the cluster totals
-        for (int i = tid; i < kTkBins; i += kTkThreads) sh.hist[i] = ld_cluster_u32(dsmem_addr(smem_u32(&sh.hist[i]), 0));
-    }
-    __syncthreads();
-    {
-        // Thread i holds bins 2047-4i .. 2044-4i (descending); one block scan
-        // gives the count above its group, and the group containing the K-th
-        // largest key names B.
-        constexpr int kPer = kTkBins / kTkThreads;
-        uint32_t c[kPer], sum = 0;
+        const uint64_t range = static_cast<uint64_t>(1) << wb;
+        for (int i = tid; i < len; i += kTkThreads) {
+            const uint32_t k = keys[i];
+            if (k >= base && static_cast<uint64_t>(k - base) < range) atomicAdd(&hist[(k - base) >> s], 1u);
+        }
+        cbar();  // every CTA's histogram of this level is complete
+        // Cluster totals of this thread's four bins, read from every CTA; the
+        // thread holds bins b0+3 .. b0 (descending key order across threads).
+        const int b0 = kTkBins - kPer * (tid + 1);
+        uint32_t c[kPer] = {0u, 0u, 0u, 0u}, sum = 0;
+        for (uint32_t r = 0; r < C; ++r) {
+            const uint4 v = ld_cluster_u32x4(dsmem_addr(smem_u32(hist + b0), r));
+            c[0] += v.w;
+            c[1] += v.z;
+            c[2] += v.y;
+            c[3] += v.x;
+        }
 #pragma unroll
-        for (int j = 0; j < kPer; ++j) {
-            c[j] = sh.hist[kTkBins - 1 - (tid * kPer + j)];
-            sum += c[j];
-        }
+        for (int j = 0; j < kPer; ++j) sum += c[j];
         uint32_t tot;
         uint32_t above = block_excl_scan(sum, sh.warp_tot, &tot);
-        if (tid == 0 && tot < static_cast<uint32_t>(K)) {  // counts lost: cannot happen with consistent data
+        if (tid == 0 && tot < static_cast<uint32_t>(need)) {  // counts lost: cannot happen with consistent data
             set_status(status, KP_ERR_DEVICE_BOUNDS);
             sh.pick_bin = kTkBins - 1;
             sh.pick_need = 1;
         }
-        if (above < static_cast<uint32_t>(K) && static_cast<uint32_t>(K) <= above + sum) {
+        if (above < static_cast<uint32_t>(need) && static_cast<uint32_t>(need) <= above + sum) {
 #pragma unroll
             for (int j = 0; j < kPer; ++j) {
-                if (above < static_cast<uint32_t>(K) && above + c[j] >= static_cast<uint32_t>(K)) {
-                    sh.pick_bin = kTkBins - 1 - (tid * kPer + j);
-                    sh.pick_need = K - static_cast<int>(above);
+                if (above < static_cast<uint32_t>(need) && above + c[j] >= static_cast<uint32_t>(need)) {
+                    sh.pick_bin = b0 + kPer - 1 - j;
+                    sh.pick_need = need - static_cast<int>(above);
                 }
                 above += c[j];
             }
         }
+        __syncthreads();
+        base += static_cast<uint32_t>(sh.pick_bin) << s;
+        need = sh.pick_need;
+        __syncthreads();  // pick_* is rewritten by the next level
+        if (s == 0) break;
+        wb = s;  // the chosen bin is the next range
+        s = wb > kTkDigit ? wb - kTkDigit : 0;
     }
-    __syncthreads();
-    const uint32_t B = static_cast<uint32_t>(sh.pick_bin);
-    const int need = sh.pick_need;
-    const uint32_t cnt_b = sh.hist[B];
+    const uint32_t T = base;                               // the K-th largest key
+    const uint32_t eq_take = static_cast<uint32_t>(need);  // keys equal to T that are taken
 
-    uint32_t T;         // threshold key
-    uint32_t eq_take;   // keys equal to T that are taken (lowest indices first)
-    if (cnt_b <= static_cast<uint32_t>(kTkCandMax)) {
-        // ---- gather bin B into the leader, sort, read off T
-        const uint32_t cnt_addr = dsmem_addr(smem_u32(&sh.n_cand), 0);
-        const uint32_t cand_addr = dsmem_addr(smem_u32(&sh.cand[0]), 0);
-        for (int base = 0; base < len; base += kTkThreads) {
-            const int i = base + tid;
-            const bool m = i < len && bin_of(keys[i]) == B;
-            const uint32_t bal = __ballot_sync(0xffffffffu, m);
-            if (bal) {
-                uint32_t slot0 = 0;
-                if (lane == __ffs(bal) - 1) slot0 = atom_add_cluster(cnt_addr, __popc(bal));
-                slot0 = __shfl_sync(0xffffffffu, slot0, __ffs(bal) - 1);
-                if (m) {
-                    const uint32_t slot = slot0 + __popc(bal & ((1u << lane) - 1u));
-                    const uint64_t v = (static_cast<uint64_t>(keys[i]) << 32) |
-                                       static_cast<uint32_t>(~static_cast<uint32_t>(cs + i));
-                    if (slot < static_cast<uint32_t>(kTkCandMax)) st_cluster_u64(cand_addr + 8u * slot, v);
-                }
-            }
-        }
-        cbar();
-        if (rank == 0) {
-            const int m = static_cast<int>(min(sh.n_cand, static_cast<uint32_t>(kTkCandMax)));
-            const bool need_ok = need >= 1 && need <= m;
-            if (!need_ok && tid == 0) set_status(status, KP_ERR_DEVICE_BOUNDS);
-            const int nd = need_ok ? need : (m > 0 ? m : 1);
-            if (m <= kTkThreads) {
-                // Rank every candidate against all others (values are distinct: the
-                // low half holds the inverted index); the one of rank nd-1 is T.
-                uint64_t v = 0;
-                int rk = m;
-                if (tid < m) {
-                    v = sh.cand[tid];
-                    rk = 0;
-                    for (int j = 0; j < m; ++j) rk += sh.cand[j] > v;
-                    if (rk == nd - 1) sh.thr_key = static_cast<uint32_t>(v >> 32);
-                }
-                __syncthreads();
-                const uint32_t tk = sh.thr_key;
-                const int e = __syncthreads_count(tid < m && rk < nd && static_cast<uint32_t>(v >> 32) == tk);
-                if (tid == 0) sh.eq_take = static_cast<uint32_t>(e);
-            } else {
-                int m2 = 1;
-                while (m2 < m) m2 <<= 1;
-                for (int i = m + tid; i < m2; i += kTkThreads) sh.cand[i] = 0ull;  // sorts last
-                __syncthreads();
-                // bitonic sort, descending
-                for (int kk = 2; kk <= m2; kk <<= 1) {
-                    for (int j = kk >> 1; j > 0; j >>= 1) {
-                        for (int i = tid; i < (m2 >> 1); i += kTkThreads) {
-                            const int lo = 2 * i - (i & (j - 1));
-                            const int hi = lo + j;
-                            const bool desc = (lo & kk) == 0;
-                            const uint64_t a = sh.cand[lo], b = sh.cand[hi];
-                            if ((a < b) == desc) {
-                                sh.cand[lo] = b;
-                                sh.cand[hi] = a;
-                            }
-                        }
-                        __syncthreads();
-                    }
-                }
-                if (tid == 0) {
-                    const uint32_t tk = static_cast<uint32_t>(sh.cand[nd - 1] >> 32);
-                    uint32_t e = 0;
-                    for (int j = nd - 1; j >= 0 && static_cast<uint32_t>(sh.cand[j] >> 32) == tk; --j) ++e;
-                    sh.thr_key = tk;
-                    sh.eq_take = e;
-                }
-            }
-        }
-        cbar();
-        T = ld_cluster_u32(dsmem_addr(smem_u32(&sh.thr_key), 0));
-        eq_take = ld_cluster_u32(dsmem_addr(smem_u32(&sh.eq_take), 0));
-    } else {
-        // ---- heavy ties: 8-bit radix passes over the keys of bin B
-        uint32_t prefix = 0, mask = 0;
-        int krem = need;
-        for (int pass = 0; pass < 4; ++pass) {
-            const int shift = 24 - 8 * pass;
-            cbar();  // every CTA is done reading the leader's previous totals
-            for (int i = tid; i < 256; i += kTkThreads) sh.hist[i] = 0u;
-            cbar();  // ... and every histogram is cleared
-            for (int i = tid; i < len; i += kTkThreads) {
-                const uint32_t k = keys[i];
-                if (bin_of(k) == B && (k & mask) == prefix) atomicAdd(&sh.hist[(k >> shift) & 255u], 1u);
-            }
-            __syncthreads();
-            if (rank != 0 && tid < 256 && sh.hist[tid]) red_add_cluster(dsmem_addr(smem_u32(&sh.hist[tid]), 0), sh.hist[tid]);
-            cbar();
-            if (warp == 0) {
-                uint32_t c[8], sum = 0;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    c[j] = ld_cluster_u32(dsmem_addr(smem_u32(&sh.hist[255 - (lane * 8 + j)]), 0));
-                    sum += c[j];
-                }
-                uint32_t incl = sum;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
-                    if (lane >= o) incl += v;
-                }
-                const uint32_t excl = incl - sum;
-                const bool hit = excl < static_cast<uint32_t>(krem) && static_cast<uint32_t>(krem) <= incl;
-                const uint32_t hb = __ballot_sync(0xffffffffu, hit);
-                if (hb == 0u && lane == 0) {
-                    set_status(status, KP_ERR_DEVICE_BOUNDS);
-                    sh.pick_bin = 0;
-                    sh.pick_need = 1;
-                }
-                if (lane == __ffs(hb) - 1) {
-                    uint32_t above = excl;
-                    for (int j = 0; j < 8; ++j) {
-                        if (above + c[j] >= static_cast<uint32_t>(krem)) {
-                            sh.pick_bin = 255 - (lane * 8 + j);
-                            sh.pick_need = krem - static_cast<int>(above);
-                            break;
-                        }
-                        above += c[j];
-                    }
-                }
-            }
-            __syncthreads();
-            prefix |= static_cast<uint32_t>(sh.pick_bin) << shift;
-            mask |= 255u << shift;
-            krem = sh.pick_need;
-            __syncthreads();
-        }
-        T = prefix;
-        eq_take = static_cast<uint32_t>(krem);
-    }
-
-    // ---- per-CTA counts above / equal to T, output offsets
-    if (tid == 0) {
-        sh.cnt_gt = 0u;
-        sh.cnt_eq = 0u;
-    }
-    __syncthreads();
-    const int per = (len + kTkThreads - 1) / kTkThreads;
-    const int i0 = min(len, tid * per), i1 = min(len, i0 + per);
+    // ---- per-warp and per-CTA counts above / equal to T
+    const int wlen = ((len + kTkWarps - 1) / kTkWarps + 31) & ~31;  // contiguous keys per warp
+    const int w0 = min(len, warp * wlen), w1 = min(len, w0 + wlen);
     uint32_t gt = 0, eq = 0;
-    for (int i = i0; i < i1; ++i) {
-        gt += keys[i] > T;
-        eq += keys[i] == T;
+    for (int i = w0 + lane; i < w1; i += 32) {
+        const uint32_t k = keys[i];
+        gt += k > T;
+        eq += k == T;
     }
-    {
-        const uint32_t g = __reduce_add_sync(0xffffffffu, gt), e = __reduce_add_sync(0xffffffffu, eq);
-        if (lane == 0) {
-            atomicAdd(&sh.cnt_gt, g);
-            atomicAdd(&sh.cnt_eq, e);
+    gt = __reduce_add_sync(0xffffffffu, gt);
+    eq = __reduce_add_sync(0xffffffffu, eq);
+    if (lane == 0) {
+        sh.wgt[warp] = gt;
+        sh.weq[warp] = eq;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        uint32_t g = 0, e = 0;
+        for (int w = 0; w < kTkWarps; ++w) {
+            g += sh.wgt[w];
+            e += sh.weq[w];
         }
+        sh.cnt_gt = g;
+        sh.cnt_eq = e;
     }
     cbar();
     uint32_t out_base = 0, eq_before = 0;
@@ -411,23 +281,27 @@ __global__ void __launch_bounds__(kTkThreads, 1)
     }
     const uint32_t my_take = min(eq_take > eq_before ? eq_take - eq_before : 0u, sh.cnt_eq);
 
-    // ---- order-preserving compaction: one packed scan (ties in the high half)
-    uint32_t tot;
-    const uint32_t pre = block_excl_scan((eq << 16) | gt, sh.warp_tot, &tot);
-    uint32_t gt_pre = pre & 0xffffu, eq_pre = pre >> 16;
-    for (int i = i0; i < i1; ++i) {
-        const uint32_t k = keys[i];
-        if (k > T) {
-            const uint32_t pos = out_base + gt_pre + min(eq_pre, my_take);
+    // ---- order-preserving compaction: a selected key's position is the number of
+    // keys above T before it plus min(keys equal to T before it, my_take).
+    uint32_t gt_run = 0, eq_run = 0;
+    for (int w = 0; w < warp; ++w) {
+        gt_run += sh.wgt[w];
+        eq_run += sh.weq[w];
+    }
+    const uint32_t lane_lt = (1u << lane) - 1u;
+    for (int i0 = w0; i0 < w1; i0 += 32) {
+        const int i = i0 + lane;
+        const uint32_t k = i < w1 ? keys[i] : 0u;
+        const bool isgt = i < w1 && k > T;
+        const bool iseq = i < w1 && k == T;
+        const uint32_t bgt = __ballot_sync(0xffffffffu, isgt), beq = __ballot_sync(0xffffffffu, iseq);
+        const uint32_t eq_b = eq_run + __popc(beq & lane_lt);
+        if (isgt || (iseq && eq_b < my_take)) {
+            const uint32_t pos = out_base + gt_run + __popc(bgt & lane_lt) + min(eq_b, my_take);
             if (pos < static_cast<uint32_t>(K)) out[pos] = cs + i;
-            ++gt_pre;
-        } else if (k == T) {
-            if (eq_pre < my_take) {
-                const uint32_t pos = out_base + gt_pre + eq_pre;
-                if (pos < static_cast<uint32_t>(K)) out[pos] = cs + i;
-            }
-            ++eq_pre;
         }
+        gt_run += __popc(bgt);
+        eq_run += __popc(beq);
     }
     if (rank == 0 && tid == 0) n_sel[q] = K;
     cbar();  // keep this CTA's shared memory alive until every peer is done reading it
@@ -440,17 +314,12 @@ kp_status launch_topk(const kp_topk_args &a, cudaStream_t s) {
     if (nq == 0) return KP_OK;
     const int K = a.cfg.topk_tokens / a.cfg.kpool;
     const int maxp = a.q.max_pools;
-    const int sms = device_sm_count();
-    if (sms <= 0) return KP_ERR_CUDA;
-    // Enough CTAs per row to hold it in shared memory; more (up to 8) while the
-    // grid is smaller than the GPU and every CTA keeps >= 2048 keys.
     // A row is latency-bound work: one CTA per row while it fits comfortably,
     // a cluster only for long rows (up to 8 CTAs of <= 32768 keys).
     int C = 1;
     while (C < kTkMaxCluster && (maxp + C - 1) / C > kTkKeysPerCta) C *= 2;
     const int chunk_cap = (maxp + C - 1) / C;
     if (chunk_cap > kTkChunkMax) return KP_ERR_UNSUPPORTED;
-    if (static_cast<int64_t>(chunk_cap) + 16 >= 65536) return KP_ERR_UNSUPPORTED;  // packed 16-bit scan
     const size_t smem = static_cast<size_t>(chunk_cap > 0 ? chunk_cap : 1) * sizeof(uint32_t);
     cudaError_t e = cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kTkChunkMax * static_cast<int>(sizeof(uint32_t)));
