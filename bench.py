@@ -437,7 +437,7 @@ def main():
             "stage_ms": stage_ms,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": 5 * args.steps,
+            "gpu_launches": step.launches_per_step() * args.steps,
             "clocks": clocks,
             "device_status": status,
         }

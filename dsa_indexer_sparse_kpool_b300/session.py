@@ -116,6 +116,17 @@ class Step:
     def run(self, stream=None) -> None:
         kp_dsa_forward(self.args, stream=stream)
 
+    def launches_per_step(self) -> int:
+        """Kernels one ``run`` launches: compress (carrying the scorer's plan in
+        an extra grid row when there are new tokens), score (plus its own plan
+        kernel otherwise), top-k and attention; no queries stops after compress."""
+        nq = self.queries.q_seq.numel()
+        new = int(self.new_off[-1].item()) > 0
+        if nq == 0:
+            return 1 if new else 0
+        fused = new and self.seqs.seq_len.numel() < 65535
+        return (1 if new else 0) + (1 if fused else 2) + 2
+
     def stage_calls(self):
         """The four stage calls on persistent buffers (capturable one by one):
         [compress, score, topk, attend]; returns (calls, scores tensor)."""
