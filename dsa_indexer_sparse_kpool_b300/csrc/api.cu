@@ -207,6 +207,7 @@ kp_status validate_attend(const kp_attend_args *a) {
     if (a->q.num_queries == 0) return KP_OK;
     if (!a->q_lat || !a->latent || !a->pool_idx || !a->n_sel || !a->out) return KP_ERR_INVALID_ARG;
     if (!aligned(a->q_lat, 16) || !aligned(a->latent, 16) || !aligned(a->out, 4)) return KP_ERR_INVALID_ARG;
+    if (a->seqs.latent_rows > INT32_MAX) return KP_ERR_UNSUPPORTED;  // TMA row coordinates are int32
     const size_t need = attend_ws_need(a->cfg, a->q.num_queries);
     if (need > 256 && (!a->workspace || a->workspace_bytes < need || !aligned(a->workspace, 256)))
         return KP_ERR_WORKSPACE;

@@ -20,12 +20,19 @@
 // 64-token tiles of latent rows (64 KB) are gathered into two shared-memory
 // slots in the 128-byte-swizzle layout, so the next tile streams in while
 // this one is computed; the S product reads a tile K-major, the P.V product
-// reads the same bytes M-major, so each latent row crosses HBM once.  S^T
+// reads the same bytes M-major, so each latent row crosses HBM once.  A
+// selected pool is kpool = 4 consecutive latent rows, so the gather is a plain
+// tiled TMA load per (pool, 64-column block): a 4-row box of 512 bytes that
+// lands at a 512-byte offset of its 1 KB swizzle atom (the swizzle follows the
+// shared-memory address, so a half atom gets the rows 4-7 pattern).  Pools
+// missing from a partial tile load rows at a negative coordinate, which the
+// TMA fills with zeros, so P.V never multiplies stale bytes.  S^T
 // (M = 64: token r in TMEM lane 32*(r/16) + r%16) and O^T (4 x 64 columns)
-// live in TMEM.  Each softmax thread owns one token: per-head tile maxima come
-// from one warp redux per head plus a 4-warp exchange; the running max is
-// raised only when a tile's max exceeds it by 2^8 (then O^T and the row sums
-// are rescaled), so the correction pass almost never runs.
+// live in TMEM.  The softmax reads S^T with the 16-lane TMEM load, so each
+// thread holds 2 tokens x 8 heads; per-head tile maxima come from three
+// shuffles per head plus a 4-warp exchange; the running max is raised only
+// when a tile's max exceeds it by 2^8 (then O^T and the row sums are
+// rescaled), so the correction pass almost never runs.
 //
 // A query's token list is split over the CTAs of a thread-block cluster
 // (up to 8).  After its tiles, each CTA dumps its unnormalised O^T, running
@@ -35,14 +42,14 @@
 // tail never costs a tensor-core tile), normalises and writes bf16 out and
 // fp32 lse.  No global scratch, no second launch.
 //
-// Warp roles (384 threads, one CTA per SM):
+// Warp roles (416 threads, one CTA per SM):
 //   warps 0-7  softmax: warp w owns TMEM lane quadrant w % 4 (tokens 16(w%4) ..
 //              +15 in lanes 0-15) and heads 32 * (w / 4) .. +31; then the O^T dump
 //   warp 8     TMEM allocation, Q TMA, MMA issue (one lane)
-//   warps 9-11 gather: cp.async 16-byte pieces of the selected rows into the
-//              swizzled tile (each warp instruction moves two whole 256-byte
-//              row segments; warp g takes token pairs g, g+3, g+6, ...), up to
-//              two tiles in flight
+//   warps 9-12 gather: warp 9 + c loads 128-column chunk c of every tile, lane
+//              l the TMA box of pool l % 16 and 64-column block 2c + l / 16
+//              (TMA issue is serial within a warp, so four warps issue at
+//              four times the rate of one)
 //   all        cluster merge and output
 #include "kp_common.cuh"
 #include "kp_internal.h"
@@ -66,9 +73,12 @@ constexpr int kAtSoftWarps = 8;
 constexpr int kAtSoftThreads = 32 * kAtSoftWarps;
 constexpr int kAtMmaWarp = 8;
 constexpr int kAtProdWarp0 = 9;
-constexpr int kAtProdWarps = 3;
+constexpr int kAtProdWarps = 4;                           // one per 128-column chunk
 constexpr int kAtProdThreads = 32 * kAtProdWarps;
-constexpr int kAtThreads = 384;
+constexpr int kAtThreads = 416;
+constexpr int kAtPoolsPerTile = kAtTok / kKpool;          // 16 pools of 4 rows
+constexpr int kAtBoxBytes = kKpool * 128;                 // one pool's rows of one 64-column block
+static_assert(kAtPoolsPerTile * 2 == 32, "one gather lane per (pool, block) of a 128-column chunk");
 constexpr int kAtTmemCols = 512;
 constexpr uint32_t kAtOCol = 0;                           // O^T: chunk c at columns 64c .. 64c+63
 constexpr uint32_t kAtSCol = 256;                         // S^T: two buffers of 64 columns
@@ -105,7 +115,7 @@ static_assert(kAtSmemBytes <= 232448, "attention shared memory over the per-CTA 
 static_assert(kAtSlots * kAtTileBytes >= kMlaHeads * kNopeDim * 4, "the merge buffer must fit in the tile slots");
 
 // mbarrier indices
-constexpr int kBarFull = 0;    // [slot][4] chunk gathered (96 producer arrivals)
+constexpr int kBarFull = 0;    // [slot][4] chunk gathered (one arrival + 16 KB of TMA bytes)
 constexpr int kBarFree = 8;    // [slot][4] chunk consumed by P.V (tcgen05.commit)
 constexpr int kBarQ = 16;      // Q landed (TMA)
 constexpr int kBarS = 17;      // [2] S^T buffer ready (commit)
@@ -177,7 +187,8 @@ __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v 
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
 __global__ void __launch_bounds__(kAtThreads, 1)
-    sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, AttendParams P) {
+    sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_lat,
+                         AttendParams P) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
@@ -210,7 +221,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     // writes, so they are read before the grid dependency resolves.
     if (tid == 0) {
         for (int c = 0; c < kAtSlots * kAtChunks; ++c) {
-            mbar_init(bar(kBarFull + c), kAtProdThreads);
+            mbar_init(bar(kBarFull + c), 1);
             mbar_init(bar(kBarFree + c), 1);
         }
         mbar_init(bar(kBarQ), 1);
@@ -223,6 +234,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         fence_mbar_init();
         *abort_s = 0;
         tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_lat);
     }
     if (tid < kMlaHeads) {
         mused_s[tid] = -INFINITY;
@@ -346,118 +358,96 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         }
     } else if (warp >= kAtProdWarp0) {
         // ------------------------------------------------------------ gather
-        const int pw = warp - kAtProdWarp0;
-        const int piece = lane & 15, sub = lane >> 4;
-        // Token pairs (2k, 2k+1) of a tile, k = pw + 3m, m < n_pairs; list index j = 2m + sub.
-        constexpr int kPairs = kAtTok / 2;
-        const int n_pairs = (kPairs - pw + kAtProdWarps - 1) / kAtProdWarps;
-        bool ok = true;
         // This CTA's selected pools, once, into shared memory (no global read
         // sits between a freed slot and its refill).
         int32_t *pools_s = reinterpret_cast<int32_t *>(misc + kMiscPools);
-        const int pool0 = tb * (kAtTok / kKpool);
-        const int npools = min(nt * (kAtTok / kKpool), ns - pool0);
+        const int pool0 = tb * kAtPoolsPerTile;
+        const int npools = min(nt * kAtPoolsPerTile, ns - pool0);
         for (int k = tid - 32 * kAtProdWarp0; k < npools; k += kAtProdThreads)
             pools_s[k] = P.pool_idx[static_cast<int64_t>(q) * P.K + pool0 + k];
         named_bar(2, kAtProdThreads);
-        // Issues the 4 chunk groups of tile jj into its slot (waiting for the
-        // slot's previous tile to be consumed by P.V).
-        auto issue = [&](int jj) {
-            const int tile = tb + jj, slot = jj & 1;
-            int64_t row = -1;
-            if (lane < 2 * n_pairs) {
-                const int tok = tile * kAtTok + 2 * (pw + kAtProdWarps * (lane >> 1)) + (lane & 1);
-                if (tok < n_pool_tok) {
-                    const int p = pools_s[tok / kKpool - pool0];
-                    if (p >= 0 && p < nf) row = base_row + static_cast<int64_t>(p) * kKpool + (tok % kKpool);
-                    else set_status(P.status, KP_ERR_DEVICE_BOUNDS);
-                }
+        const int c = warp - kAtProdWarp0;  // the 128-column chunk this warp loads
+        const int my_pool = lane % kAtPoolsPerTile, blk = 2 * c + lane / kAtPoolsPerTile;
+        bool ok = true;
+        int slot_tile[kAtSlots] = {-1, -1};   // latest tile whose chunk load was issued, per slot
+        for (int jj = 0; ok && jj < nt; ++jj) {
+            const int slot = jj & 1;
+            // First row of this lane's pool, or a coordinate wholly above row 0
+            // (zero fill) for a pool past the end of the list.
+            int y = -kKpool;
+            const int pl = jj * kAtPoolsPerTile + my_pool;
+            if (pl < npools) {
+                const int p = pools_s[pl];
+                if (p >= 0 && p < nf) y = static_cast<int>(base_row + static_cast<int64_t>(p) * kKpool);
+                else if (lane < kAtPoolsPerTile && c == 0) set_status(P.status, KP_ERR_DEVICE_BOUNDS);
             }
-            const uint32_t dst0 = sTile + slot * kAtTileBytes;
-            for (int c = 0; c < kAtChunks; ++c) {
-                if (ok && jj >= 2)
-                    ok = mbar_wait(bar(kBarFree + slot * kAtChunks + c), ((jj >> 1) - 1) & 1, abort_flag, P.status);
-                if (ok) {
-                    for (int m = 0; m < n_pairs; ++m) {
-                        const int tk = 2 * (pw + kAtProdWarps * m) + sub;
-                        const int64_t r = __shfl_sync(0xffffffffu, row, 2 * m + sub);
-                        const uint16_t *src = P.latent + (r < 0 ? 0 : r) * kLatentDim + c * 128 + piece * 8;
-                        const uint32_t dst = dst0 + (2 * c + (piece >> 3)) * kAtBlockBytes + tk * 128 +
-                                             (((piece & 7) ^ (tk & 7)) << 4);
-                        cp_async_16(dst, src, r < 0 ? 0u : 16u);
-                    }
-                }
-                cp_async_commit();  // always 4 groups per tile, so the counts below hold
+            if (jj >= 2) {  // P.V of the slot's previous tile has read this chunk
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarFree + slot * kAtChunks + c),
+                                                      ((jj >> 1) - 1) & 1, abort_flag, P.status));
+                if (!ok) break;
             }
-        };
-        // Signals each chunk of tile jj once it has landed; `newer` = 4 when the
-        // next tile's 4 groups were issued after it.
-        auto complete = [&](int jj, bool newer) {
-            const uint32_t fb = bar(kBarFull + (jj & 1) * kAtChunks);
-            if (newer) {
-                cp_async_wait<7>(); fence_proxy_async_smem(); if (ok) mbar_arrive(fb);
-                cp_async_wait<6>(); fence_proxy_async_smem(); if (ok) mbar_arrive(fb + 8);
-                cp_async_wait<5>(); fence_proxy_async_smem(); if (ok) mbar_arrive(fb + 16);
-                cp_async_wait<4>(); fence_proxy_async_smem(); if (ok) mbar_arrive(fb + 24);
-            } else {
-                cp_async_wait<3>(); fence_proxy_async_smem(); if (ok) mbar_arrive(fb);
-                cp_async_wait<2>(); fence_proxy_async_smem(); if (ok) mbar_arrive(fb + 8);
-                cp_async_wait<1>(); fence_proxy_async_smem(); if (ok) mbar_arrive(fb + 16);
-                cp_async_wait<0>(); fence_proxy_async_smem(); if (ok) mbar_arrive(fb + 24);
-            }
-        };
-        // Both slots are filled up front; afterwards tile jj+2 is issued as soon
-        // as P.V of tile jj frees its slot, and signalled as soon as it lands.
-        if (nt > 0) issue(0);
-        if (nt > 1) issue(1);
-        if (nt > 0) complete(0, nt > 1);
-        if (nt > 1) complete(1, false);
-        for (int jj = 0; ok && jj + 2 < nt; ++jj) {
-            issue(jj + 2);
-            complete(jj + 2, false);
+            const uint32_t fb = bar(kBarFull + slot * kAtChunks + c);
+            if (lane == 0) mbar_expect_tx(fb, kAtChunkBytes);
+            __syncwarp();
+            tma_load_2d(sTile + slot * kAtTileBytes + blk * kAtBlockBytes + my_pool * kAtBoxBytes, &tm_lat, fb,
+                        blk * 64, y);
+            slot_tile[slot] = jj;
         }
-        cp_async_wait<0>();
+        if (!ok) {
+            // Every load already issued lands before the shared memory is reused.
+            for (int sl = 0; sl < kAtSlots; ++sl)
+                if (slot_tile[sl] >= 0)
+                    mbar_wait(bar(kBarFull + sl * kAtChunks + c), (slot_tile[sl] >> 1) & 1, nullptr, P.status);
+        }
     } else {
         // ------------------------------------------------------------ softmax
+        // S^T keeps token 16q + i of the tile in TMEM lane 32q + i (i < 16); the
+        // 16-lane load gives thread l tokens tA = l/4 and tB = l/4 + 8 of its
+        // quadrant and, in each 8-head group g, heads 8g + 2(l%4) and + 1.
         const int quad = warp & 3, half = warp >> 2;
-        const bool has_tok = lane < 16;              // M = 64: lanes 0-15 of each quadrant
-        const int i = quad * 16 + (lane & 15);       // token of the tile
         const int hb = half * 32;                    // this warp's first head
+        const int tA = quad * 16 + (lane >> 2), tB = tA + 8;
+        const int cp = 2 * (lane & 3);               // my first head within each 8-head group
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-        float lp[32];  // row-sum partials, heads hb .. hb+31 (the running max is in mused_s)
+        // Per head k = 2g + j (head hb + 8g + cp + j): row-sum partials and the
+        // running max (log2 units; a copy of mused_s).
+        float lp[8], mr[8];
 #pragma unroll
-        for (int h = 0; h < 32; ++h) lp[h] = 0.f;
+        for (int k = 0; k < 8; ++k) {
+            lp[k] = 0.f;
+            mr[k] = -INFINITY;
+        }
         bool ok = true;
         for (int jj = 0; jj < nt; ++jj) {
             ok = named_bar_all(1, kAtSoftThreads,
                                mbar_wait(bar(kBarS + (jj & 1)), (jj >> 1) & 1, abort_flag, P.status));
             if (!ok) break;
             tc_fence_after();
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(tmem + lane_base + kAtSCol + 64 * (jj & 1) + hb, r);
+            uint32_t r[16];
+            tmem_ld_16x256b_x4(tmem + lane_base + kAtSCol + 64 * (jj & 1) + hb, r);
             tmem_ld_wait();
             const int n_valid = min(kAtTok, n_pool_tok - (tb + jj) * kAtTok);
-            const bool valid = has_tok && i < n_valid;
-            float x[32];
+            const bool vA = tA < n_valid, vB = tB < n_valid;
+            float xa[8], xb[8];
             bool high = false;  // a logit more than 2^8 above the running max
 #pragma unroll
-            for (int h = 0; h < 32; h += 4) {
-                const float4 m4 = *reinterpret_cast<const float4 *>(mused_s + hb + h);
-                x[h] = valid ? __uint_as_float(r[h]) * P.scale_log2 : -INFINITY;
-                x[h + 1] = valid ? __uint_as_float(r[h + 1]) * P.scale_log2 : -INFINITY;
-                x[h + 2] = valid ? __uint_as_float(r[h + 2]) * P.scale_log2 : -INFINITY;
-                x[h + 3] = valid ? __uint_as_float(r[h + 3]) * P.scale_log2 : -INFINITY;
-                high |= (x[h] > m4.x + kAtRescaleLog2) | (x[h + 1] > m4.y + kAtRescaleLog2) |
-                        (x[h + 2] > m4.z + kAtRescaleLog2) | (x[h + 3] > m4.w + kAtRescaleLog2);
+            for (int k = 0; k < 8; ++k) {
+                const int g = k >> 1, j = k & 1;
+                xa[k] = vA ? __uint_as_float(r[4 * g + j]) * P.scale_log2 : -INFINITY;
+                xb[k] = vB ? __uint_as_float(r[4 * g + 2 + j]) * P.scale_log2 : -INFINITY;
+                high |= (xa[k] > mr[k] + kAtRescaleLog2) | (xb[k] > mr[k] + kAtRescaleLog2);
             }
             bool rescale = false;
             if (named_bar_any(1, kAtSoftThreads, high)) {
                 // Slow path (the first tile, and whenever a head's max jumps): exact
                 // per-head tile max, raise the running max, rescale O^T and row sums.
 #pragma unroll
-                for (int h = 0; h < 32; ++h) {
-                    const float m = warp_max_f32(x[h]);
-                    if (lane == h) red_s[quad * 64 + hb + h] = m;
+                for (int k = 0; k < 8; ++k) {
+                    float m = fmaxf(xa[k], xb[k]);
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+                    if (lane < 4) red_s[quad * 64 + hb + 8 * (k >> 1) + cp + (k & 1)] = m;
                 }
                 named_bar(1, kAtSoftThreads);
                 if (tid < kMlaHeads) {
@@ -472,43 +462,43 @@ __global__ void __launch_bounds__(kAtThreads, 1)
                 }
                 named_bar(1, kAtSoftThreads);
 #pragma unroll
-                for (int h = 0; h < 32; ++h) lp[h] *= fac_s[hb + h];
+                for (int k = 0; k < 8; ++k) {
+                    const int h = hb + 8 * (k >> 1) + cp + (k & 1);
+                    lp[k] *= fac_s[h];
+                    mr[k] = mused_s[h];
+                }
                 rescale = jj > 0;
             }
-            // p = 2^(x - m), row partial sums, bf16 P (token i, heads hb..hb+31), swizzled.
-            if (has_tok) {
-                uint8_t *prow = smem + kOffP + (jj & 1) * kAtPBytes + i * 128;
+            // p = 2^(x - m), row partial sums, bf16 P rows tA and tB (128-byte swizzle).
+            {
+                uint8_t *pt = smem + kOffP + (jj & 1) * kAtPBytes;
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    uint32_t pk[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int h = 8 * k + 2 * e;
-                        const float2 m2 = *reinterpret_cast<const float2 *>(mused_s + hb + h);
-                        const float p0 = fast_exp2(x[h] - m2.x);
-                        const float p1 = fast_exp2(x[h + 1] - m2.y);
-                        lp[h] += p0;
-                        lp[h + 1] += p1;
-                        pk[e] = pack_bf16x2(p0, p1);
-                    }
-                    const int chunk = 4 * half + k;
-                    *reinterpret_cast<uint4 *>(prow + ((chunk ^ (i & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                for (int g = 0; g < 4; ++g) {
+                    const float pa0 = fast_exp2(xa[2 * g] - mr[2 * g]);
+                    const float pa1 = fast_exp2(xa[2 * g + 1] - mr[2 * g + 1]);
+                    const float pb0 = fast_exp2(xb[2 * g] - mr[2 * g]);
+                    const float pb1 = fast_exp2(xb[2 * g + 1] - mr[2 * g + 1]);
+                    lp[2 * g] += pa0 + pb0;
+                    lp[2 * g + 1] += pa1 + pb1;
+                    const int chunk = 4 * half + g;
+                    *reinterpret_cast<uint32_t *>(pt + tA * 128 + ((chunk ^ (tA & 7)) << 4) + 2 * cp) = pack_bf16x2(pa0, pa1);
+                    *reinterpret_cast<uint32_t *>(pt + tB * 128 + ((chunk ^ (tB & 7)) << 4) + 2 * cp) = pack_bf16x2(pb0, pb1);
                 }
             }
             if (rescale) {
                 // O^T must hold P.V of the previous tile before it is rescaled; P.V of
-                // this tile waits for our arrival below.  (After P, so that the
-                // logits' registers are free.)
+                // this tile waits for our arrival below.
                 mbar_wait(bar(kBarPV), (jj - 1) & 1, abort_flag, P.status);
                 tc_fence_after();
-                for (int c = 0; c < kAtChunks; ++c) {
-                    uint32_t o[32];
-                    const uint32_t ta = tmem + lane_base + kAtOCol + 64 * c + hb;
-                    tmem_ld_32x32b_x32(ta, o);
+                for (int c = 0; c < 2 * kAtChunks; ++c) {  // 16 heads at a time
+                    uint32_t o[16];
+                    const int h0c = hb + 16 * (c & 1);
+                    const uint32_t ta = tmem + lane_base + kAtOCol + 64 * (c >> 1) + h0c;
+                    tmem_ld_32x32b_x16(ta, o);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int h = 0; h < 32; ++h) o[h] = __float_as_uint(__uint_as_float(o[h]) * fac_s[hb + h]);
-                    tmem_st_32x32b_x32(ta, o);
+                    for (int h = 0; h < 16; ++h) o[h] = __float_as_uint(__uint_as_float(o[h]) * fac_s[h0c + h]);
+                    tmem_st_32x32b_x16(ta, o);
                 }
                 tmem_st_wait();
             }
@@ -519,43 +509,16 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         if (ok) ok = named_bar_all(1, kAtSoftThreads, mbar_wait(bar(kBarO), 0, abort_flag, P.status));
         if (ok) {
             tc_fence_after();
-            // Row sums: transpose-reduce the 32 per-thread partials over the warp
-            // (lane l ends with head hb + l); the quadrants are added in order below.
+            // Row sums: add the 8 threads that share my heads (fixed order), then
+            // lanes 0-3 hold the quadrant's sums; the quadrants are added in order below.
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const bool hi = lane & 16;
-                const float send = hi ? lp[j] : lp[j + 16];
-                const float keep = hi ? lp[j + 16] : lp[j];
-                lp[j] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+            for (int k = 0; k < 8; ++k) {
+                float v = lp[k];
+                v += __shfl_xor_sync(0xffffffffu, v, 4);
+                v += __shfl_xor_sync(0xffffffffu, v, 8);
+                v += __shfl_xor_sync(0xffffffffu, v, 16);
+                if (lane < 4) lpart_s[quad * 64 + hb + 8 * (k >> 1) + cp + (k & 1)] = v;
             }
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const bool hi = lane & 8;
-                const float send = hi ? lp[j] : lp[j + 8];
-                const float keep = hi ? lp[j + 8] : lp[j];
-                lp[j] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-            }
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const bool hi = lane & 4;
-                const float send = hi ? lp[j] : lp[j + 4];
-                const float keep = hi ? lp[j + 4] : lp[j];
-                lp[j] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
-            }
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const bool hi = lane & 2;
-                const float send = hi ? lp[j] : lp[j + 2];
-                const float keep = hi ? lp[j + 2] : lp[j];
-                lp[j] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
-            }
-            {
-                const bool hi = lane & 1;
-                const float send = hi ? lp[0] : lp[1];
-                const float keep = hi ? lp[1] : lp[0];
-                lp[0] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
-            }
-            lpart_s[quad * 64 + hb + lane] = lp[0];
         }
     }
 
@@ -581,14 +544,15 @@ __global__ void __launch_bounds__(kAtThreads, 1)
             const int quad = warp & 3, hb = (warp >> 2) * 32;
             const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
             const int lg = 31 - __clz(nh);
-            for (int c = 0; c < kAtChunks; ++c) {
-                uint32_t o[32];
-                tmem_ld_32x32b_x32(tmem + lane_base + kAtOCol + 64 * c + hb, o);
+            for (int c = 0; c < 2 * kAtChunks; ++c) {  // 16 heads at a time
+                uint32_t o[16];
+                const int h0c = hb + 16 * (c & 1);
+                tmem_ld_32x32b_x16(tmem + lane_base + kAtOCol + 64 * (c >> 1) + h0c, o);
                 tmem_ld_wait();
-                const int d = c * 128 + quad * 32 + lane;  // O^T rows are latent columns
+                const int d = (c >> 1) * 128 + quad * 32 + lane;  // O^T rows are latent columns
 #pragma unroll
-                for (int h = 0; h < 32; ++h) {
-                    const int hg = hb + h, owner = hg >> lg, hl = hg & (nh - 1);
+                for (int h = 0; h < 16; ++h) {
+                    const int hg = h0c + h, owner = hg >> lg, hl = hg & (nh - 1);
                     st_cluster_f32(dsmem_addr(recv_o + ((split * nh + hl) * kNopeDim + d) * 4, owner),
                                    __uint_as_float(o[h]));
                 }
@@ -771,9 +735,14 @@ kp_status launch_attend(const kp_attend_args &a, cudaStream_t s) {
     int splits = attend_splits(a.cfg, nq, sms);
     while (splits > 1 && max_active_clusters(splits) < nq) splits /= 2;
 
-    CUtensorMap tm_q;
+    // The gather addresses latent rows by a signed 32-bit TMA coordinate
+    // (validated: latent_rows <= INT32_MAX).
+    CUtensorMap tm_q, tm_lat;
     if (!make_tmap_bf16_sw128(&tm_q, a.q_lat, kLatentDim, static_cast<uint64_t>(nq) * kMlaHeads,
                               kLatentDim * 2, 64, kMlaHeads))
+        return KP_ERR_CUDA;
+    if (!make_tmap_bf16_sw128(&tm_lat, a.latent, kLatentDim, static_cast<uint64_t>(a.seqs.latent_rows),
+                              kLatentDim * 2, 64, kKpool))
         return KP_ERR_CUDA;
     AttendParams P;
     P.latent = a.latent;
@@ -794,7 +763,7 @@ kp_status launch_attend(const kp_attend_args &a, cudaStream_t s) {
 
     return launch_kernel("sparse_mla_tc_kernel", sparse_mla_tc_kernel,
                          LaunchCfg(dim3(static_cast<unsigned>(nq) * splits), dim3(kAtThreads), kAtSmemBytes, s, splits),
-                         tm_q, P);
+                         tm_q, tm_lat, P);
 }
 
 }  // namespace kp

@@ -208,7 +208,9 @@ typedef struct kp_topk_args {
  *   z_s = sm_scale * sum_{d<512} q_lat[q][h][d] * latent[row_s][d]
  *   out[q][h][:] = sum_s softmax(z)_s * latent[row_s][0..512)   (bf16, RNE)
  *   lse[q][h] = ln sum_s exp(z_s)                                (fp32)
- * An empty token set gives out = 0 and lse = -inf. */
+ * An empty token set gives out = 0 and lse = -inf.
+ * latent_rows above 2^31 - 1 returns KP_ERR_UNSUPPORTED (rows are gathered
+ * by TMA, whose coordinates are signed 32-bit). */
 typedef struct kp_attend_args {
     kp_config cfg;
     kp_seqs seqs;                 /* uses latent_row_off, latent_rows */
