@@ -20,7 +20,13 @@
 // 64-token tiles of latent rows (64 KB) are gathered into two shared-memory
 // slots in the 128-byte-swizzle layout, so the next tile streams in while
 // this one is computed; the S product reads a tile K-major, the P.V product
-// reads the same bytes M-major, so each latent row crosses HBM once.  A
+// reads the same bytes M-major, so each latent row crosses HBM once.  Q takes
+// the other 64 KB, so two slots is all that fits.  Measured on B300, these
+// small-N products cost about 50 cycles per instruction at best (about 75 with
+// operand addresses changing every instruction), whatever M is, so a tile's
+// 48 MMAs take ~1.8 us: the S product's 32 instructions are per tile, not per
+// token, which is why smaller tiles in more slots (48 tokens in three) came
+// out slower.  A
 // selected pool is kpool = 4 consecutive latent rows, so the gather is a plain
 // tiled TMA load per (pool, 64-column block): a 4-row box of 512 bytes that
 // lands at a 512-byte offset of its 1 KB swizzle atom (the swizzle follows the
@@ -46,10 +52,9 @@
 //   warps 0-7  softmax: warp w owns TMEM lane quadrant w % 4 (tokens 16(w%4) ..
 //              +15 in lanes 0-15) and heads 32 * (w / 4) .. +31; then the O^T dump
 //   warp 8     TMEM allocation, Q TMA, MMA issue (one lane)
-//   warps 9-12 gather: warp 9 + c loads 128-column chunk c of every tile, lane
-//              l the TMA box of pool l % 16 and 64-column block 2c + l / 16
-//              (TMA issue is serial within a warp, so four warps issue at
-//              four times the rate of one)
+//   warps 9-12 gather: all four load each 128-column chunk of a tile in turn,
+//              8 TMA boxes per warp per chunk (TMA issue is serial within a
+//              warp, so four warps issue at four times the rate of one)
 //   all        cluster merge and output
 #include "kp_common.cuh"
 #include "kp_internal.h"
@@ -58,7 +63,7 @@ namespace kp {
 
 namespace {
 
-constexpr int kAtTok = 64;                                // tokens per tile
+constexpr int kAtTok = 64;                                // tokens per tile (16 pools)
 constexpr int kAtSlots = 2;                               // tiles resident in shared memory
 constexpr int kAtChunks = 4;                              // 128-column chunks of a latent row
 constexpr int kAtBlockBytes = kAtTok * 128;               // [64 rows][64 bf16] swizzle block, 8 KB
@@ -74,55 +79,61 @@ constexpr int kAtSoftThreads = 32 * kAtSoftWarps;
 constexpr int kAtMmaWarp = 8;
 constexpr int kAtProdWarp0 = 9;
 constexpr int kAtProdWarps = 4;                           // one per 128-column chunk
-constexpr int kAtProdThreads = 32 * kAtProdWarps;
 constexpr int kAtThreads = 416;
+static_assert(kAtThreads == 32 * (kAtSoftWarps + 1 + kAtProdWarps), "softmax, MMA and gather warps");
 constexpr int kAtPoolsPerTile = kAtTok / kKpool;          // 16 pools of 4 rows
 constexpr int kAtBoxBytes = kKpool * 128;                 // one pool's rows of one 64-column block
-static_assert(kAtPoolsPerTile * 2 == 32, "one gather lane per (pool, block) of a 128-column chunk");
+static_assert(kAtPoolsPerTile <= 16, "a gather lane per (pool, block) of a 128-column chunk");
+static_assert(kAtTok % 16 == 0 && kAtTok <= 64, "a tile is whole K-steps of P.V and fits the M = 64 product");
+static_assert(kAtBlockBytes % 1024 == 0, "blocks start on a swizzle atom");
 constexpr int kAtTmemCols = 512;
 constexpr uint32_t kAtOCol = 0;                           // O^T: chunk c at columns 64c .. 64c+63
 constexpr uint32_t kAtSCol = 256;                         // S^T: two buffers of 64 columns
 constexpr float kAtRescaleLog2 = 8.f;                     // raise the running max only past 2^8
 
-// Shared memory (offsets from a 1024-aligned base).
+// Shared memory (offsets from a 1024-aligned base).  During the tile loop:
+// Q, the tile slots, the two P buffers and a small block of per-head state and
+// barriers.  After the loop the slots receive the pushed O^T of every split;
+// the merge's small buffers (per-split maxima and sums, tail rows and logits,
+// merge weights, row-sum partials) follow it in the slots when they fit there,
+// else they sit after the barriers.
 constexpr int kOffQ = 0;
-constexpr int kOffTile = kOffQ + kAtQBytes;               // slots; also the O dump [64][512] fp32
+constexpr int kOffTile = kOffQ + kAtQBytes;               // slots; then the pushed O^T
 constexpr int kOffP = kOffTile + kAtSlots * kAtTileBytes;
 constexpr int kOffMisc = kOffP + 2 * kAtPBytes;
 constexpr int kMiscRed = 0;                               // [4][64] f32 per-quadrant tile maxima
 constexpr int kMiscMUsed = kMiscRed + 4 * 64 * 4;         // [64] f32 running max (log2 units)
 constexpr int kMiscFac = kMiscMUsed + 64 * 4;             // [64] f32 rescale factors of this tile
 constexpr int kMiscLSum = kMiscFac + 64 * 4;              // [64] f32 row sums
-constexpr int kMiscLPart = kMiscLSum + 64 * 4;            // [4][64] f32 row sums per lane quadrant
-constexpr int kMiscRecvM = kMiscLPart + 4 * 64 * 4;       // [8][64] f32 running max pushed by each split
-constexpr int kMiscRecvL = kMiscRecvM + 8 * 64 * 4;       // [8][64] f32 row sums pushed by each split
-constexpr int kMiscTail = kMiscRecvL + 8 * 64 * 4;        // [3][512] bf16 tail rows
-constexpr int kMiscZTail = kMiscTail + kAtMaxTail * kNopeDim * 2;   // [64][4] f32 tail logits
-constexpr int kMiscW = kMiscZTail + 64 * 4 * 4;           // [64][16] f32 merge weights
-constexpr int kMaxCtaPools = KP_MAX_TOPK_POOLS;          // selected pools one CTA can cover
-// [kMaxCtaPools] i32 this CTA's selected pools: read only during the tile loop,
-// so it shares bytes with the tail rows / tail logits / merge weights, which are
-// written only after it.
-constexpr int kMiscPools = kMiscTail;
-static_assert(kMaxCtaPools * 4 <= kMiscW + 64 * 16 * 4 - kMiscTail, "pool list overlaps past the merge buffers");
-constexpr int kMiscBars = kMiscW + 64 * 16 * 4;           // mbarriers
-constexpr int kNumBars = 23;
+constexpr int kMiscBars = kMiscLSum + 64 * 4;             // mbarriers
+constexpr int kNumBars = 4 * kAtSlots * 2 + 8;
 constexpr int kMiscTmem = kMiscBars + kNumBars * 8;
 constexpr int kMiscAbort = kMiscTmem + 4;
-constexpr int kMiscBytes = kMiscAbort + 12;
+constexpr int kMiscCore = (kMiscAbort + 12 + 15) / 16 * 16;
+// The merge's small buffers, offsets from their base.
+constexpr int kAuxTail = 0;                               // [3][512] bf16 tail rows
+constexpr int kAuxZTail = kAuxTail + kAtMaxTail * kNopeDim * 2;   // [64][4] f32 tail logits
+constexpr int kAuxW = kAuxZTail + 64 * 4 * 4;             // [64][16] f32 merge weights
+constexpr int kAuxLPart = kAuxW + 64 * 16 * 4;            // [4][64] f32 row sums per lane quadrant
+constexpr int kAuxBytes = kAuxLPart + 4 * 64 * 4;
+constexpr int kMrgOBytes = kMlaHeads * kNopeDim * 4;      // [64 heads][512] f32 dump of this CTA's O^T
+static_assert(kMrgOBytes <= kAtSlots * kAtTileBytes, "the O^T dump must fit in the tile slots");
+constexpr bool kAuxInTiles = kMrgOBytes + kAuxBytes <= kAtSlots * kAtTileBytes;
+constexpr int kOffAux = kAuxInTiles ? kOffTile + kMrgOBytes : kOffMisc + kMiscCore;
+constexpr int kMiscBytes = kMiscCore + (kAuxInTiles ? 0 : kAuxBytes);
 constexpr int kAtSmemBytes = kOffMisc + kMiscBytes + 1024;  // + alignment slack
 static_assert(kAtSmemBytes <= 232448, "attention shared memory over the per-CTA limit");
-static_assert(kAtSlots * kAtTileBytes >= kMlaHeads * kNopeDim * 4, "the merge buffer must fit in the tile slots");
 
 // mbarrier indices
-constexpr int kBarFull = 0;    // [slot][4] chunk gathered (one arrival + 16 KB of TMA bytes)
-constexpr int kBarFree = 8;    // [slot][4] chunk consumed by P.V (tcgen05.commit)
-constexpr int kBarQ = 16;      // Q landed (TMA)
-constexpr int kBarS = 17;      // [2] S^T buffer ready (commit)
-constexpr int kBarP = 19;      // P written and O^T rescaled (256 softmax arrivals)
-constexpr int kBarO = 20;      // every MMA of the CTA done (commit)
-constexpr int kBarDrain = 21;  // teardown after an abort
-constexpr int kBarPV = 22;     // P.V of a tile done (commit): O^T is stable
+constexpr int kBarFull = 0;                        // [slot][4] chunk gathered (one arrival + TMA bytes)
+constexpr int kBarFree = kBarFull + 4 * kAtSlots;  // [slot][4] chunk consumed by P.V (tcgen05.commit)
+constexpr int kBarQ = kBarFree + 4 * kAtSlots;     // Q landed (TMA)
+constexpr int kBarS = kBarQ + 1;                   // [2] S^T buffer ready (commit)
+constexpr int kBarP = kBarS + 2;                   // [2] P buffer written, O^T rescaled (256 softmax arrivals)
+constexpr int kBarO = kBarP + 2;                   // every MMA of the CTA done (commit)
+constexpr int kBarDrain = kBarO + 1;               // teardown after an abort
+constexpr int kBarPV = kBarDrain + 1;              // P.V of a tile done (commit): O^T is stable
+static_assert(kBarPV + 1 == kNumBars, "barrier count");
 
 struct AttendParams {
     const uint16_t *latent;
@@ -174,14 +185,13 @@ __device__ __forceinline__ bool named_bar_any(int id, int count, bool v) {
     return r != 0;
 }
 
-__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
-    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
 
 // Byte offset of element (row, col) of a [rows][64 bf16] 128-byte-swizzled block.
 __device__ __forceinline__ uint32_t sw128_off(int row, int col) {
     return static_cast<uint32_t>(row * 128 + ((((col >> 3) ^ row) & 7) << 4) + (col & 7) * 2);
 }
+
+
 
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
@@ -199,12 +209,11 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     float *mused_s = reinterpret_cast<float *>(misc + kMiscMUsed);
     float *fac_s = reinterpret_cast<float *>(misc + kMiscFac);
     float *lsum_s = reinterpret_cast<float *>(misc + kMiscLSum);
-    float *lpart_s = reinterpret_cast<float *>(misc + kMiscLPart);
-    float *recvm_s = reinterpret_cast<float *>(misc + kMiscRecvM);
-    float *recvl_s = reinterpret_cast<float *>(misc + kMiscRecvL);
-    uint16_t *tail_s = reinterpret_cast<uint16_t *>(misc + kMiscTail);
-    float *ztail_s = reinterpret_cast<float *>(misc + kMiscZTail);
-    float *wm_s = reinterpret_cast<float *>(misc + kMiscW);
+    uint8_t *aux = smem + kOffAux;  // merge buffers: valid only after the tile loop
+    float *lpart_s = reinterpret_cast<float *>(aux + kAuxLPart);
+    uint16_t *tail_s = reinterpret_cast<uint16_t *>(aux + kAuxTail);
+    float *ztail_s = reinterpret_cast<float *>(aux + kAuxZTail);
+    float *wm_s = reinterpret_cast<float *>(aux + kAuxW);
     const uint32_t bar0 = sbase + kOffMisc + kMiscBars;
     auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
     uint32_t *tmem_s = reinterpret_cast<uint32_t *>(misc + kMiscTmem);
@@ -229,6 +238,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         mbar_init(bar(kBarS + 1), 1);
         mbar_init(bar(kBarPV), 1);
         mbar_init(bar(kBarP), kAtSoftThreads);
+        mbar_init(bar(kBarP + 1), kAtSoftThreads);
         mbar_init(bar(kBarO), 1);
         mbar_init(bar(kBarDrain), 1);
         fence_mbar_init();
@@ -280,12 +290,15 @@ __global__ void __launch_bounds__(kAtThreads, 1)
 
     if (warp == kAtMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
-        // Event-driven: S of the next tile, chunk by chunk as it lands, and P.V of
-        // the oldest softmaxed tile, whichever is ready first (non-blocking tests:
-        // a blocking wait on one would stall the other).
+        // S(t) chunk by chunk as the gather lands it; P.V(t - 1) as soon as its P
+        // is written, even between S(t)'s chunks, so tile t - 1's slot goes back
+        // to the gather without waiting for tile t's data.  S(t) reuses the S^T
+        // buffer of tile t - 2, so P.V(t - 2) (after its P) is issued before it.
+        // The thread polls with test_wait: a suspended thread would wake late
+        // with the pipe idle.
         if (lane == 0) {
             bool ok = nt == 0 || mbar_wait(bar(kBarQ), 0, abort_flag, P.status);
-            const uint32_t idesc_s = idesc_bf16_f32(kAtTok, kMlaHeads);             // M = 64
+            const uint32_t idesc_s = idesc_bf16_f32(64, kMlaHeads);                 // M = 64
             const uint32_t idesc_pv = idesc_bf16_f32(128, kMlaHeads, true, true);   // M = 128 columns
             // Descriptors are built once; a step along K or to another block adds
             // (bytes >> 4) to the start-address field (addresses stay < 256 KB).
@@ -295,56 +308,63 @@ __global__ void __launch_bounds__(kAtThreads, 1)
             const uint64_t dv0 = desc_sw128(sTile, kAtBlockBytes, 1024);
             // B of P.V = P (tokens x heads), N-major, one 64-head group wide.
             const uint64_t dp0 = desc_sw128(sP, 4096, 1024);
-            int next_s = 0, s_chunk = 0, next_pv = 0;
-            unsigned long long idle_since = 0;
-            while (ok && next_pv < nt) {
-                bool progressed = false;
-                if (next_s < nt && next_s < next_pv + 2) {
-                    const int slot = next_s & 1;
-                    if (mbar_test(bar(kBarFull + slot * kAtChunks + s_chunk), (next_s >> 1) & 1)) {
-                        tc_fence_after();
+            int pv_next = 0;  // oldest tile whose P.V is not issued yet
+            auto issue_pv = [&]() {
+                const int tp = pv_next, slot = tp % kAtSlots, pbuf = tp & 1;
+                tc_fence_after();
 #pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) {
-                            const uint32_t blk = 2 * s_chunk + (kk >> 2), koff = (kk & 3) * 32;
-                            const uint64_t ad = dt0 + ((slot * kAtTileBytes + blk * kAtBlockBytes + koff) >> 4);
-                            const uint64_t bd = dq0 + ((blk * kAtQBlockBytes + koff) >> 4);
-                            tc_mma_bf16(tmem + kAtSCol + 64 * slot, ad, bd, idesc_s, (s_chunk | kk) ? 1u : 0u);
-                        }
-                        if (++s_chunk == kAtChunks) {
-                            tc_commit(bar(kBarS + slot));
-                            s_chunk = 0;
-                            ++next_s;
-                        }
-                        progressed = true;
+                for (int c = 0; c < kAtChunks; ++c) {
+#pragma unroll
+                    for (int kk = 0; kk < kAtTok / 16; ++kk) {
+                        const uint64_t ad = dv0 + ((slot * kAtTileBytes + 2 * c * kAtBlockBytes + kk * 2048) >> 4);
+                        const uint64_t bd = dp0 + ((pbuf * kAtPBytes + kk * 2048) >> 4);
+                        tc_mma_bf16(tmem + kAtOCol + 64 * c, ad, bd, idesc_pv, (tp | kk) ? 1u : 0u);
                     }
+                    tc_commit(bar(kBarFree + slot * kAtChunks + c));
                 }
-                if (next_pv < next_s && mbar_test(bar(kBarP), next_pv & 1)) {
-                    const int slot = next_pv & 1;
+                tc_commit(bar(kBarPV));
+                ++pv_next;
+            };
+            for (int t = 0; ok && t < nt; ++t) {
+                if (pv_next < t - 1) {  // P.V(t - 2): frees the S^T buffer S(t) writes
+                    ok = mbar_spin(bar(kBarP + (pv_next & 1)), (pv_next >> 1) & 1, abort_flag, P.status);
+                    if (!ok) break;
+                    issue_pv();
+                }
+                const int slot = t % kAtSlots, sbuf = t & 1;
+                for (int c = 0; ok && c < kAtChunks; ++c) {
+                    const uint32_t fb = bar(kBarFull + slot * kAtChunks + c);
+                    const uint32_t fpar = (t / kAtSlots) & 1;
+                    if (!mbar_test(fb, fpar)) {
+                        const unsigned long long t0 = globaltimer_ns();
+                        for (uint32_t it = 1;; ++it) {
+                            if (pv_next < t && mbar_test(bar(kBarP + (pv_next & 1)), (pv_next >> 1) & 1)) issue_pv();
+                            if (mbar_test(fb, fpar)) break;
+                            if ((it & 255u) == 0 &&
+                                (*abort_flag || globaltimer_ns() - t0 > KP_WAIT_NS)) {
+                                set_status(P.status, KP_ERR_DEVICE_TIMEOUT);
+                                *abort_flag = 1;
+                                ok = false;
+                                break;
+                            }
+                        }
+                        if (!ok) break;
+                    }
                     tc_fence_after();
-                    for (int c = 0; c < kAtChunks; ++c) {
 #pragma unroll
-                        for (int kk = 0; kk < kAtTok / 16; ++kk) {
-                            const uint64_t ad = dv0 + ((slot * kAtTileBytes + 2 * c * kAtBlockBytes + kk * 2048) >> 4);
-                            const uint64_t bd = dp0 + ((slot * kAtPBytes + kk * 2048) >> 4);
-                            tc_mma_bf16(tmem + kAtOCol + 64 * c, ad, bd, idesc_pv, (next_pv | kk) ? 1u : 0u);
-                        }
-                        tc_commit(bar(kBarFree + slot * kAtChunks + c));
-                    }
-                    tc_commit(bar(kBarPV));
-                    ++next_pv;
-                    progressed = true;
-                }
-                if (progressed) {
-                    idle_since = 0;
-                } else {
-                    const unsigned long long now = globaltimer_ns();
-                    if (idle_since == 0) idle_since = now;
-                    if (*abort_flag || now - idle_since > KP_WAIT_NS) {
-                        set_status(P.status, KP_ERR_DEVICE_TIMEOUT);
-                        *abort_flag = 1;
-                        ok = false;
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t blk = 2 * c + (kk >> 2), koff = (kk & 3) * 32;
+                        const uint64_t ad = dt0 + ((slot * kAtTileBytes + blk * kAtBlockBytes + koff) >> 4);
+                        const uint64_t bd = dq0 + ((blk * kAtQBlockBytes + koff) >> 4);
+                        tc_mma_bf16(tmem + kAtSCol + 64 * sbuf, ad, bd, idesc_s, (c | kk) ? 1u : 0u);
                     }
                 }
+                if (!ok) break;
+                tc_commit(bar(kBarS + sbuf));
+            }
+            while (ok && pv_next < nt) {  // the last tiles' P.V
+                ok = mbar_spin(bar(kBarP + (pv_next & 1)), (pv_next >> 1) & 1, abort_flag, P.status);
+                if (ok) issue_pv();
             }
             if (ok) {
                 if (nt > 0) tc_commit(bar(kBarO));
@@ -358,46 +378,73 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         }
     } else if (warp >= kAtProdWarp0) {
         // ------------------------------------------------------------ gather
-        // This CTA's selected pools, once, into shared memory (no global read
-        // sits between a freed slot and its refill).
-        int32_t *pools_s = reinterpret_cast<int32_t *>(misc + kMiscPools);
+        // A tile is 4 chunks of 32 TMA boxes (16 pools x 2 64-column blocks).
+        // The four warps load every chunk together, chunk by chunk: lanes 8c ..
+        // 8c + 7 of warp w issue boxes j = 4 (l % 8) + w of chunk c (pool j % 16,
+        // block 2c + j / 16), so chunk 0 of a tile lands first and the S product
+        // starts on it while chunks 1-3 are still in flight.  Warp 0 posts each
+        // chunk's byte count (boxes of other warps may land before it: the
+        // transaction count may go negative, the phase cannot complete without
+        // this arrival).  Each lane reads its pool index one ring ahead of its
+        // slot, so no global read sits between a freed slot and its refill.
+        const int w = warp - kAtProdWarp0;
+        const int my_chunk = lane >> 3, j = 4 * (lane & 7) + w;
+        const int my_pool = j & 15, blk = 2 * my_chunk + (j >> 4);
+        const bool active = my_pool < kAtPoolsPerTile;
         const int pool0 = tb * kAtPoolsPerTile;
         const int npools = min(nt * kAtPoolsPerTile, ns - pool0);
-        for (int k = tid - 32 * kAtProdWarp0; k < npools; k += kAtProdThreads)
-            pools_s[k] = P.pool_idx[static_cast<int64_t>(q) * P.K + pool0 + k];
-        named_bar(2, kAtProdThreads);
-        const int c = warp - kAtProdWarp0;  // the 128-column chunk this warp loads
-        const int my_pool = lane % kAtPoolsPerTile, blk = 2 * c + lane / kAtPoolsPerTile;
+        const int32_t *plist = P.pool_idx + static_cast<int64_t>(q) * P.K + pool0 + my_pool;
+        auto fetch = [&](int t) -> int {
+            return (active && t * kAtPoolsPerTile + my_pool < npools) ? plist[t * kAtPoolsPerTile] : -1;
+        };
+        int pf[kAtSlots];
+#pragma unroll
+        for (int u = 0; u < kAtSlots; ++u) pf[u] = fetch(u);
         bool ok = true;
-        int slot_tile[kAtSlots] = {-1, -1};   // latest tile whose chunk load was issued, per slot
-        for (int jj = 0; ok && jj < nt; ++jj) {
-            const int slot = jj & 1;
-            // First row of this lane's pool, or a coordinate wholly above row 0
-            // (zero fill) for a pool past the end of the list.
-            int y = -kKpool;
-            const int pl = jj * kAtPoolsPerTile + my_pool;
-            if (pl < npools) {
-                const int p = pools_s[pl];
-                if (p >= 0 && p < nf) y = static_cast<int>(base_row + static_cast<int64_t>(p) * kKpool);
-                else if (lane < kAtPoolsPerTile && c == 0) set_status(P.status, KP_ERR_DEVICE_BOUNDS);
+        int issued[kAtSlots][kAtChunks];   // latest tile whose chunk this warp loaded, per slot
+#pragma unroll
+        for (int u = 0; u < kAtSlots; ++u)
+#pragma unroll
+            for (int cc = 0; cc < kAtChunks; ++cc) issued[u][cc] = -1;
+        for (int j0 = 0; ok && j0 < nt; j0 += kAtSlots) {
+#pragma unroll
+            for (int u = 0; u < kAtSlots; ++u) {  // tile jj = j0 + u lives in slot u
+                const int jj = j0 + u;
+                if (!ok || jj >= nt) break;
+                const int p = pf[u];
+                pf[u] = fetch(jj + kAtSlots);
+                // First row of this lane's pool, or a coordinate wholly above row 0
+                // (zero fill) for a pool past the end of the list.
+                int y = -kKpool;
+                if (active && jj * kAtPoolsPerTile + my_pool < npools) {
+                    if (p >= 0 && p < nf) y = static_cast<int>(base_row + static_cast<int64_t>(p) * kKpool);
+                    else set_status(P.status, KP_ERR_DEVICE_BOUNDS);
+                }
+                const uint32_t dst = sTile + u * kAtTileBytes + blk * kAtBlockBytes + my_pool * kAtBoxBytes;
+#pragma unroll
+                for (int cc = 0; cc < kAtChunks; ++cc) {
+                    if (jj >= kAtSlots) {  // P.V of the slot's previous tile has read this chunk
+                        ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarFree + u * kAtChunks + cc),
+                                                              ((jj / kAtSlots) - 1) & 1, abort_flag, P.status));
+                        if (!ok) break;
+                    }
+                    const uint32_t fb = bar(kBarFull + u * kAtChunks + cc);
+                    if (w == 0 && lane == 0) mbar_expect_tx(fb, kAtChunkBytes);
+                    if (my_chunk == cc && active) tma_load_2d(dst, &tm_lat, fb, blk * 64, y);
+                    issued[u][cc] = jj;
+                }
             }
-            if (jj >= 2) {  // P.V of the slot's previous tile has read this chunk
-                ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarFree + slot * kAtChunks + c),
-                                                      ((jj >> 1) - 1) & 1, abort_flag, P.status));
-                if (!ok) break;
-            }
-            const uint32_t fb = bar(kBarFull + slot * kAtChunks + c);
-            if (lane == 0) mbar_expect_tx(fb, kAtChunkBytes);
-            __syncwarp();
-            tma_load_2d(sTile + slot * kAtTileBytes + blk * kAtBlockBytes + my_pool * kAtBoxBytes, &tm_lat, fb,
-                        blk * 64, y);
-            slot_tile[slot] = jj;
         }
         if (!ok) {
-            // Every load already issued lands before the shared memory is reused.
-            for (int sl = 0; sl < kAtSlots; ++sl)
-                if (slot_tile[sl] >= 0)
-                    mbar_wait(bar(kBarFull + sl * kAtChunks + c), (slot_tile[sl] >> 1) & 1, nullptr, P.status);
+            // Every load this warp issued lands before the shared memory is reused
+            // (bounded: a chunk whose other boxes were never issued times out).
+#pragma unroll
+            for (int u = 0; u < kAtSlots; ++u)
+#pragma unroll
+                for (int cc = 0; cc < kAtChunks; ++cc)
+                    if (issued[u][cc] >= 0)
+                        mbar_wait(bar(kBarFull + u * kAtChunks + cc), (issued[u][cc] / kAtSlots) & 1, nullptr,
+                                  P.status);
         }
     } else {
         // ------------------------------------------------------------ softmax
@@ -481,8 +528,10 @@ __global__ void __launch_bounds__(kAtThreads, 1)
                     lp[2 * g] += pa0 + pb0;
                     lp[2 * g + 1] += pa1 + pb1;
                     const int chunk = 4 * half + g;
-                    *reinterpret_cast<uint32_t *>(pt + tA * 128 + ((chunk ^ (tA & 7)) << 4) + 2 * cp) = pack_bf16x2(pa0, pa1);
-                    *reinterpret_cast<uint32_t *>(pt + tB * 128 + ((chunk ^ (tB & 7)) << 4) + 2 * cp) = pack_bf16x2(pb0, pb1);
+                    if (quad * 16 < kAtTok) {  // lanes past the tile hold no token
+                        *reinterpret_cast<uint32_t *>(pt + tA * 128 + ((chunk ^ (tA & 7)) << 4) + 2 * cp) = pack_bf16x2(pa0, pa1);
+                        *reinterpret_cast<uint32_t *>(pt + tB * 128 + ((chunk ^ (tB & 7)) << 4) + 2 * cp) = pack_bf16x2(pb0, pb1);
+                    }
                 }
             }
             if (rescale) {
@@ -504,7 +553,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
             }
             fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(bar(kBarP));
+            mbar_arrive(bar(kBarP + (jj & 1)));
         }
         if (ok) ok = named_bar_all(1, kAtSoftThreads, mbar_wait(bar(kBarO), 0, abort_flag, P.status));
         if (ok) {
@@ -522,28 +571,26 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         }
     }
 
-    // ---- merge over the cluster: every CTA pushes its unnormalised O^T, running
-    // max and row sums into the shared memory of the CTA that owns each head,
-    // then every CTA merges its own heads from local memory.
+    // ---- merge over the cluster (pull).  Every CTA dumps its unnormalised O^T
+    // into its own tile slots as [head][512] f32 while warps 8-12 stage the
+    // tail rows and compute the tail logits of this CTA's heads; after one
+    // cluster barrier, CTA r reads heads [64r/S, 64(r+1)/S) of every CTA's dump,
+    // running max and row sums through distributed shared memory (16-byte
+    // loads), merges them in split order with the tail and writes out and lse;
+    // a second barrier keeps every dump alive until its readers are done.
+    // (Measured on B300: pushing with 4- or 16-byte remote stores into a
+    // receive buffer, or keeping more remote loads in flight, was slower.)
     tc_fence_before();
     __syncthreads();
-    if (tid < kMlaHeads && nt > 0)  // row sums in a fixed order: repeated calls give the same bits
-        lsum_s[tid] = (lpart_s[tid] + lpart_s[64 + tid]) + (lpart_s[128 + tid] + lpart_s[192 + tid]);
-    if (S > 1) cluster_barrier();  // every CTA is done with its tile slots, which receive the pushes
-    else __syncthreads();
     const bool aborted = *abort_flag != 0;
-    const uint32_t recv_o = sbase + kOffTile;  // [S][nh][512] f32
-    if (!aborted) {
-        if (tid < kMlaHeads) {
-            const int owner = tid / nh, hl = tid % nh;
-            st_cluster_f32(dsmem_addr(smem_u32(recvm_s + split * 64 + hl), owner), nt > 0 ? mused_s[tid] : -INFINITY);
-            st_cluster_f32(dsmem_addr(smem_u32(recvl_s + split * 64 + hl), owner), nt > 0 ? lsum_s[tid] : 0.f);
-        }
-        if (warp < kAtSoftWarps && nt > 0) {
+    float *dump = reinterpret_cast<float *>(smem + kOffTile);   // [64 heads][512] f32
+    if (warp < kAtSoftWarps) {
+        if (tid < kMlaHeads && nt > 0)  // row sums in a fixed order: repeated calls give the same bits
+            lsum_s[tid] = (lpart_s[tid] + lpart_s[64 + tid]) + (lpart_s[128 + tid] + lpart_s[192 + tid]);
+        if (!aborted && nt > 0) {
             tc_fence_after();
             const int quad = warp & 3, hb = (warp >> 2) * 32;
             const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-            const int lg = 31 - __clz(nh);
             for (int c = 0; c < 2 * kAtChunks; ++c) {  // 16 heads at a time
                 uint32_t o[16];
                 const int h0c = hb + 16 * (c & 1);
@@ -551,20 +598,13 @@ __global__ void __launch_bounds__(kAtThreads, 1)
                 tmem_ld_wait();
                 const int d = (c >> 1) * 128 + quad * 32 + lane;  // O^T rows are latent columns
 #pragma unroll
-                for (int h = 0; h < 16; ++h) {
-                    const int hg = h0c + h, owner = hg >> lg, hl = hg & (nh - 1);
-                    st_cluster_f32(dsmem_addr(recv_o + ((split * nh + hl) * kNopeDim + d) * 4, owner),
-                                   __uint_as_float(o[h]));
-                }
+                for (int h = 0; h < 16; ++h) dump[(h0c + h) * kNopeDim + d] = __uint_as_float(o[h]);
             }
         }
-    }
-    if (S > 1) cluster_barrier();  // every push has landed
-    else __syncthreads();
-
-    if (qvalid && !aborted) {
-        // tail rows -> shared memory
-        for (int k = tid; k < n_tail * 64; k += kAtThreads) {
+    } else if (qvalid && !aborted) {
+        constexpr int kTailThreads = kAtThreads - kAtSoftThreads;
+        const int t2 = tid - kAtSoftThreads;
+        for (int k = t2; k < n_tail * 64; k += kTailThreads) {
             const int j = k >> 6, piece = k & 63;
             const int64_t row = base_row + static_cast<int64_t>(nf) * kKpool + j;
             *reinterpret_cast<uint4 *>(tail_s + j * kNopeDim + piece * 8) =
@@ -572,10 +612,9 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         }
         // Q has landed (the tail logits read it; nothing may be in flight at exit).
         const bool have_q = mbar_wait(bar(kBarQ), 0, abort_flag, P.status);
-        __syncthreads();
-        // tail logits: one warp per (head, tail token)
-        if (have_q) {
-            for (int pr = warp; pr < nh * n_tail; pr += kAtThreads / 32) {
+        named_bar(2, kTailThreads);
+        if (have_q) {  // tail logits of this CTA's heads: one warp per (head, tail token)
+            for (int pr = warp - kAtSoftWarps; pr < nh * n_tail; pr += kTailThreads / 32) {
                 const int h = h0 + pr / n_tail, j = pr % n_tail;
                 float acc = 0.f;
 #pragma unroll
@@ -593,20 +632,36 @@ __global__ void __launch_bounds__(kAtThreads, 1)
                 if (lane == 0) ztail_s[h * 4 + j] = acc * P.scale_log2;
             }
         }
-        __syncthreads();
-        // per-head merge weights
+    }
+    if (S > 1) cluster_barrier();  // every dump, running max and row sum is written
+    else __syncthreads();
+    const bool merge_ok = !aborted && *abort_flag == 0;  // the Q wait above may have timed out
+
+    if (qvalid && merge_ok) {
+        // per-head merge weights from every split's running max and row sums
         if (tid < nh) {
             const int h = h0 + tid;
+            float ms[kAtMaxSplits], ls[kAtMaxSplits];
+#pragma unroll
+            for (int s2 = 0; s2 < kAtMaxSplits; ++s2) {
+                ms[s2] = -INFINITY;
+                ls[s2] = 0.f;
+                if (s2 < S) {
+                    ms[s2] = dsmem_ld_f32(dsmem_addr(smem_u32(mused_s + h), s2));
+                    ls[s2] = dsmem_ld_f32(dsmem_addr(smem_u32(lsum_s + h), s2));
+                }
+            }
             float M = -INFINITY;
-            for (int s2 = 0; s2 < S; ++s2) M = fmaxf(M, recvm_s[s2 * 64 + tid]);
+#pragma unroll
+            for (int s2 = 0; s2 < kAtMaxSplits; ++s2) M = fmaxf(M, ms[s2]);
             for (int j = 0; j < n_tail; ++j) M = fmaxf(M, ztail_s[h * 4 + j]);
             float L = 0.f;
             float *w = wm_s + tid * 16;
+#pragma unroll
             for (int s2 = 0; s2 < kAtMaxSplits; ++s2) {
-                const float ms = s2 < S ? recvm_s[s2 * 64 + tid] : -INFINITY;
-                const float ws = ms > -INFINITY ? fast_exp2(ms - M) : 0.f;
+                const float ws = ms[s2] > -INFINITY ? fast_exp2(ms[s2] - M) : 0.f;
                 w[s2] = ws;
-                if (ws > 0.f) L += ws * recvl_s[s2 * 64 + tid];
+                if (ws > 0.f) L += ws * ls[s2];
             }
             for (int j = 0; j < kAtMaxTail; ++j) {
                 const float wt = j < n_tail ? fast_exp2(ztail_s[h * 4 + j] - M) : 0.f;
@@ -619,20 +674,26 @@ __global__ void __launch_bounds__(kAtThreads, 1)
                     L > 0.f ? (M + fast_log2(L)) * 0.69314718055994530942f : -INFINITY;
         }
         __syncthreads();
-        // out[q][h][d] = (sum_s w_s O_s[h][d] + sum_j w_j c_j[d]) / L, 4 columns per item
-        const float *recv = reinterpret_cast<const float *>(smem + kOffTile);
+        // out[q][h][d] = (sum_s w_s O_s[h][d] + sum_j w_j c_j[d]) / L, 4 columns per item;
+        // a split with no tokens (w_s = 0) wrote no dump and is skipped.
+        const uint32_t dump_u32 = smem_u32(dump);
         for (int idx = tid; idx < nh * (kNopeDim / 4); idx += kAtThreads) {
             const int hl = idx / (kNopeDim / 4), d = 4 * (idx % (kNopeDim / 4));
             const float *w = wm_s + hl * 16;
+            const uint32_t off = static_cast<uint32_t>(((h0 + hl) * kNopeDim + d) * 4);
+            float4 v[kAtMaxSplits];
+#pragma unroll
+            for (int s2 = 0; s2 < kAtMaxSplits; ++s2)
+                if (s2 < S && w[s2] > 0.f) v[s2] = dsmem_ld_f32x4(dsmem_addr(dump_u32 + off, s2));
             float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int s2 = 0; s2 < S; ++s2) {
-                const float ws = w[s2];
+#pragma unroll
+            for (int s2 = 0; s2 < kAtMaxSplits; ++s2) {
+                const float ws = s2 < S ? w[s2] : 0.f;
                 if (ws > 0.f) {
-                    const float4 v = *reinterpret_cast<const float4 *>(recv + (s2 * nh + hl) * kNopeDim + d);
-                    a.x = fmaf(ws, v.x, a.x);
-                    a.y = fmaf(ws, v.y, a.y);
-                    a.z = fmaf(ws, v.z, a.z);
-                    a.w = fmaf(ws, v.w, a.w);
+                    a.x = fmaf(ws, v[s2].x, a.x);
+                    a.y = fmaf(ws, v[s2].y, a.y);
+                    a.z = fmaf(ws, v[s2].z, a.z);
+                    a.w = fmaf(ws, v[s2].w, a.w);
                 }
             }
             for (int j = 0; j < n_tail; ++j) {
@@ -647,7 +708,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
             *reinterpret_cast<uint2 *>(P.out + (static_cast<int64_t>(q) * kMlaHeads + h0 + hl) * kNopeDim + d) =
                 make_uint2(pack_bf16x2(a.x * il, a.y * il), pack_bf16x2(a.z * il, a.w * il));
         }
-    } else if (!qvalid && !aborted) {
+    } else if (!qvalid && merge_ok) {
         // Nothing to attend: out = 0, lse = -inf.
         for (int idx = tid; idx < nh * (kNopeDim / 2); idx += kAtThreads) {
             const int h = h0 + idx / (kNopeDim / 2), d = 2 * (idx % (kNopeDim / 2));
@@ -655,6 +716,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         }
         if (P.lse && tid < nh) P.lse[static_cast<int64_t>(q) * kMlaHeads + h0 + tid] = -INFINITY;
     }
+    if (S > 1) cluster_barrier();  // every peer is done reading this CTA's dump
 
     if (qvalid && aborted && tid == 0) mbar_wait(bar(kBarQ), 0, nullptr, P.status);  // no TMA left in flight
     tc_fence_before();

@@ -108,6 +108,24 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
         }
     }
 }
+// Same contract as mbar_wait, but polls with test_wait and never suspends:
+// for the one thread that feeds the tensor pipe, where a late wake-up leaves
+// the pipe idle.
+__device__ __forceinline__ bool mbar_spin(uint32_t bar, uint32_t parity, volatile int *abort, int32_t *status) {
+    if (mbar_test(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_test(bar, parity)) return true;
+        if ((it & 255u) == 0) {
+            if (abort && *abort) return false;
+            if (globaltimer_ns() - t0 > KP_WAIT_NS) {
+                set_status(status, KP_ERR_DEVICE_TIMEOUT);
+                if (abort) *abort = 1;
+                return false;
+            }
+        }
+    }
+}
 
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ void tma_prefetch_desc(const void *tmap) {

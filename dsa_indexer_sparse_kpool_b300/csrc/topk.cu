@@ -7,9 +7,10 @@
 // lower pool index and the kept pools are written in ascending order.
 //
 // B300 design.  A query's row of n = n_full(t) scores is split over a
-// thread-block cluster of C CTAs (C = 1 up to 16K pools; up to 8 for the
-// 262,143-pool rows of a 1M-token context), each holding its slice in shared
-// memory as order-preserving uint32 keys.
+// thread-block cluster of C CTAs (one CTA for rows up to 16K keys; longer
+// rows over as many CTAs as hold them in shared memory, and more while every
+// CTA keeps over 16K keys and all rows' CTAs still fit one wave; up to 8),
+// each holding its slice in shared memory as order-preserving uint32 keys.
 //  1. The cluster's smallest key and key span fix a shift s with at most 2048
 //     bins of width 2^s.  Each level histograms the keys inside the current
 //     range into its bins, finds the bin holding the K-th largest key and
@@ -19,7 +20,12 @@
 //     keys equal to T that are taken (the lowest indices first).  A level
 //     costs one pass over the keys and one cluster barrier: every CTA reads
 //     every peer's histogram through distributed shared memory (two buffers,
-//     so a level never waits for the previous one to be read).
+//     so a level never waits for the previous one to be read).  When the
+//     K-th largest key's bin is taken whole (it holds exactly the keys still
+//     needed, typically one key at the second level) the selection is every
+//     key >= the bin's lower edge and the search stops there; otherwise, once
+//     the chosen bin holds at most 32 keys of the row, those keys are collected
+//     and one warp ranks them against each other, which gives T directly.
 //  2. Counts of keys above / equal to T, per warp and per CTA, give every
 //     selected key its output position; each warp walks its own contiguous
 //     range of keys with lanes interleaved (no shared-memory bank conflicts),
@@ -39,7 +45,9 @@ constexpr int kTkChunkMax = 32768;    // keys per CTA (128 KB of shared memory)
 constexpr int kTkMaxCluster = 8;
 constexpr int kTkBins = 2048;
 constexpr int kTkDigit = 11;           // log2(kTkBins)
-constexpr int kTkKeysPerCta = 16384;   // preferred largest slice per CTA
+constexpr int kTkKeysPerCta = 16384;   // a row this long stays in one CTA (cluster rounds cost more than the pass)
+constexpr int kTkSmall = 32;           // a chosen bin this small is resolved by ranking
+constexpr int kTkLoadUnroll = 8;       // float4 loads a thread has in flight
 
 __device__ __forceinline__ uint32_t cluster_size() {
     uint32_t r;
@@ -102,6 +110,10 @@ struct TopkShared {
     uint32_t kmin, kmax;              // this CTA's key range
     uint32_t cnt_gt, cnt_eq;          // this CTA's keys above / equal to T
     int pick_bin, pick_need;
+    uint32_t pick_cnt;                // keys of the row in the chosen bin
+    uint32_t small_n;                 // this CTA's keys in a small chosen bin
+    uint32_t small[kTkSmall];
+    uint32_t res_T, res_need;
 };
 
 __global__ void __launch_bounds__(kTkThreads, 1)
@@ -142,12 +154,24 @@ __global__ void __launch_bounds__(kTkThreads, 1)
     uint32_t kmin = 0xffffffffu, kmax = 0u;
     if ((reinterpret_cast<uintptr_t>(row) & 15) == 0) {
         const int n4 = len >> 2;
-        for (int i = tid; i < n4; i += kTkThreads) {
-            const float4 v = __ldcs(reinterpret_cast<const float4 *>(row) + i);
-            const uint32_t a = score_key(v.x), b = score_key(v.y), c = score_key(v.z), d = score_key(v.w);
-            reinterpret_cast<uint4 *>(keys)[i] = make_uint4(a, b, c, d);
-            kmin = min(kmin, min(min(a, b), min(c, d)));
-            kmax = max(kmax, max(max(a, b), max(c, d)));
+        for (int i0 = tid; i0 < n4; i0 += kTkLoadUnroll * kTkThreads) {
+            float4 v[kTkLoadUnroll];  // every load issued before the first is used
+#pragma unroll
+            for (int u = 0; u < kTkLoadUnroll; ++u) {
+                const int i = i0 + u * kTkThreads;
+                if (i < n4) v[u] = __ldcs(reinterpret_cast<const float4 *>(row) + i);
+            }
+#pragma unroll
+            for (int u = 0; u < kTkLoadUnroll; ++u) {
+                const int i = i0 + u * kTkThreads;
+                if (i < n4) {
+                    const uint32_t a = score_key(v[u].x), b = score_key(v[u].y), c = score_key(v[u].z),
+                                   d = score_key(v[u].w);
+                    reinterpret_cast<uint4 *>(keys)[i] = make_uint4(a, b, c, d);
+                    kmin = min(kmin, min(min(a, b), min(c, d)));
+                    kmax = max(kmax, max(max(a, b), max(c, d)));
+                }
+            }
         }
         for (int i = 4 * n4 + tid; i < len; i += kTkThreads) {
             const uint32_t k = score_key(row[i]);
@@ -223,6 +247,7 @@ __global__ void __launch_bounds__(kTkThreads, 1)
             set_status(status, KP_ERR_DEVICE_BOUNDS);
             sh.pick_bin = kTkBins - 1;
             sh.pick_need = 1;
+            sh.pick_cnt = 0xffffffffu;
         }
         if (above < static_cast<uint32_t>(need) && static_cast<uint32_t>(need) <= above + sum) {
 #pragma unroll
@@ -230,6 +255,7 @@ __global__ void __launch_bounds__(kTkThreads, 1)
                 if (above < static_cast<uint32_t>(need) && above + c[j] >= static_cast<uint32_t>(need)) {
                     sh.pick_bin = b0 + kPer - 1 - j;
                     sh.pick_need = need - static_cast<int>(above);
+                    sh.pick_cnt = c[j];
                 }
                 above += c[j];
             }
@@ -237,8 +263,74 @@ __global__ void __launch_bounds__(kTkThreads, 1)
         __syncthreads();
         base += static_cast<uint32_t>(sh.pick_bin) << s;
         need = sh.pick_need;
+        const uint32_t bin_cnt = sh.pick_cnt;
         __syncthreads();  // pick_* is rewritten by the next level
         if (s == 0) break;
+        if (static_cast<uint32_t>(need) == bin_cnt && base > 0u) {
+            // Every key of the chosen bin is taken (usual once a bin holds one
+            // key): the selection is the keys >= base, i.e. above base - 1.
+            base -= 1u;
+            need = 0;
+            break;
+        }
+        if (bin_cnt <= static_cast<uint32_t>(kTkSmall)) {
+            // The chosen bin [base, base + 2^s) holds at most 32 keys of the row:
+            // collect them (every CTA) and rank them in one warp.
+            if (tid == 0) sh.small_n = 0u;
+            __syncthreads();
+            const uint64_t brange = static_cast<uint64_t>(1) << s;
+            for (int i = tid; i < len; i += kTkThreads) {
+                const uint32_t k = keys[i];
+                if (k >= base && static_cast<uint64_t>(k - base) < brange) {
+                    const uint32_t slot = atomicAdd(&sh.small_n, 1u);
+                    if (slot < static_cast<uint32_t>(kTkSmall)) sh.small[slot] = k;
+                }
+            }
+            cbar();  // every CTA's list is complete
+            if (warp == 0) {
+                uint32_t key = 0u, off = 0u;
+                bool has = false;
+                for (uint32_t r = 0; r < C; ++r) {
+                    const uint32_t nr = min(static_cast<uint32_t>(kTkSmall),
+                                            ld_cluster_u32(dsmem_addr(smem_u32(&sh.small_n), r)));
+                    if (!has && static_cast<uint32_t>(lane) >= off && static_cast<uint32_t>(lane) < off + nr) {
+                        key = ld_cluster_u32(dsmem_addr(smem_u32(&sh.small[lane - off]), r));
+                        has = true;
+                    }
+                    off += nr;
+                }
+                uint32_t gtk = 0, eqk = 0;  // keys of the bin above / equal to mine
+#pragma unroll 8
+                for (int j = 0; j < 32; ++j) {
+                    const uint32_t kj = __shfl_sync(0xffffffffu, key, j);
+                    const bool hj = __shfl_sync(0xffffffffu, has, j);
+                    gtk += hj && kj > key;
+                    eqk += hj && kj == key;
+                }
+                const bool mine = has && gtk < static_cast<uint32_t>(need) && static_cast<uint32_t>(need) <= gtk + eqk;
+                const uint32_t who = __ballot_sync(0xffffffffu, mine);
+                if (lane == 0) {
+                    if (who == 0u) {  // counts lost: cannot happen with consistent data
+                        set_status(status, KP_ERR_DEVICE_BOUNDS);
+                        sh.res_T = base;
+                        sh.res_need = 1u;
+                    }
+                }
+                if (who != 0u) {
+                    const int src = __ffs(who) - 1;
+                    const uint32_t T0 = __shfl_sync(0xffffffffu, key, src);
+                    const uint32_t g0 = __shfl_sync(0xffffffffu, gtk, src);
+                    if (lane == 0) {
+                        sh.res_T = T0;
+                        sh.res_need = static_cast<uint32_t>(need) - g0;
+                    }
+                }
+            }
+            __syncthreads();
+            base = sh.res_T;
+            need = static_cast<int>(sh.res_need);
+            break;
+        }
         wb = s;  // the chosen bin is the next range
         s = wb > kTkDigit ? wb - kTkDigit : 0;
     }
@@ -314,10 +406,16 @@ kp_status launch_topk(const kp_topk_args &a, cudaStream_t s) {
     if (nq == 0) return KP_OK;
     const int K = a.cfg.topk_tokens / a.cfg.kpool;
     const int maxp = a.q.max_pools;
-    // A row is latency-bound work: one CTA per row while it fits comfortably,
-    // a cluster only for long rows (up to 8 CTAs of <= 32768 keys).
+    // A row is latency-bound work and every cluster round costs more than a
+    // pass over 16K keys in shared memory.  The cluster is as small as shared
+    // memory allows (<= 32768 keys per CTA), then grows while every CTA keeps
+    // more than 16K keys and all rows' CTAs still fit one wave on the SMs.
     int C = 1;
-    while (C < kTkMaxCluster && (maxp + C - 1) / C > kTkKeysPerCta) C *= 2;
+    while (C < kTkMaxCluster && (maxp + C - 1) / C > kTkChunkMax) C *= 2;
+    const int64_t sms = device_sm_count() > 0 ? device_sm_count() : 1;
+    while (C < kTkMaxCluster && (maxp + C - 1) / C > kTkKeysPerCta &&
+           static_cast<int64_t>(nq) * C * 2 <= sms)
+        C *= 2;
     const int chunk_cap = (maxp + C - 1) / C;
     if (chunk_cap > kTkChunkMax) return KP_ERR_UNSUPPORTED;
     const size_t smem = static_cast<size_t>(chunk_cap > 0 ? chunk_cap : 1) * sizeof(uint32_t);
