@@ -45,7 +45,8 @@ constexpr int kScThreads = 192;
 constexpr int kScTmemCols = 512;
 constexpr int kScAccCols = 256;
 constexpr int kScNumBars = 2 * kScStages + 4 + 2;
-constexpr int kScSmemBytes = kScStages * kScAStageBytes + kScBBytes + kScNumBars * 8 + 1024;
+constexpr int kScPlanStage = 4096;                        // plan unit0 entries staged in shared memory
+constexpr int kScSmemBytes = kScStages * kScAStageBytes + kScBBytes + kScNumBars * 8 + kScPlanStage * 4 + 1024;
 
 // The plan as its own one-CTA kernel (the standalone scoring call).
 __global__ void __launch_bounds__(1024) score_plan_kernel(int nq, int num_seqs,
@@ -128,19 +129,12 @@ __global__ void __launch_bounds__(kScThreads, 1)
     __shared__ __align__(16) float w_s[kScMaxQ * kIndexHeads];  // head weights of the current group
     __shared__ int nf_s[kScMaxQ];                                 // complete pools each query sees
 
-    pdl_wait_then_release();
-    PlanView plan(const_cast<int32_t *>(P.plan), P.nq);
-    const int ng = plan.hdr[0];
-    const long long n_units = plan.hdr[1];
-    const int u_begin = static_cast<int>(n_units * blockIdx.x / gridDim.x);
-    const int u_end = static_cast<int>(n_units * (blockIdx.x + 1) / gridDim.x);
-    if (u_begin >= u_end) return;
-
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
     const uint32_t sA = smem_u32(smem);
     const uint32_t sB = sA + kScStages * kScAStageBytes;
     const uint32_t bar0 = sB + kScBBytes;
+    int32_t *unit0_s = reinterpret_cast<int32_t *>(smem + kScStages * kScAStageBytes + kScBBytes + kScNumBars * 8);
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (kScStages + s); };
     auto accf_bar = [&](int a) { return bar0 + 8u * (2 * kScStages + a); };
@@ -148,6 +142,8 @@ __global__ void __launch_bounds__(kScThreads, 1)
     const uint32_t bfull_bar = bar0 + 8u * (2 * kScStages + 4);
     const uint32_t bempty_bar = bar0 + 8u * (2 * kScStages + 5);
 
+    // Set-up that reads nothing an earlier kernel writes: before the grid
+    // dependency resolves.
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < kScStages; ++s) {
@@ -169,16 +165,35 @@ __global__ void __launch_bounds__(kScThreads, 1)
         tmem_alloc(smem_u32(&tmem_base_s), kScTmemCols);
         tmem_relinquish();
     }
+
+    // ---- the plan comes from the previous kernel.  Its header and group
+    // table are read in one round trip (the table has at most nq + 1 entries),
+    // so finding a unit's group is a search in shared memory.
+    pdl_wait_then_release();
+    PlanView plan(const_cast<int32_t *>(P.plan), P.nq);
+    const bool staged = P.nq + 1 <= kScPlanStage;
+    if (staged)
+        for (int i = threadIdx.x; i <= P.nq; i += kScThreads) unit0_s[i] = plan.unit0[i];
+    const int ng = plan.hdr[0];
+    const long long n_units = plan.hdr[1];
+    const int32_t *unit0 = staged ? unit0_s : plan.unit0;
+    const int u_begin = static_cast<int>(n_units * blockIdx.x / gridDim.x);
+    const int u_end = static_cast<int>(n_units * (blockIdx.x + 1) / gridDim.x);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base_s;
     volatile int *abort_flag = &abort_s;
+    if (u_begin >= u_end || ng <= 0) {  // no work: release the TMEM and leave
+        __syncthreads();
+        if (warp == 1) tmem_dealloc(tmem, kScTmemCols);
+        return;
+    }
 
     if (warp == 0) {
         if (lane == 0) {
             GroupCursor gc;
-            gc.init(plan.unit0, find_group(plan.unit0, ng, u_begin));
+            gc.init(unit0, find_group(unit0, ng, u_begin));
             int b_loads = 0, stage = 0;
             int64_t row_base = 0;
             uint32_t phase = 0;
@@ -212,7 +227,7 @@ __global__ void __launch_bounds__(kScThreads, 1)
     } else if (warp == 1) {
         if (lane == 0) {
             GroupCursor gc;
-            gc.init(plan.unit0, find_group(plan.unit0, ng, u_begin));
+            gc.init(unit0, find_group(unit0, ng, u_begin));
             int b_loads = 0, stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0, idesc = 0;
             for (int u = u_begin; u < u_end; ++u) {
@@ -252,7 +267,7 @@ __global__ void __launch_bounds__(kScThreads, 1)
         // shared memory when the group changes.
         const int quad = warp & 3, et = threadIdx.x - 64;
         GroupCursor gc;
-        gc.init(plan.unit0, find_group(plan.unit0, ng, u_begin));
+        gc.init(unit0, find_group(unit0, ng, u_begin));
         int acc = 0, q0 = 0, nq = 0;
         bool first = true;
         uint32_t acc_phase = 0;

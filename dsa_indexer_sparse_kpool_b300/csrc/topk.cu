@@ -124,7 +124,6 @@ __global__ void __launch_bounds__(kTkThreads, 1)
     __shared__ __align__(16) TopkShared sh;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    pdl_wait_then_release();
     const uint32_t rank = cluster_ctarank(), C = cluster_size();
     const int q = blockIdx.x / C;
     // A one-CTA row needs only block barriers.
@@ -132,9 +131,17 @@ __global__ void __launch_bounds__(kTkThreads, 1)
         if (C > 1) cluster_barrier();
         else __syncthreads();
     };
+    // Inputs and shared-memory set-up first: the scores come from the previous
+    // kernel, so only their reads wait for the grid dependency.
     const int t = q_pos[q];
     const int n = t >= 0 ? (t + 1) / kKpool : 0;
     int32_t *out = pool_idx + static_cast<int64_t>(q) * K;
+    if (tid == 0) {
+        sh.kmin = 0xffffffffu;
+        sh.kmax = 0u;
+    }
+    for (int i = tid; i < kTkBins; i += kTkThreads) sh.hist[0][i] = 0u;
+    pdl_wait_then_release();
 
     if (n <= K) {  // every visible pool is kept
         for (int i = rank * kTkThreads + tid; i < K; i += C * kTkThreads) out[i] = i < n ? i : -1;
@@ -189,11 +196,6 @@ __global__ void __launch_bounds__(kTkThreads, 1)
     }
     kmin = __reduce_min_sync(0xffffffffu, kmin);
     kmax = __reduce_max_sync(0xffffffffu, kmax);
-    if (tid == 0) {
-        sh.kmin = 0xffffffffu;
-        sh.kmax = 0u;
-    }
-    for (int i = tid; i < kTkBins; i += kTkThreads) sh.hist[0][i] = 0u;
     __syncthreads();
     if (lane == 0) {
         atomicMin(&sh.kmin, kmin);
