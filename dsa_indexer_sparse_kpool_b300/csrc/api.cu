@@ -334,10 +334,17 @@ kp_status kp_dsa_forward(const kp_forward_args *a, kp_stream_t stream) {
     if ((st = validate_attend(&at)) != KP_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const bool queries = a->q.num_queries > 0;
-    // The scorer's plan is built by an extra CTA of the compression launch
-    // (one launch fewer), except when there is nothing to compress or no room
-    // for one more row of CTAs in gridDim.y.
-    if (c.num_new > 0 && queries && c.num_seqs < 65535) {
+    // The scorer's plan: built by the scorer itself in shared memory when it
+    // fits (then the scorer also starts on the older pooled keys during the
+    // compression); otherwise by an extra CTA of the compression launch (one
+    // launch fewer), except when there is nothing to compress or no room for
+    // one more row of CTAs in gridDim.y, where the scorer's own plan kernel runs.
+    if (c.num_new > 0 && queries && score_plan_is_local(a->q.num_queries)) {
+        // The scorer builds its plan itself and loads the pooled keys older than
+        // this step while the compression runs.
+        if ((st = launch_compress(c, s)) != KP_OK) return st;
+        if ((st = launch_score(sc, s, false, c.prev_len)) != KP_OK) return st;
+    } else if (c.num_new > 0 && queries && c.num_seqs < 65535) {
         const ScorePlanArgs pa = score_plan_args(sc);
         if ((st = launch_compress(c, s, &pa)) != KP_OK) return st;
         if ((st = launch_score(sc, s, true)) != KP_OK) return st;
@@ -381,3 +388,11 @@ kp_status kp_read_device_status(const int32_t *d_status, kp_stream_t stream) {
 int kp_version(void) { return 100; }
 
 }  // extern "C"
+
+namespace kp {
+kp_status score_with_workspace_plan(const kp_score_args *a, cudaStream_t stream) {
+    const kp_status st = validate_score(a);
+    if (st != KP_OK || a->q.num_queries == 0) return st;
+    return launch_score(*a, stream, false, nullptr, false);
+}
+}  // namespace kp

@@ -87,10 +87,18 @@ ScorePlanArgs score_plan_args(const kp_score_args &a);
 
 // Launchers (arguments already validated).  launch_compress with a plan also
 // builds the scorer's plan (one extra CTA); launch_score with plan_ready then
-// skips its own plan kernel.
+// skips its own plan kernel.  Up to score_plan_is_local(nq) queries the scorer
+// builds its plan in shared memory (no plan kernel, no plan read) unless
+// allow_local_plan is false; with prev_len (the compression's prev_len) it
+// also loads pooled-key tiles that the compression cannot have written before
+// waiting for it.
 kp_status launch_compress(const kp_compress_args &a, cudaStream_t s, const ScorePlanArgs *plan = nullptr);
-kp_status launch_score(const kp_score_args &a, cudaStream_t s, bool plan_ready = false);
+bool score_plan_is_local(int32_t num_queries);
+kp_status launch_score(const kp_score_args &a, cudaStream_t s, bool plan_ready = false,
+                       const int32_t *prev_len = nullptr, bool allow_local_plan = true);
 kp_status launch_topk(const kp_topk_args &a, cudaStream_t s);
+// kp_indexer_score with its plan always in the caller's workspace (validated).
+kp_status score_with_workspace_plan(const kp_score_args *a, cudaStream_t stream);
 kp_status launch_attend(const kp_attend_args &a, cudaStream_t s);
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }

@@ -77,5 +77,5 @@ extern "C" kp_status kp_indexer_score_noalloc(const kp_score_args *a, kp_stream_
     kp_score_args b = *a;
     b.workspace = plan;
     b.workspace_bytes = sizeof(int32_t) * kp::kNoallocPlanWords;
-    return kp_indexer_score(&b, stream);
+    return kp::score_with_workspace_plan(&b, reinterpret_cast<cudaStream_t>(stream));
 }

@@ -45,7 +45,8 @@ constexpr int kScThreads = 192;
 constexpr int kScTmemCols = 512;
 constexpr int kScAccCols = 256;
 constexpr int kScNumBars = 2 * kScStages + 4 + 2;
-constexpr int kScPlanStage = 4096;                        // plan unit0 entries staged in shared memory
+constexpr int kScPlanStage = 4096;                        // plan words held in shared memory
+constexpr int kScLocalPlanMaxQ = (kScPlanStage - 5) / 4;  // queries whose whole plan fits there
 constexpr int kScSmemBytes = kScStages * kScAStageBytes + kScBBytes + kScNumBars * 8 + kScPlanStage * 4 + 1024;
 
 // The plan as its own one-CTA kernel (the standalone scoring call).
@@ -60,8 +61,13 @@ __global__ void __launch_bounds__(1024) score_plan_kernel(int nq, int num_seqs,
 }
 
 struct ScoreParams {
-    const int32_t *plan;
+    const int32_t *plan;       // the plan in global memory (when not built here)
     int nq;
+    bool local_plan;           // build the plan in shared memory from q_seq / q_pos
+    int num_seqs;
+    int max_tiles;
+    const int32_t *q_seq;
+    const int32_t *prev_len;   // tokens of each sequence before this step (nullptr: no early loads)
     const int32_t *q_pos;
     const float *w;
     const int64_t *pool_row_off;
@@ -166,25 +172,41 @@ __global__ void __launch_bounds__(kScThreads, 1)
         tmem_relinquish();
     }
 
-    // ---- the plan comes from the previous kernel.  Its header and group
-    // table are read in one round trip (the table has at most nq + 1 entries),
-    // so finding a unit's group is a search in shared memory.
-    pdl_wait_then_release();
-    PlanView plan(const_cast<int32_t *>(P.plan), P.nq);
-    const bool staged = P.nq + 1 <= kScPlanStage;
-    if (staged)
-        for (int i = threadIdx.x; i <= P.nq; i += kScThreads) unit0_s[i] = plan.unit0[i];
-    const int ng = plan.hdr[0];
-    const long long n_units = plan.hdr[1];
-    const int32_t *unit0 = staged ? unit0_s : plan.unit0;
-    const int u_begin = static_cast<int>(n_units * blockIdx.x / gridDim.x);
-    const int u_end = static_cast<int>(n_units * (blockIdx.x + 1) / gridDim.x);
+    // ---- the plan.  Built right here from the query positions when it fits
+    // in shared memory (it depends only on inputs, so this overlaps the
+    // previous kernel); otherwise it comes from the previous kernel, and its
+    // header and group table are read in one round trip (the table has at
+    // most nq + 1 entries), so finding a unit's group is a search in shared
+    // memory.  Only reads of pooled keys that this step's compression may have
+    // written need the grid dependency: with prev_len given, the producer
+    // loads tiles wholly below each sequence's first new pool before waiting.
+    __shared__ int plan_scratch[33];
+    int32_t *plan_base;
+    bool dep_done = false;
+    if (P.local_plan) {
+        build_score_plan(P.nq, P.num_seqs, P.q_seq, P.q_pos, P.max_tiles, unit0_s, P.status, plan_scratch);
+        plan_base = unit0_s;
+    } else {
+        pdl_wait_then_release();
+        dep_done = true;
+        const PlanView gplan(const_cast<int32_t *>(P.plan), P.nq);
+        if (P.nq + 1 <= kScPlanStage)
+            for (int i = threadIdx.x; i <= P.nq; i += kScThreads) unit0_s[i] = gplan.unit0[i];
+        plan_base = const_cast<int32_t *>(P.plan);
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    const PlanView plan(plan_base, P.nq);
+    const int ng = plan.hdr[0];
+    const long long n_units = plan.hdr[1];
+    const int32_t *unit0 = (P.local_plan || P.nq + 1 > kScPlanStage) ? plan.unit0 : unit0_s;
+    const int u_begin = static_cast<int>(n_units * blockIdx.x / gridDim.x);
+    const int u_end = static_cast<int>(n_units * (blockIdx.x + 1) / gridDim.x);
     const uint32_t tmem = tmem_base_s;
     volatile int *abort_flag = &abort_s;
     if (u_begin >= u_end || ng <= 0) {  // no work: release the TMEM and leave
+        if (!dep_done && threadIdx.x == 0) pdl_wait_then_release();
         __syncthreads();
         if (warp == 1) tmem_dealloc(tmem, kScTmemCols);
         return;
@@ -197,6 +219,7 @@ __global__ void __launch_bounds__(kScThreads, 1)
             int b_loads = 0, stage = 0;
             int64_t row_base = 0;
             uint32_t phase = 0;
+            int old_pools = 0;  // pools of the group's sequence complete before this step
             for (int u = u_begin; u < u_end; ++u) {
                 if (gc.seek(u) || b_loads == 0) {
                     const int g = gc.g;
@@ -205,6 +228,7 @@ __global__ void __launch_bounds__(kScThreads, 1)
                         break;
                     const int q0 = plan.q0[g], nq = plan.nq[g];
                     row_base = P.pool_row_off[plan.seq[g]];
+                    old_pools = P.prev_len ? P.prev_len[plan.seq[g]] / kKpool : 0;
                     mbar_expect_tx(bfull_bar, nq * 2 * kScQBoxBytes);
                     for (int qi = 0; qi < nq; ++qi)
                         for (int kb = 0; kb < 2; ++kb)
@@ -213,6 +237,10 @@ __global__ void __launch_bounds__(kScThreads, 1)
                     ++b_loads;
                 }
                 if (!mbar_wait(empty_bar(stage), phase ^ 1, abort_flag, P.status)) break;
+                if (!dep_done && (u - gc.u0 + 1) * kScM > old_pools) {  // may hold pools written this step
+                    pdl_wait_then_release();
+                    dep_done = true;
+                }
                 mbar_expect_tx(full_bar(stage), kScAStageBytes);
                 const int row = static_cast<int>(row_base + static_cast<int64_t>(u - gc.u0) * kScM);
                 const uint32_t dst = sA + stage * kScAStageBytes;
@@ -223,6 +251,9 @@ __global__ void __launch_bounds__(kScThreads, 1)
                     phase ^= 1;
                 }
             }
+            // This grid completes only after the previous one: kernels that wait
+            // on this one may rely on everything before it.
+            if (!dep_done) pdl_wait_then_release();
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -339,14 +370,18 @@ ScorePlanArgs score_plan_args(const kp_score_args &a) {
     return p;
 }
 
-kp_status launch_score(const kp_score_args &a, cudaStream_t s, bool plan_ready) {
+bool score_plan_is_local(int32_t num_queries) { return num_queries <= kScLocalPlanMaxQ; }
+
+kp_status launch_score(const kp_score_args &a, cudaStream_t s, bool plan_ready, const int32_t *prev_len,
+                       bool allow_local_plan) {
     const int nq = a.q.num_queries;
     if (nq == 0) return KP_OK;
     const int sms = device_sm_count();
     if (sms <= 0) return KP_ERR_CUDA;
     int32_t *plan = static_cast<int32_t *>(a.workspace);
     const int max_tiles = (a.q.max_pools + kScM - 1) / kScM;
-    if (!plan_ready) {
+    const bool local_plan = allow_local_plan && score_plan_is_local(nq);
+    if (!plan_ready && !local_plan) {
         const kp_status st = launch_kernel("score_plan_kernel", score_plan_kernel,
                                            LaunchCfg(dim3(1), dim3(1024), 0, s), nq, a.seqs.num_seqs, a.q.q_seq,
                                            a.q.q_pos, max_tiles, plan, a.d_status);
@@ -369,6 +404,11 @@ kp_status launch_score(const kp_score_args &a, cudaStream_t s, bool plan_ready) 
     ScoreParams P;
     P.plan = plan;
     P.nq = nq;
+    P.local_plan = local_plan;
+    P.num_seqs = a.seqs.num_seqs;
+    P.max_tiles = max_tiles;
+    P.q_seq = a.q.q_seq;
+    P.prev_len = local_plan ? prev_len : nullptr;
     P.q_pos = a.q.q_pos;
     P.w = a.w;
     P.pool_row_off = a.seqs.pool_row_off;

@@ -16,6 +16,11 @@ from . import (Config, Queries, Seqs, forward_args, kp_dsa_forward, kp_indexer_s
                kp_workspace_size, score_stride, INDEX_DIM, MLA_HEADS, NOPE_DIM)
 
 
+# Queries up to which the library's scorer builds its work plan in shared
+# memory (4096 plan words: a 4-word header, four words per query, one more).
+SCORE_LOCAL_PLAN_MAX_QUERIES = (4096 - 5) // 4
+
+
 def _dev_i32(x, device):
     return torch.as_tensor(x, dtype=torch.int32).to(device).contiguous()
 
@@ -117,15 +122,17 @@ class Step:
         kp_dsa_forward(self.args, stream=stream)
 
     def launches_per_step(self) -> int:
-        """Kernels one ``run`` launches: compress (carrying the scorer's plan in
-        an extra grid row when there are new tokens), score (plus its own plan
-        kernel otherwise), top-k and attention; no queries stops after compress."""
+        """Kernels one ``run`` launches: compress, score, top-k and attention;
+        no queries stops after compress.  The scorer builds its own work plan
+        up to SCORE_LOCAL_PLAN_MAX_QUERIES queries; above that the plan rides in
+        an extra grid row of the compression launch when there are new tokens,
+        else it is one more kernel."""
         nq = self.queries.q_seq.numel()
         new = int(self.new_off[-1].item()) > 0
         if nq == 0:
             return 1 if new else 0
-        fused = new and self.seqs.seq_len.numel() < 65535
-        return (1 if new else 0) + (1 if fused else 2) + 2
+        plan_free = nq <= SCORE_LOCAL_PLAN_MAX_QUERIES or (new and self.seqs.seq_len.numel() < 65535)
+        return (1 if new else 0) + (1 if plan_free else 2) + 2
 
     def stage_calls(self):
         """The four stage calls on persistent buffers (capturable one by one):
