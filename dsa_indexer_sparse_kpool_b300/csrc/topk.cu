@@ -11,6 +11,9 @@
 // rows over as many CTAs as hold them in shared memory, and more while every
 // CTA keeps over 16K keys and all rows' CTAs still fit one wave; up to 8),
 // each holding its slice in shared memory as order-preserving uint32 keys.
+// A CTA has 1024 threads when every row's CTAs fit one wave on the SMs (few
+// rows: shorter passes cut the latency) and 512 otherwise (many rows: the SMs
+// are full either way and block barriers are cheaper).
 //  1. The cluster's smallest key and key span fix a shift s with at most 2048
 //     bins of width 2^s.  Each level histograms the keys inside the current
 //     range into its bins, finds the bin holding the K-th largest key and
@@ -39,8 +42,9 @@ namespace kp {
 
 namespace {
 
-constexpr int kTkThreads = 512;
-constexpr int kTkWarps = kTkThreads / 32;
+constexpr int kTkMaxThreads = 1024;    // CTA size when every row's CTAs fit one wave (latency)
+constexpr int kTkMinThreads = 512;     // otherwise (many rows: throughput)
+constexpr int kTkMaxWarps = kTkMaxThreads / 32;
 constexpr int kTkChunkMax = 32768;    // keys per CTA (128 KB of shared memory)
 constexpr int kTkMaxCluster = 8;
 constexpr int kTkBins = 2048;
@@ -65,6 +69,11 @@ __device__ __forceinline__ uint4 ld_cluster_u32x4(uint32_t addr) {
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "r"(addr)
                  : "memory");
+    return v;
+}
+__device__ __forceinline__ uint2 ld_cluster_u32x2(uint32_t addr) {
+    uint2 v;
+    asm volatile("ld.shared::cluster.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
     return v;
 }
 
@@ -106,7 +115,7 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *warp_t
 struct TopkShared {
     uint32_t hist[2][kTkBins];        // this CTA's histogram of a level (two buffers)
     uint32_t warp_tot[32];
-    uint32_t wgt[kTkWarps], weq[kTkWarps];  // per-warp counts above / equal to T
+    uint32_t wgt[kTkMaxWarps], weq[kTkMaxWarps];  // per-warp counts above / equal to T
     uint32_t kmin, kmax;              // this CTA's key range
     uint32_t cnt_gt, cnt_eq;          // this CTA's keys above / equal to T
     int pick_bin, pick_need;
@@ -116,10 +125,12 @@ struct TopkShared {
     uint32_t res_T, res_need;
 };
 
+template <int kTkThreads>
 __global__ void __launch_bounds__(kTkThreads, 1)
     topk_select_kernel(const float *__restrict__ scores, int64_t stride,
                        const int32_t *__restrict__ q_pos, int K, int32_t *__restrict__ pool_idx,
                        int32_t *__restrict__ n_sel, int chunk_cap, int32_t *status) {
+    constexpr int kTkWarps = kTkThreads / 32;
     extern __shared__ uint32_t keys[];
     __shared__ __align__(16) TopkShared sh;
 
@@ -217,7 +228,7 @@ __global__ void __launch_bounds__(kTkThreads, 1)
     uint32_t base = gmin;
     int need = K;
     constexpr int kPer = kTkBins / kTkThreads;  // bins per thread in the scan
-    static_assert(kPer == 4, "the histogram scan reads four bins per thread");
+    static_assert(kPer == 2 || kPer == 4, "the histogram scan reads two or four bins per thread");
     for (int level = 0;; ++level) {
         uint32_t *hist = sh.hist[level & 1];
         if (level > 0) {  // this buffer was last read by peers two levels ago
@@ -230,16 +241,24 @@ __global__ void __launch_bounds__(kTkThreads, 1)
             if (k >= base && static_cast<uint64_t>(k - base) < range) atomicAdd(&hist[(k - base) >> s], 1u);
         }
         cbar();  // every CTA's histogram of this level is complete
-        // Cluster totals of this thread's four bins, read from every CTA; the
-        // thread holds bins b0+3 .. b0 (descending key order across threads).
+        // Cluster totals of this thread's kPer bins, read from every CTA; the
+        // thread holds bins b0+kPer-1 .. b0 (descending key order across threads).
         const int b0 = kTkBins - kPer * (tid + 1);
-        uint32_t c[kPer] = {0u, 0u, 0u, 0u}, sum = 0;
+        uint32_t c[kPer], sum = 0;
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) c[j] = 0u;
         for (uint32_t r = 0; r < C; ++r) {
-            const uint4 v = ld_cluster_u32x4(dsmem_addr(smem_u32(hist + b0), r));
-            c[0] += v.w;
-            c[1] += v.z;
-            c[2] += v.y;
-            c[3] += v.x;
+            if constexpr (kPer == 4) {
+                const uint4 v = ld_cluster_u32x4(dsmem_addr(smem_u32(hist + b0), r));
+                c[0] += v.w;
+                c[1] += v.z;
+                c[2] += v.y;
+                c[3] += v.x;
+            } else {
+                const uint2 v = ld_cluster_u32x2(dsmem_addr(smem_u32(hist + b0), r));
+                c[0] += v.y;
+                c[1] += v.x;
+            }
         }
 #pragma unroll
         for (int j = 0; j < kPer; ++j) sum += c[j];
@@ -421,15 +440,20 @@ kp_status launch_topk(const kp_topk_args &a, cudaStream_t s) {
     const int chunk_cap = (maxp + C - 1) / C;
     if (chunk_cap > kTkChunkMax) return KP_ERR_UNSUPPORTED;
     const size_t smem = static_cast<size_t>(chunk_cap > 0 ? chunk_cap : 1) * sizeof(uint32_t);
-    cudaError_t e = cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    // Few rows (every CTA in one wave): the wider CTA shortens each pass.  Many
+    // rows: the narrower one, since the SMs are full either way.
+    const bool wide = static_cast<int64_t>(nq) * C <= sms;
+    auto kern = wide ? topk_select_kernel<kTkMaxThreads> : topk_select_kernel<kTkMinThreads>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kTkChunkMax * static_cast<int>(sizeof(uint32_t)));
     if (e != cudaSuccess) {
         record_cuda_error("cudaFuncSetAttribute(topk_select_kernel)", e);
         return KP_ERR_CUDA;
     }
-    return launch_kernel("topk_select_kernel", topk_select_kernel,
-                         LaunchCfg(dim3(static_cast<unsigned>(nq) * C), dim3(kTkThreads), smem, s, C), a.scores,
-                         a.score_stride, a.q.q_pos, K, a.pool_idx, a.n_sel, chunk_cap, a.d_status);
+    return launch_kernel("topk_select_kernel", kern,
+                         LaunchCfg(dim3(static_cast<unsigned>(nq) * C), dim3(wide ? kTkMaxThreads : kTkMinThreads),
+                                   smem, s, C),
+                         a.scores, a.score_stride, a.q.q_pos, K, a.pool_idx, a.n_sel, chunk_cap, a.d_status);
 }
 
 }  // namespace kp
