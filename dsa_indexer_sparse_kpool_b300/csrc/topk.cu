@@ -116,7 +116,10 @@ struct TopkShared {
     uint32_t hist[2][kTkBins];        // this CTA's histogram of a level (two buffers)
     uint32_t warp_tot[32];
     uint32_t wgt[kTkMaxWarps], weq[kTkMaxWarps];  // per-warp counts above / equal to T
+    uint32_t wgt_before[kTkMaxWarps], weq_before[kTkMaxWarps];  // the same summed over earlier warps
     uint32_t kmin, kmax;              // this CTA's key range
+    uint32_t gmin, gmax;              // the cluster's key range
+    uint32_t out_base, eq_before;     // output offset and equal keys of earlier CTAs
     uint32_t cnt_gt, cnt_eq;          // this CTA's keys above / equal to T
     int pick_bin, pick_need;
     uint32_t pick_cnt;                // keys of the row in the chosen bin
@@ -213,11 +216,23 @@ __global__ void __launch_bounds__(kTkThreads, 1)
         atomicMax(&sh.kmax, kmax);
     }
     cbar();
-    uint32_t gmin = 0xffffffffu, gmax = 0u;
-    for (uint32_t r = 0; r < C; ++r) {
-        gmin = min(gmin, ld_cluster_u32(dsmem_addr(smem_u32(&sh.kmin), r)));
-        gmax = max(gmax, ld_cluster_u32(dsmem_addr(smem_u32(&sh.kmax), r)));
+    // One warp gathers the cluster's key range (every thread reading the same
+    // remote words would serialise on them) and broadcasts it.
+    if (warp == 0) {
+        uint32_t mn = 0xffffffffu, mx = 0u;
+        if (static_cast<uint32_t>(lane) < C) {
+            mn = ld_cluster_u32(dsmem_addr(smem_u32(&sh.kmin), lane));
+            mx = ld_cluster_u32(dsmem_addr(smem_u32(&sh.kmax), lane));
+        }
+        mn = __reduce_min_sync(0xffffffffu, mn);
+        mx = __reduce_max_sync(0xffffffffu, mx);
+        if (lane == 0) {
+            sh.gmin = mn;
+            sh.gmax = mx;
+        }
     }
+    __syncthreads();
+    const uint32_t gmin = sh.gmin, gmax = sh.gmax;
 
     // ---- radix select: the range [base, base + 2^wb) holds the K-th largest key;
     // a level splits it into bins of width 2^s (at most 2048 of them).
@@ -249,13 +264,15 @@ __global__ void __launch_bounds__(kTkThreads, 1)
         for (int j = 0; j < kPer; ++j) c[j] = 0u;
         for (uint32_t r = 0; r < C; ++r) {
             if constexpr (kPer == 4) {
-                const uint4 v = ld_cluster_u32x4(dsmem_addr(smem_u32(hist + b0), r));
+                const uint4 v = C == 1 ? *reinterpret_cast<const uint4 *>(hist + b0)
+                                       : ld_cluster_u32x4(dsmem_addr(smem_u32(hist + b0), r));
                 c[0] += v.w;
                 c[1] += v.z;
                 c[2] += v.y;
                 c[3] += v.x;
             } else {
-                const uint2 v = ld_cluster_u32x2(dsmem_addr(smem_u32(hist + b0), r));
+                const uint2 v = C == 1 ? *reinterpret_cast<const uint2 *>(hist + b0)
+                                       : ld_cluster_u32x2(dsmem_addr(smem_u32(hist + b0), r));
                 c[0] += v.y;
                 c[1] += v.x;
             }
@@ -374,33 +391,52 @@ __global__ void __launch_bounds__(kTkThreads, 1)
         sh.weq[warp] = eq;
     }
     __syncthreads();
-    if (tid == 0) {
-        uint32_t g = 0, e = 0;
-        for (int w = 0; w < kTkWarps; ++w) {
-            g += sh.wgt[w];
-            e += sh.weq[w];
+    // Warp 0 turns the per-warp counts into exclusive prefixes (a shuffle scan)
+    // and the CTA's totals.
+    if (warp == 0) {
+        const uint32_t g = lane < kTkWarps ? sh.wgt[lane] : 0u, e = lane < kTkWarps ? sh.weq[lane] : 0u;
+        uint32_t gi = g, ei = e;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t gu = __shfl_up_sync(0xffffffffu, gi, o), eu = __shfl_up_sync(0xffffffffu, ei, o);
+            if (lane >= o) {
+                gi += gu;
+                ei += eu;
+            }
         }
-        sh.cnt_gt = g;
-        sh.cnt_eq = e;
+        if (lane < kTkWarps) {
+            sh.wgt_before[lane] = gi - g;
+            sh.weq_before[lane] = ei - e;
+        }
+        if (lane == 31) {
+            sh.cnt_gt = gi;
+            sh.cnt_eq = ei;
+        }
     }
     cbar();
-    uint32_t out_base = 0, eq_before = 0;
-    for (uint32_t r = 0; r < rank; ++r) {
-        const uint32_t gt_r = ld_cluster_u32(dsmem_addr(smem_u32(&sh.cnt_gt), r));
-        const uint32_t eq_r = ld_cluster_u32(dsmem_addr(smem_u32(&sh.cnt_eq), r));
-        const uint32_t rem = eq_take > eq_before ? eq_take - eq_before : 0u;
-        out_base += gt_r + min(rem, eq_r);
-        eq_before += eq_r;
+    // This CTA's first output position and share of the keys equal to T, from
+    // the counts of the CTAs before it (one thread reads them, then broadcasts).
+    if (C > 1) {
+        if (tid == 0) {
+            uint32_t ob = 0, eb = 0;
+            for (uint32_t r = 0; r < rank; ++r) {
+                const uint32_t gt_r = ld_cluster_u32(dsmem_addr(smem_u32(&sh.cnt_gt), r));
+                const uint32_t eq_r = ld_cluster_u32(dsmem_addr(smem_u32(&sh.cnt_eq), r));
+                const uint32_t rem = eq_take > eb ? eq_take - eb : 0u;
+                ob += gt_r + min(rem, eq_r);
+                eb += eq_r;
+            }
+            sh.out_base = ob;
+            sh.eq_before = eb;
+        }
+        __syncthreads();
     }
+    const uint32_t out_base = C > 1 ? sh.out_base : 0u, eq_before = C > 1 ? sh.eq_before : 0u;
     const uint32_t my_take = min(eq_take > eq_before ? eq_take - eq_before : 0u, sh.cnt_eq);
 
     // ---- order-preserving compaction: a selected key's position is the number of
     // keys above T before it plus min(keys equal to T before it, my_take).
-    uint32_t gt_run = 0, eq_run = 0;
-    for (int w = 0; w < warp; ++w) {
-        gt_run += sh.wgt[w];
-        eq_run += sh.weq[w];
-    }
+    uint32_t gt_run = sh.wgt_before[warp], eq_run = sh.weq_before[warp];
     const uint32_t lane_lt = (1u << lane) - 1u;
     for (int i0 = w0; i0 < w1; i0 += 32) {
         const int i = i0 + lane;
