@@ -149,7 +149,16 @@ __global__ void __launch_bounds__(kScThreads, 1)
     const uint32_t bempty_bar = bar0 + 8u * (2 * kScStages + 5);
 
     // Set-up that reads nothing an earlier kernel writes: before the grid
-    // dependency resolves.
+    // dependency resolves.  The query sequences and positions the local plan
+    // is built from are fetched first, so their latency hides behind the rest.
+    const int plan_words = 4 + 4 * P.nq + 1;
+    const bool stage_q = P.local_plan && plan_words + 2 * P.nq <= kScPlanStage;
+    int32_t *qseq_s = unit0_s + plan_words, *qpos_s = qseq_s + P.nq;
+    if (stage_q)
+        for (int i = threadIdx.x; i < P.nq; i += kScThreads) {
+            qseq_s[i] = P.q_seq[i];
+            qpos_s[i] = P.q_pos[i];
+        }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < kScStages; ++s) {
@@ -184,7 +193,9 @@ __global__ void __launch_bounds__(kScThreads, 1)
     int32_t *plan_base;
     bool dep_done = false;
     if (P.local_plan) {
-        build_score_plan(P.nq, P.num_seqs, P.q_seq, P.q_pos, P.max_tiles, unit0_s, P.status, plan_scratch);
+        if (stage_q) __syncthreads();
+        build_score_plan(P.nq, P.num_seqs, stage_q ? qseq_s : P.q_seq, stage_q ? qpos_s : P.q_pos, P.max_tiles,
+                         unit0_s, P.status, plan_scratch);
         plan_base = unit0_s;
     } else {
         pdl_wait_then_release();
