@@ -10,6 +10,7 @@ import torch
 import kpool_inputs as KI
 import oracle
 import parity_lib as PL
+import dsa_indexer_sparse_kpool_b300 as kp
 from dsa_indexer_sparse_kpool_b300 import COMPRESS_MEAN
 
 pytestmark = pytest.mark.gpu
@@ -159,3 +160,35 @@ def test_forward_without_new_tokens():
             assert (np.abs(o_sc[diff] - sK) <= PL.NEAR_TIE * abs(sK)).all()
         o_out, o_lse = PL.oracle_attend_on_selection(wl, qi, g_idx[qi][:ns])
         PL.check_attend(step.out[qi].float().cpu().numpy(), step.lse[qi].cpu().numpy(), o_out, o_lse)
+
+
+def test_mtp_draft_layer_reuses_target_selection():
+    """index_share_for_mtp_iteration (MAX docs, Glm5NextConfig): the MTP draft
+    layer reuses the target layer's top-k selection.  The draft layer's step is
+    then attention only: kp_sparse_mla_attend over the draft layer's own latent
+    cache and absorbed queries, with the target's pool_idx / n_sel.  Checked
+    against the oracle's attention on the draft data with that selection."""
+    lens, n_q = [300, 517, 1030], [2, 2, 1]
+    wl = KI.make(small_spec(lens, n_q, topk_tokens=256, seed=11))
+    draft = KI.make(small_spec(lens, n_q, topk_tokens=256, seed=12))  # same layout, other values
+    assert np.array_equal(wl.tok_off, draft.tok_off) and np.array_equal(wl.q_pos, draft.q_pos)
+    cfg = PL.cfg_of(wl)
+    sess, step = PL.make_gpu(wl, cfg)
+    step.run()
+    latent_d = draft.latent.to(sess.device).contiguous()
+    q_lat_d = draft.q_lat.to(sess.device).contiguous()
+    out_d = torch.empty_like(step.out)
+    lse_d = torch.empty_like(step.lse)
+    aws = torch.empty(max(256, kp.kp_attend_workspace_size(cfg, wl.NQ)), dtype=torch.uint8, device=sess.device)
+    kp.kp_sparse_mla_attend(cfg, step.seqs, step.queries, q_lat_d, latent_d, step.pool_idx, step.n_sel, out_d,
+                            lse_d, aws, d_status=sess.status)
+    torch.cuda.synchronize()
+    assert int(sess.status.item()) == 0
+    g_idx, g_ns = step.pool_idx.cpu().numpy(), step.n_sel.cpu().numpy()
+    for qi in range(wl.NQ):
+        ns = int(g_ns[qi])
+        o_out, o_lse = PL.oracle_attend_on_selection(draft, qi, g_idx[qi][:ns], int(cfg.always_select_tail))
+        PL.check_attend(out_d[qi].float().cpu().numpy(), lse_d[qi].cpu().numpy(), o_out, o_lse)
+    # the target layer's own output is untouched by the draft call
+    o_out, o_lse = PL.oracle_attend_on_selection(wl, 0, g_idx[0][:int(g_ns[0])], int(cfg.always_select_tail))
+    PL.check_attend(step.out[0].float().cpu().numpy(), step.lse[0].cpu().numpy(), o_out, o_lse)
