@@ -78,7 +78,7 @@ constexpr int kAtSoftWarps = 8;
 constexpr int kAtSoftThreads = 32 * kAtSoftWarps;
 constexpr int kAtMmaWarp = 8;
 constexpr int kAtProdWarp0 = 9;
-constexpr int kAtProdWarps = 4;                           // one per 128-column chunk
+constexpr int kAtProdWarps = 4;                           // TMA gather warps
 constexpr int kAtThreads = 416;
 static_assert(kAtThreads == 32 * (kAtSoftWarps + 1 + kAtProdWarps), "softmax, MMA and gather warps");
 constexpr int kAtPoolsPerTile = kAtTok / kKpool;          // 16 pools of 4 rows
@@ -93,12 +93,12 @@ constexpr float kAtRescaleLog2 = 8.f;                     // raise the running m
 
 // Shared memory (offsets from a 1024-aligned base).  During the tile loop:
 // Q, the tile slots, the two P buffers and a small block of per-head state and
-// barriers.  After the loop the slots receive the pushed O^T of every split;
-// the merge's small buffers (per-split maxima and sums, tail rows and logits,
-// merge weights, row-sum partials) follow it in the slots when they fit there,
-// else they sit after the barriers.
+// barriers.  After the loop the slots hold this CTA's O^T dump, which the
+// cluster's CTAs read; the merge's small buffers (tail rows and logits, merge
+// weights, row-sum partials) follow it in the slots when they fit there, else
+// they sit after the barriers.
 constexpr int kOffQ = 0;
-constexpr int kOffTile = kOffQ + kAtQBytes;               // slots; then the pushed O^T
+constexpr int kOffTile = kOffQ + kAtQBytes;               // slots; then this CTA's O^T dump
 constexpr int kOffP = kOffTile + kAtSlots * kAtTileBytes;
 constexpr int kOffMisc = kOffP + 2 * kAtPBytes;
 constexpr int kMiscRed = 0;                               // [4][64] f32 per-quadrant tile maxima
