@@ -365,25 +365,32 @@ def main():
         stage_ms = {STAGES[j]: float(np.mean([sev[i][j].elapsed_time(sev[i][j + 1]) for i in range(ks)]))
                     for j in range(4)}
 
-        # ---- end to end: pinned host inputs -> step -> host outputs, every step
-        h_in = [(t.detach().cpu().pin_memory(), t) for t in (step.q_idx, step.w, step.q_lat, step.keys, step.gates,
-                                                            step.prev_len, step.new_off, step.queries.q_seq,
-                                                            step.queries.q_pos)]
-        h_out = [(torch.empty_like(t, device="cpu").pin_memory(), t) for t in (step.out, step.lse)]
-        h2d = sum(h.numel() * h.element_size() for h, _ in h_in)
-        d2h = sum(h.numel() * h.element_size() for h, _ in h_out)
+        # ---- end to end: pinned host inputs -> step -> host outputs, every step.
+        # The step's inputs and outputs are packed into one device buffer each
+        # (Step.pack_io), so each direction is one copy from / to pinned memory,
+        # and the step is captured again on the packed tensors.
+        keep_alive = (step.q_idx, step.w, step.q_lat, step.keys, step.gates, step.prev_len, step.new_off,
+                      step.queries, step.out, step.lse)  # the headline graph's tensors
+        in_buf, out_buf = step.pack_io()
+        graph_e2e = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_e2e, stream=stream):
+            step.run()
+        h_in = torch.empty(in_buf.numel(), dtype=torch.uint8).pin_memory()
+        h_in.copy_(in_buf)
+        h_out = torch.empty(out_buf.numel(), dtype=torch.uint8).pin_memory()
+        h2d = in_buf.numel()
+        d2h = out_buf.numel()
         ke = max(1, min(args.steps, 1000))
         eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(ke)]
         for i in range(ke):
             flush_l2()
             eev[i][0].record(stream)
-            for h, d in h_in:
-                d.copy_(h, non_blocking=True)
-            graph.replay()
-            for h, d in h_out:
-                h.copy_(d, non_blocking=True)
+            in_buf.copy_(h_in, non_blocking=True)
+            graph_e2e.replay()
+            h_out.copy_(out_buf, non_blocking=True)
             eev[i][1].record(stream)
         barrier()
+        del keep_alive
         e2e_ms = float(np.mean([a.elapsed_time(b) for a, b in eev]))
         status = int(sess.status.item())
 

@@ -121,6 +121,38 @@ class Step:
     def run(self, stream=None) -> None:
         kp_dsa_forward(self.args, stream=stream)
 
+    def pack_io(self):
+        """Moves the step's per-step inputs (positions, new keys and gates,
+        queries) into one device buffer and its outputs (out, lse) into
+        another, keeping their values, and re-points the step at them, so a
+        caller moves each direction with one copy.  Returns the two buffers
+        (uint8 device tensors, 256-byte aligned pieces).  A CUDA graph captured
+        before the call still reads the old tensors."""
+        d = self.sess.device
+        ins = [self.prev_len, self.new_off, self.keys, self.gates, self.queries.q_seq, self.queries.q_pos,
+               self.q_idx, self.w, self.q_lat]
+        outs = [self.out, self.lse]
+
+        def carve(ts):
+            offs, n = [], 0
+            for t in ts:
+                offs.append(n)
+                n += (t.numel() * t.element_size() + 255) // 256 * 256
+            buf = torch.empty(max(n, 256), dtype=torch.uint8, device=d)
+            views = []
+            for t, o in zip(ts, offs):
+                v = buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+                v.copy_(t)
+                views.append(v)
+            return buf, views
+
+        in_buf, (self.prev_len, self.new_off, self.keys, self.gates, q_seq, q_pos, self.q_idx, self.w,
+                 self.q_lat) = carve(ins)
+        self.queries = Queries(q_seq, q_pos, self.queries.max_pools)
+        out_buf, (self.out, self.lse) = carve(outs)
+        self.args = self._args(self.workspace)
+        return in_buf, out_buf
+
     def launches_per_step(self) -> int:
         """Kernels one ``run`` launches: compress, score, top-k and attention;
         no queries stops after compress.  The scorer builds its own work plan
