@@ -22,8 +22,10 @@
 //   warp 0     TMA producer (one elected lane)
 //   warp 1     TMEM allocator + MMA issuer (one elected lane)
 //   warps 2-5  epilogue: TMEM -> registers -> masked scores -> global
-// Work units are (query group, 128-pool tile) pairs laid out by a tiny plan
-// kernel; each CTA takes a contiguous range of units.
+// Work units are (query group, 128-pool tile) pairs laid out by a work plan:
+// built by every CTA in shared memory for up to 1,022 queries, else by a plan
+// kernel or an extra row of the compression launch; each CTA takes a
+// contiguous range of units.
 #include <cuda.h>
 
 #include "kp_common.cuh"

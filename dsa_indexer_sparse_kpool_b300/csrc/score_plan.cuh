@@ -1,6 +1,7 @@
 // score_plan.cuh -- the work plan of the indexer scorer: query groups and the
-// 128-pool tiles each one covers.  Built by one CTA, either by the scorer's own
-// plan kernel or by an extra CTA of the compression launch in the fused step.
+// 128-pool tiles each one covers.  Built by one CTA: by every scorer CTA into
+// its own shared memory (small batches), by the scorer's plan kernel, or by an
+// extra CTA of the compression launch in the fused step.
 #pragma once
 
 #include "kp_common.cuh"
