@@ -123,7 +123,8 @@ typedef struct kp_seqs {
     const int64_t *latent_row_off;   /* [B] */
     const int64_t *pool_row_off;     /* [B] */
     int64_t latent_rows;             /* host: rows allocated in the latent cache */
-    int64_t pool_rows;               /* host: rows allocated in the pooled cache */
+    int64_t pool_rows;               /* host: rows allocated in the pooled cache (< 2^31:
+                                        TMA row coordinates are signed 32-bit) */
 } kp_seqs;
 
 /* The query tokens of this step, flattened over sequences.  Queries of one

@@ -78,6 +78,10 @@ def test_score_rejects_small_workspace_and_stride(L):
     assert L.kp_indexer_score(ctypes.byref(a), None) == 6
     a.q = kp.kp_queries(4, 0x1000, 0x1000, kp.MAX_SCORE_POOLS + 1)
     assert L.kp_indexer_score(ctypes.byref(a), None) == 2
+    a.q = kp.kp_queries(4, 0x1000, 0x1000, 64)
+    a.workspace_bytes = 1 << 20
+    a.seqs = kp.kp_seqs(1, 0x1000, 0x1000, 0x1000, 100, 1 << 31)   # pooled rows beyond TMA's int32 rows
+    assert L.kp_indexer_score(ctypes.byref(a), None) == 1
 
 
 def test_compress_rejects_inconsistent_sizes(L):
