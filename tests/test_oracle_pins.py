@@ -376,3 +376,61 @@ def test_kpool_one_reduces_to_per_token_selection():
     pooled, _ = oracle.kpool_compress(keys, rand_bf16((L, dim)), rand_bf16((1, dim), 0.1), kpool=1)
     assert (pooled == keys).all()
     assert oracle.token_set(39, 1, np.array([1, 5], np.int32), 1).tolist() == [1, 5]
+
+
+# ------------------------------------------------------------------ whole path
+
+
+def _tiny_with_budget(k_pools):
+    spec = KI.named("tiny")
+    spec.topk_tokens = 4 * k_pools
+    return KI.make(spec)
+
+
+def test_whole_path_is_causal_per_query():
+    # A query at position t sees only tokens 0..t: cutting every per-token array
+    # (keys, gates, latent) after t leaves its selection, output and lse
+    # unchanged.  A wrong pool count, tail bound or row offset breaks this.
+    wl = _tiny_with_budget(16)
+    keys, gates, ape, lat = KI.bits(wl.keys), KI.bits(wl.gates), KI.bits(wl.ape), KI.bits(wl.latent)
+    pooled, _ = oracle.kpool_compress(keys, gates, ape, 4)
+    z = np.zeros(1, np.int64)
+    full = oracle.dsa_queries(wl.q_seq, wl.q_pos, z, z, 4, 16, 1, KI.bits(wl.q_idx), wl.w.numpy(), pooled,
+                              KI.bits(wl.q_lat), lat, wl.spec.sm_scale)
+    for qi, t in enumerate(wl.q_pos):
+        n = int(t) + 1
+        pooled_t, _ = oracle.kpool_compress(keys[:n], gates[:n], ape, 4)
+        one = oracle.dsa_queries(np.zeros(1, np.int32), np.array([t], np.int32), z, z, 4, 16, 1,
+                                 KI.bits(wl.q_idx)[qi:qi + 1], wl.w.numpy()[qi:qi + 1], pooled_t,
+                                 KI.bits(wl.q_lat)[qi:qi + 1], lat[:n], wl.spec.sm_scale)
+        assert one["n_sel"][0] == full["n_sel"][qi]
+        assert np.array_equal(one["sel"][0], full["sel"][qi])
+        assert np.array_equal(one["out"][0], full["out"][qi])
+        assert np.array_equal(one["lse"][0], full["lse"][qi])
+
+
+def test_ragged_batch_equals_sequences_run_singly():
+    # Two sequences of different lengths packed back to back (row offsets)
+    # give each query the same result as its sequence alone.
+    wl = KI.make(KI.Spec("two", [130, 77], [2, 3], topk_tokens=64, seed=21))
+    keys, gates, ape, lat = KI.bits(wl.keys), KI.bits(wl.gates), KI.bits(wl.ape), KI.bits(wl.latent)
+    pooled_rows, pool_off = [], []
+    for b in range(2):
+        lo, hi = int(wl.tok_off[b]), int(wl.tok_off[b]) + int(wl.lens[b])
+        p, _ = oracle.kpool_compress(keys[lo:hi], gates[lo:hi], ape, 4)
+        pool_off.append(sum(r.shape[0] for r in pooled_rows))
+        pooled_rows.append(p)
+    pooled = np.concatenate(pooled_rows)
+    both = oracle.dsa_queries(wl.q_seq, wl.q_pos, np.array(pool_off, np.int64), wl.tok_off.astype(np.int64), 4,
+                              16, 1, KI.bits(wl.q_idx), wl.w.numpy(), pooled, KI.bits(wl.q_lat), lat,
+                              wl.spec.sm_scale)
+    z = np.zeros(1, np.int64)
+    for qi in range(wl.NQ):
+        b = int(wl.q_seq[qi])
+        lo, hi = int(wl.tok_off[b]), int(wl.tok_off[b]) + int(wl.lens[b])
+        one = oracle.dsa_queries(np.zeros(1, np.int32), wl.q_pos[qi:qi + 1], z, z, 4, 16, 1,
+                                 KI.bits(wl.q_idx)[qi:qi + 1], wl.w.numpy()[qi:qi + 1], pooled_rows[b],
+                                 KI.bits(wl.q_lat)[qi:qi + 1], lat[lo:hi], wl.spec.sm_scale)
+        assert np.array_equal(one["sel"][0], both["sel"][qi])
+        assert np.array_equal(one["out"][0], both["out"][qi])
+        assert np.array_equal(one["lse"][0], both["lse"][qi])
