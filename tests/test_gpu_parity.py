@@ -192,3 +192,41 @@ def test_mtp_draft_layer_reuses_target_selection():
     # the target layer's own output is untouched by the draft call
     o_out, o_lse = PL.oracle_attend_on_selection(wl, 0, g_idx[0][:int(g_ns[0])], int(cfg.always_select_tail))
     PL.check_attend(step.out[0].float().cpu().numpy(), step.lse[0].cpu().numpy(), o_out, o_lse)
+
+
+def test_two_steps_with_the_tail_ring_equal_one_step():
+    """Appending a chunk in one step or in two steps (the tail ring of the
+    incomplete pool carried between them) gives the same pooled cache and the
+    same outputs for the final step's queries, bit for bit."""
+    from dsa_indexer_sparse_kpool_b300.session import build_session, build_step
+    lens, n_q = [203, 346], [13, 11]          # 13 and 11 new tokens, split 6 + 7 and 5 + 6
+    wl = KI.make(small_spec(lens, n_q, topk_tokens=64, seed=31))
+    cfg = PL.cfg_of(wl)
+    prev = wl.prev_len.tolist()
+    mid = [int(wl.prev_len[0]) + 6, int(wl.prev_len[1]) + 5]
+    args = (wl.lens.tolist(), wl.tok_off.tolist(), wl.pool_off.tolist(), wl.pool_rows, wl.latent, wl.keys,
+            wl.gates, wl.ape)
+
+    def session():
+        return build_session(cfg, args[0], prev, args[1], args[2], args[3], args[4], args[5], args[6], args[7])
+
+    # one step: all new tokens, queries = the last two positions of each sequence
+    last = [qi for qi in range(wl.NQ) if int(wl.q_pos[qi]) >= int(wl.lens[int(wl.q_seq[qi])]) - 2]
+    qs = lambda sel: (wl.q_seq[sel], wl.q_pos[sel], wl.q_idx[sel], wl.w[sel], wl.q_lat[sel])
+    sA = session()
+    stA = build_step(sA, args[0], prev, args[1], wl.keys, wl.gates, *qs(last))
+    stA.run()
+    # two steps: first up to `mid` (queries at the first new position of each sequence), then the rest
+    sB = session()
+    first = [qi for qi in range(wl.NQ) if int(wl.q_pos[qi]) == int(wl.prev_len[int(wl.q_seq[qi])])]
+    st1 = build_step(sB, mid, prev, args[1], wl.keys, wl.gates, *qs(first))
+    st1.run()
+    st2 = build_step(sB, args[0], mid, args[1], wl.keys, wl.gates, *qs(last))
+    st2.run()
+    torch.cuda.synchronize()
+    assert int(sA.status.item()) == 0 and int(sB.status.item()) == 0
+    assert torch.equal(sA.pooled, sB.pooled)
+    assert torch.equal(stA.pool_idx, st2.pool_idx) and torch.equal(stA.n_sel, st2.n_sel)
+    assert torch.equal(stA.out, st2.out) and torch.equal(stA.lse, st2.lse)
+    # and the one-step path matches the oracle
+    PL.check_pooled(sA, wl)
