@@ -19,7 +19,6 @@ import hashlib
 import json
 import os
 import statistics
-import subprocess
 import sys
 import time
 
@@ -120,9 +119,10 @@ def measured_peaks():
     return 6400.0, 1800.0, 1400.0, "fallback"
 
 
-def kernel_traffic(stage: str):
-    """ncu DRAM bytes per launch of this stage's kernel (profiles/ncu_traffic.txt),
-    if that capture was taken on the current kernel source (else None)."""
+def kernel_traffic(stage: str, workload_name: str):
+    """ncu DRAM bytes per launch of this stage's kernel on this workload
+    (profiles/ncu_traffic.txt), if that capture was taken on the current kernel
+    source; else None."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
     if not os.path.exists(p):
         return None
@@ -130,7 +130,7 @@ def kernel_traffic(stage: str):
     sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     for line in open(p):
         f = line.split()
-        if len(f) >= 5 and not line.startswith("#") and f[0] == stage and f[4] == sha:
+        if len(f) >= 5 and not line.startswith("#") and f[0] == stage and f[2] == workload_name and f[4] == sha:
             return int(f[3])
     return None
 
@@ -138,55 +138,84 @@ def kernel_traffic(stage: str):
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
-              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-              "clocks_event_reasons.sw_power_cap")
+    """SM clock and throttle reasons sampled through NVML every millisecond in
+    a background thread (reads only; no setting of the GPU is changed), so
+    that even a timed region of a few milliseconds holds samples.  Each sample
+    is stamped with time.monotonic(); `window(t0, t1)` summarises the samples
+    inside [t0, t1]."""
+    REASONS = (("hw_slowdown", 0x8), ("sw_thermal_slowdown", 0x20), ("hw_thermal_slowdown", 0x40),
+               ("hw_power_brake_slowdown", 0x80), ("sw_power_cap", 0x4))
 
     def __init__(self, device_index: int):
-        self.proc = None
-        self.path = None
+        import threading
+        self.samples = []
+        self.error = None
+        self._stop = threading.Event()
+        self._thread = threading.Thread(target=self._run, args=(device_index,), daemon=True)
+
+    def _run(self, device_index):
         try:
+            import ctypes
+            nv = ctypes.CDLL("libnvidia-ml.so.1")        # the driver's NVML, read-only queries
+
+            def ok(r, what):
+                if r != 0:
+                    raise RuntimeError(f"{what} returned {r}")
+            ok(nv.nvmlInit_v2(), "nvmlInit_v2")
             uuid = str(torch.cuda.get_device_properties(device_index).uuid)
-            sel = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
-        except Exception:
-            sel = []
-        self.cmd = ["nvidia-smi", *sel, "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits", "-lms", "20"]
+            uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            h = ctypes.c_void_p()
+            ok(nv.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h)), "nvmlDeviceGetHandleByUUID")
+            clk, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+            sm_clock = 1                                   # NVML_CLOCK_SM
+            ok(nv.nvmlDeviceGetMaxClockInfo(h, sm_clock, ctypes.byref(mx)), "nvmlDeviceGetMaxClockInfo")
+            reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            while not self._stop.is_set():
+                ok(nv.nvmlDeviceGetClockInfo(h, sm_clock, ctypes.byref(clk)), "nvmlDeviceGetClockInfo")
+                ok(reasons(h, ctypes.byref(rs)), "clock event reasons")
+                self.samples.append((time.monotonic(), clk.value, mx.value, rs.value))
+                time.sleep(0.001)
+            nv.nvmlShutdown()
+        except Exception as e:  # no NVML: report that, never guess
+            self.error = f"{type(e).__name__}: {e}"
 
     def start(self):
-        try:
-            self.out = open(os.devnull, "w")
-            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except Exception:
-            self.proc = None
+        self._thread.start()
+        t0 = time.monotonic()
+        while not self.samples and self.error is None and time.monotonic() - t0 < 5.0:
+            time.sleep(0.005)
 
     def stop(self):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        self.proc.terminate()
-        try:
-            text, _ = self.proc.communicate(timeout=5)
-        except Exception:
-            self.proc.kill()
-            text = ""
-        sm, mx, reasons = [], [], set()
-        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for line in text.strip().splitlines():
-            parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 7:
-                continue
-            try:
-                sm.append(float(parts[0]))
-                mx.append(float(parts[1]))
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[3:7]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        self._stop.set()
+        self._thread.join(timeout=5)
+
+    def window(self, t0: float, t1: float):
+        if self.error is not None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml unavailable: " + self.error], "samples": 0}
+        sel = [x for x in self.samples if t0 <= x[0] <= t1]
+        reasons = set()
+        for _, _, _, rs in sel:
+            for name, bit in self.REASONS:
+                if rs & bit:
+                    reasons.add(name)
+        sm = [x[1] for x in sel]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(x[2] for x in sel) if sel else None,
+                "sm_mhz_min": min(sm) if sm else None, "reasons": sorted(reasons), "samples": len(sel),
+                "source": "NVML, 1 ms period"}
 
 
 # ------------------------------------------------------------------ CPU oracle baseline
+
+def cpu_model() -> str:
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
 
 class OracleStep:
     """The fp64 oracle doing this workload's step for a batch of queries:
@@ -269,6 +298,7 @@ def run_reference(args, rank, world):
             "dtype": "f64", "data": "synthetic",
             "config": {"workload": DESCR[args.workload], "queries_per_step": min(threads, wl.NQ)},
             "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                             "cpu_model": cpu_model(),
                              "sample": f"each step = {min(threads, wl.NQ)} whole queries of the workload (compress "
                                        f"of the step's new pools, scores, top-k, attention), OpenMP over queries; "
                                        f"steps capped so the run ends in about 2 minutes"},
@@ -335,20 +365,21 @@ def main():
                 dist.barrier()
 
         # ---- headline: K replays of the whole step
+        sampler = ClockSampler(local)
+        sampler.start()
         for _ in range(args.warmup):
             flush_l2()
             graph.replay()
         barrier()
-        sampler = ClockSampler(local)
-        sampler.start()
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        th0 = time.monotonic()
         for i in range(args.steps):
             flush_l2()
             ev[i][0].record(stream)
             graph.replay()
             ev[i][1].record(stream)
         barrier()
-        clocks = sampler.stop()
+        th1 = time.monotonic()
         step_ms = [a.elapsed_time(b) for a, b in ev]
         total_ms = float(sum(step_ms))
 
@@ -390,9 +421,16 @@ def main():
             h_out.copy_(out_buf, non_blocking=True)
             eev[i][1].record(stream)
         barrier()
+        t_all1 = time.monotonic()
+        sampler.stop()
         del keep_alive
         e2e_ms = float(np.mean([a.elapsed_time(b) for a, b in eev]))
         status = int(sess.status.item())
+        clocks = sampler.window(th0, th1)
+        clocks["window"] = "headline timed region"
+        if clocks["samples"] < 3:      # a very short headline region: every timed phase
+            clocks = sampler.window(th0, t_all1)
+            clocks["window"] = "all timed phases (headline, per-stage, end-to-end)"
 
     # ---- aggregate over ranks (max of the ranks' times)
     total_ms, e2e_ms = replicas.max_over_ranks([total_ms, e2e_ms], device=dev)
@@ -405,31 +443,45 @@ def main():
         alg, n_tok = algorithmic_bytes(wl)
         flops = algorithmic_flops(wl)
         hbm, bf16, bf16_sus, src = measured_peaks()
-        dominant = max(("indexer_score", "sparse_mla_attend", "topk_select", "kpool_compress"),
-                       key=lambda s: stage_ms[s])
-        t_dom = stage_ms[dominant] * 1e-3
-        # the stage's bound: whichever of HBM bytes and tensor flops takes longer at peak
-        stage_loop_s = t_dom * ks
-        tpeak = bf16 if stage_loop_s < 1.0 else bf16_sus
-        if flops[dominant] / (tpeak * 1e12) > alg[dominant] / (hbm * 1e9):
-            ach = flops[dominant] / t_dom / 1e12
-            roof = {"bound": "tensor", "kernel": dominant, "achieved": ach, "peak": tpeak, "unit": "TFLOP/s",
-                    "frac": ach / tpeak, "peak_source": src + (" bf16 burst" if tpeak == bf16 else " bf16 sustained"),
-                    "traffic": kernel_traffic(dominant), "algorithmic_flops": flops[dominant],
-                    "algorithmic_bytes": alg[dominant], "avg_launch_ms": stage_ms[dominant]}
-        else:
-            ach = alg[dominant] / t_dom / 1e9
-            roof = {"bound": "hbm", "kernel": dominant, "achieved": ach, "peak": hbm, "unit": "GB/s",
-                    "frac": ach / hbm, "peak_source": src + " HBM copy", "traffic": kernel_traffic(dominant),
-                    "algorithmic_bytes": alg[dominant], "avg_launch_ms": stage_ms[dominant]}
+        # Every stage against its bound: tensor when its flops take longer at
+        # the bf16 peak than its bytes at the HBM peak, else HBM; stages with
+        # neither (top-k: the score matrix is an intermediate) are latency-bound.
+        # The per-stage graphs run ks launches back to back, under a second: the
+        # burst bf16 peak applies.
+        stage_roof = {}
+        for st in STAGES:
+            t = stage_ms[st] * 1e-3
+            tpeak = bf16 if t * ks < 1.0 else bf16_sus
+            tr = kernel_traffic(st, args.workload)
+            if flops[st] > 0 and flops[st] / (tpeak * 1e12) > alg[st] / (hbm * 1e9):
+                ach = flops[st] / t / 1e12
+                stage_roof[st] = {"bound": "tensor", "achieved": ach, "peak": tpeak, "unit": "TFLOP/s",
+                                  "frac": ach / tpeak,
+                                  "peak_source": src + (" bf16 burst" if tpeak == bf16 else " bf16 sustained"),
+                                  "traffic": tr, "algorithmic_flops": flops[st], "algorithmic_bytes": alg[st],
+                                  "avg_launch_ms": stage_ms[st]}
+            elif alg[st] > 0:
+                ach = alg[st] / t / 1e9
+                stage_roof[st] = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+                                  "peak_source": src + " HBM copy", "traffic": tr, "algorithmic_bytes": alg[st],
+                                  "avg_launch_ms": stage_ms[st]}
+            else:
+                stage_roof[st] = {"bound": "latency", "achieved": None, "peak": None, "unit": None, "frac": None,
+                                  "traffic": tr, "algorithmic_bytes": 0, "avg_launch_ms": stage_ms[st]}
+        dominant = max(STAGES, key=lambda st: stage_ms[st])
+        roof = dict(stage_roof[dominant], kernel=dominant)
         step_bytes = sum(alg.values())
         cpu = None
         if not args.no_cpu_baseline:
             threads = os.cpu_count() or 1
             rate, done, wall = OracleStep(wl, threads).rate(args.cpu_seconds)
+            rate1, done1, wall1 = OracleStep(wl, 1).rate(max(1.0, args.cpu_seconds / 3))
             cpu = {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                   "cpu_model": cpu_model(),
                    "sample": f"{done} whole queries of this workload in {wall:.1f} s (compress of the step's new "
-                             f"pools, scores over all visible pools, top-k, attention), OpenMP over queries"}
+                             f"pools, scores over all visible pools, top-k, attention), OpenMP over queries",
+                   "single_thread": {"value": rate1, "unit": "tokens/s", "cores": 1,
+                                     "sample": f"{done1} whole queries in {wall1:.1f} s on one thread"}}
         line = {
             "metric": METRIC[args.workload], "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step, "higher_is_better": True,
@@ -439,6 +491,7 @@ def main():
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                        "l2": "flushed between timed steps (256 MB read)", "timing": "CUDA-graph replay, events"},
             "roofline": roof,
+            "stage_roofline": stage_roof,
             "step_roofline": {"algorithmic_bytes": step_bytes, "achieved_GBps": step_bytes / (t_step * 1e-3) / 1e9,
                               "frac": step_bytes / (t_step * 1e-3) / 1e9 / hbm},
             "stage_ms": stage_ms,

@@ -22,6 +22,7 @@ LIB_PATH = os.path.join(_PKG, "libkpool_dsa.so")
 INDEX_HEADS, INDEX_DIM, MLA_HEADS, LATENT_DIM, NOPE_DIM, KPOOL = 32, 128, 64, 576, 512, 4
 MAX_TOPK_POOLS, MAX_SCORE_POOLS, NOALLOC_MAX_QUERIES = 1024, 262144, 8192
 COMPRESS_LEARNED, COMPRESS_MEAN = 0, 1
+DEBUG_STALL_FIRST_WAIT = 1
 
 STATUS = {0: "KP_OK", 1: "KP_ERR_INVALID_ARG", 2: "KP_ERR_UNSUPPORTED", 3: "KP_ERR_CUDA",
           4: "KP_ERR_DEVICE_TIMEOUT", 5: "KP_ERR_DEVICE_BOUNDS", 6: "KP_ERR_WORKSPACE"}
@@ -31,7 +32,8 @@ _i32, _i64, _f32, _vp, _sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, cty
 
 class kp_config(ctypes.Structure):
     _fields_ = [("kpool", _i32), ("topk_tokens", _i32), ("compress_mode", _i32),
-                ("always_select_tail", _i32), ("sm_scale", _f32)]
+                ("always_select_tail", _i32), ("sm_scale", _f32), ("wait_limit_us", _i32),
+                ("debug_flags", _i32)]
 
 
 class kp_seqs(ctypes.Structure):
@@ -152,10 +154,12 @@ class Config:
     compress_mode: int = COMPRESS_LEARNED
     always_select_tail: bool = True
     sm_scale: float = 1.0 / 16.0
+    wait_limit_us: int = 0          # 0: each device-side wait gives up after 1 s
+    debug_flags: int = 0            # DEBUG_* bits (failure-path tests only)
 
     def c(self) -> kp_config:
         return kp_config(self.kpool, self.topk_tokens, self.compress_mode, int(self.always_select_tail),
-                         float(self.sm_scale))
+                         float(self.sm_scale), int(self.wait_limit_us), int(self.debug_flags))
 
     @property
     def k_pools(self) -> int:

@@ -24,6 +24,8 @@ kp_status check_config(const kp_config &c) {
         return KP_ERR_INVALID_ARG;
     if (c.always_select_tail != 0 && c.always_select_tail != 1) return KP_ERR_INVALID_ARG;
     if (!std::isfinite(c.sm_scale)) return KP_ERR_INVALID_ARG;
+    if (c.wait_limit_us < 0) return KP_ERR_INVALID_ARG;
+    if ((c.debug_flags & ~KP_DEBUG_STALL_FIRST_WAIT) != 0) return KP_ERR_INVALID_ARG;
     return KP_OK;
 }
 
@@ -37,7 +39,7 @@ kp_status check_queries(const kp_queries &q) {
 }
 
 kp_status check_seqs(const kp_seqs &s, bool latent, bool pooled) {
-    if (s.num_seqs < 1 || s.num_seqs > 65535) return KP_ERR_INVALID_ARG;
+    if (s.num_seqs < 1 || s.num_seqs > 65535 || !s.seq_len) return KP_ERR_INVALID_ARG;
     if (latent && (!s.latent_row_off || s.latent_rows <= 0 || s.latent_rows >= (int64_t(1) << 40)))
         return KP_ERR_INVALID_ARG;
     if (pooled && (!s.pool_row_off || s.pool_rows <= 0 || s.pool_rows >= (int64_t(1) << 31)))
@@ -385,7 +387,7 @@ kp_status kp_read_device_status(const int32_t *d_status, kp_stream_t stream) {
     return static_cast<kp_status>(v);
 }
 
-int kp_version(void) { return 100; }
+int kp_version(void) { return 20000; }
 
 }  // extern "C"
 

@@ -56,6 +56,8 @@
 //              8 TMA boxes per warp per chunk (TMA issue is serial within a
 //              warp, so four warps issue at four times the rate of one)
 //   all        cluster merge and output
+#include <atomic>
+
 #include "kp_common.cuh"
 #include "kp_internal.h"
 
@@ -106,7 +108,7 @@ constexpr int kMiscMUsed = kMiscRed + 4 * 64 * 4;         // [64] f32 running ma
 constexpr int kMiscFac = kMiscMUsed + 64 * 4;             // [64] f32 rescale factors of this tile
 constexpr int kMiscLSum = kMiscFac + 64 * 4;              // [64] f32 row sums
 constexpr int kMiscBars = kMiscLSum + 64 * 4;             // mbarriers
-constexpr int kNumBars = 4 * kAtSlots * 2 + 8;
+constexpr int kNumBars = 4 * kAtSlots * 2 + 9;
 constexpr int kMiscTmem = kMiscBars + kNumBars * 8;
 constexpr int kMiscAbort = kMiscTmem + 4;
 constexpr int kMiscCore = (kMiscAbort + 12 + 15) / 16 * 16;
@@ -133,13 +135,15 @@ constexpr int kBarP = kBarS + 2;                   // [2] P buffer written, O^T 
 constexpr int kBarO = kBarP + 2;                   // every MMA of the CTA done (commit)
 constexpr int kBarDrain = kBarO + 1;               // teardown after an abort
 constexpr int kBarPV = kBarDrain + 1;              // P.V of a tile done (commit): O^T is stable
-static_assert(kBarPV + 1 == kNumBars, "barrier count");
+constexpr int kBarNever = kBarPV + 1;              // nothing arrives (failure-path tests)
+static_assert(kBarNever + 1 == kNumBars, "barrier count");
 
 struct AttendParams {
     const uint16_t *latent;
     int64_t latent_rows;
     const int32_t *q_seq;
     const int32_t *q_pos;
+    const int32_t *seq_len;
     const int64_t *latent_row_off;
     int num_seqs;
     const int32_t *pool_idx;
@@ -151,6 +155,8 @@ struct AttendParams {
     float *lse;
     int splits;
     int32_t *status;
+    unsigned long long wait_ns;  // limit of one pipeline wait
+    int stall;                   // KP_DEBUG_STALL_FIRST_WAIT: the MMA warp's first wait never completes
 };
 
 __device__ __forceinline__ void named_bar(int id, int count) {
@@ -241,6 +247,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         mbar_init(bar(kBarP + 1), kAtSoftThreads);
         mbar_init(bar(kBarO), 1);
         mbar_init(bar(kBarDrain), 1);
+        mbar_init(bar(kBarNever), 1);
         fence_mbar_init();
         *abort_s = 0;
         tma_prefetch_desc(&tm_q);
@@ -258,6 +265,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     const int t = P.q_pos[q];
     bool qvalid = b >= 0 && b < P.num_seqs && t >= 0;
     int64_t base_row = qvalid ? P.latent_row_off[b] : 0;
+    if (qvalid && t >= P.seq_len[b]) qvalid = false;   // a query sits inside its sequence
     if (qvalid && (base_row < 0 || base_row + t >= P.latent_rows)) qvalid = false;
     if (!qvalid && tid == 0) set_status(P.status, KP_ERR_DEVICE_BOUNDS);
     const int nf = qvalid ? (t + 1) / kKpool : 0;
@@ -297,7 +305,8 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         // The thread polls with test_wait: a suspended thread would wake late
         // with the pipe idle.
         if (lane == 0) {
-            bool ok = nt == 0 || mbar_wait(bar(kBarQ), 0, abort_flag, P.status);
+            bool ok = !P.stall || mbar_wait(bar(kBarNever), 0, abort_flag, P.status, P.wait_ns);
+            ok = ok && (nt == 0 || mbar_wait(bar(kBarQ), 0, abort_flag, P.status, P.wait_ns));
             const uint32_t idesc_s = idesc_bf16_f32(64, kMlaHeads);                 // M = 64
             const uint32_t idesc_pv = idesc_bf16_f32(128, kMlaHeads, true, true);   // M = 128 columns
             // Descriptors are built once; a step along K or to another block adds
@@ -327,7 +336,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
             };
             for (int t = 0; ok && t < nt; ++t) {
                 if (pv_next < t - 1) {  // P.V(t - 2): frees the S^T buffer S(t) writes
-                    ok = mbar_spin(bar(kBarP + (pv_next & 1)), (pv_next >> 1) & 1, abort_flag, P.status);
+                    ok = mbar_spin(bar(kBarP + (pv_next & 1)), (pv_next >> 1) & 1, abort_flag, P.status, P.wait_ns);
                     if (!ok) break;
                     issue_pv();
                 }
@@ -341,7 +350,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
                             if (pv_next < t && mbar_test(bar(kBarP + (pv_next & 1)), (pv_next >> 1) & 1)) issue_pv();
                             if (mbar_test(fb, fpar)) break;
                             if ((it & 255u) == 0 &&
-                                (*abort_flag || globaltimer_ns() - t0 > KP_WAIT_NS)) {
+                                (*abort_flag || globaltimer_ns() - t0 > P.wait_ns)) {
                                 set_status(P.status, KP_ERR_DEVICE_TIMEOUT);
                                 *abort_flag = 1;
                                 ok = false;
@@ -363,7 +372,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
                 tc_commit(bar(kBarS + sbuf));
             }
             while (ok && pv_next < nt) {  // the last tiles' P.V
-                ok = mbar_spin(bar(kBarP + (pv_next & 1)), (pv_next >> 1) & 1, abort_flag, P.status);
+                ok = mbar_spin(bar(kBarP + (pv_next & 1)), (pv_next >> 1) & 1, abort_flag, P.status, P.wait_ns);
                 if (ok) issue_pv();
             }
             if (ok) {
@@ -425,7 +434,8 @@ __global__ void __launch_bounds__(kAtThreads, 1)
                 for (int cc = 0; cc < kAtChunks; ++cc) {
                     if (jj >= kAtSlots) {  // P.V of the slot's previous tile has read this chunk
                         ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarFree + u * kAtChunks + cc),
-                                                              ((jj / kAtSlots) - 1) & 1, abort_flag, P.status));
+                                                              ((jj / kAtSlots) - 1) & 1, abort_flag, P.status,
+                                                              P.wait_ns));
                         if (!ok) break;
                     }
                     const uint32_t fb = bar(kBarFull + u * kAtChunks + cc);
@@ -467,7 +477,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         bool ok = true;
         for (int jj = 0; jj < nt; ++jj) {
             ok = named_bar_all(1, kAtSoftThreads,
-                               mbar_wait(bar(kBarS + (jj & 1)), (jj >> 1) & 1, abort_flag, P.status));
+                               mbar_wait(bar(kBarS + (jj & 1)), (jj >> 1) & 1, abort_flag, P.status, P.wait_ns));
             if (!ok) break;
             tc_fence_after();
             uint32_t r[16];
@@ -537,7 +547,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
             if (rescale) {
                 // O^T must hold P.V of the previous tile before it is rescaled; P.V of
                 // this tile waits for our arrival below.
-                mbar_wait(bar(kBarPV), (jj - 1) & 1, abort_flag, P.status);
+                mbar_wait(bar(kBarPV), (jj - 1) & 1, abort_flag, P.status, P.wait_ns);
                 tc_fence_after();
                 for (int c = 0; c < 2 * kAtChunks; ++c) {  // 16 heads at a time
                     uint32_t o[16];
@@ -555,7 +565,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
             tc_fence_before();
             mbar_arrive(bar(kBarP + (jj & 1)));
         }
-        if (ok) ok = named_bar_all(1, kAtSoftThreads, mbar_wait(bar(kBarO), 0, abort_flag, P.status));
+        if (ok) ok = named_bar_all(1, kAtSoftThreads, mbar_wait(bar(kBarO), 0, abort_flag, P.status, P.wait_ns));
         if (ok) {
             tc_fence_after();
             // Row sums: add the 8 threads that share my heads (fixed order), then
@@ -611,7 +621,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
                 *reinterpret_cast<const uint4 *>(P.latent + row * kLatentDim + piece * 8);
         }
         // Q has landed (the tail logits read it; nothing may be in flight at exit).
-        const bool have_q = mbar_wait(bar(kBarQ), 0, abort_flag, P.status);
+        const bool have_q = mbar_wait(bar(kBarQ), 0, abort_flag, P.status, P.wait_ns);
         named_bar(2, kTailThreads);
         if (have_q) {  // tail logits of this CTA's heads: one warp per (head, tail token)
             for (int pr = warp - kAtSoftWarps; pr < nh * n_tail; pr += kTailThreads / 32) {
@@ -727,12 +737,17 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     }
 }
 
-// Largest cluster size whose clusters, one CTA per SM, all fit at once (cached per device).
+// Largest cluster size whose clusters, one CTA per SM, all fit at once
+// (cached per device; host threads that race here compute the same value, and
+// the cache entries are atomics, so the race is benign).
+std::atomic<int> g_active_clusters[64][kAtMaxSplits + 1];
+std::atomic<int> g_smem_configured[64];
+
 int max_active_clusters(int cluster) {
-    static int cache[64][kAtMaxSplits + 1] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    if (cache[dev][cluster] != 0) return cache[dev][cluster];
+    const int cached = g_active_clusters[dev][cluster].load(std::memory_order_relaxed);
+    if (cached != 0) return cached;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(cluster * 64);
     cfg.blockDim = dim3(kAtThreads);
@@ -749,22 +764,21 @@ int max_active_clusters(int cluster) {
         cudaGetLastError();
         n = 0;
     }
-    cache[dev][cluster] = n > 0 ? n : -1;
+    g_active_clusters[dev][cluster].store(n > 0 ? n : -1, std::memory_order_relaxed);
     return n;
 }
 
 bool attend_smem_configured() {
-    static int done[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
-    if (done[dev]) return true;
+    if (g_smem_configured[dev].load(std::memory_order_relaxed)) return true;
     cudaError_t e = cudaFuncSetAttribute(sparse_mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kAtSmemBytes);
     if (e != cudaSuccess) {
         record_cuda_error("cudaFuncSetAttribute(sparse_mla_tc_kernel)", e);
         return false;
     }
-    done[dev] = 1;
+    g_smem_configured[dev].store(1, std::memory_order_relaxed);
     return true;
 }
 
@@ -811,6 +825,7 @@ kp_status launch_attend(const kp_attend_args &a, cudaStream_t s) {
     P.latent_rows = a.seqs.latent_rows;
     P.q_seq = a.q.q_seq;
     P.q_pos = a.q.q_pos;
+    P.seq_len = a.seqs.seq_len;
     P.latent_row_off = a.seqs.latent_row_off;
     P.num_seqs = a.seqs.num_seqs;
     P.pool_idx = a.pool_idx;
@@ -822,6 +837,8 @@ kp_status launch_attend(const kp_attend_args &a, cudaStream_t s) {
     P.lse = a.lse;
     P.splits = splits;
     P.status = a.d_status;
+    P.wait_ns = wait_limit_ns(a.cfg.wait_limit_us);
+    P.stall = (a.cfg.debug_flags & KP_DEBUG_STALL_FIRST_WAIT) ? 1 : 0;
 
     return launch_kernel("sparse_mla_tc_kernel", sparse_mla_tc_kernel,
                          LaunchCfg(dim3(static_cast<unsigned>(nq) * splits), dim3(kAtThreads), kAtSmemBytes, s, splits),

@@ -56,8 +56,8 @@ __global__ void __launch_bounds__(kCompressWarps * 32)
     pdl_wait_then_release();
     if (plan.plan && blockIdx.y == gridDim.y - 1) {  // the extra row of CTAs: the scorer's plan
         if (blockIdx.x == 0)
-            build_score_plan(plan.nq, plan.num_seqs, plan.q_seq, plan.q_pos, plan.max_tiles, plan.plan,
-                             plan.status, scratch);
+            build_score_plan(plan.nq, plan.num_seqs, plan.q_seq, plan.q_pos, plan.seq_len, plan.max_tiles,
+                             plan.plan, plan.status, scratch);
         return;
     }
     const int b = blockIdx.y;

@@ -1,9 +1,8 @@
 // kp_common.cuh -- device helpers shared by the KPool DSA kernels (sm_103a).
 //
 // Thin inline-PTX wrappers for the Blackwell data movers and tensor cores
-// (mbarrier, TMA tensor copies, tcgen05 MMA / TMEM), the Ampere-style
-// cp.async / ldmatrix / mma.sync used by the attention kernel, a block-wide
-// scan, and the status word.  Every wait on an mbarrier is bounded in time:
+// (mbarrier, TMA tensor copies, tcgen05 MMA / TMEM, distributed shared
+// memory), a block-wide scan, and the status word.  Every wait on an mbarrier is bounded in time:
 // after KP_WAIT_NS it records KP_ERR_DEVICE_TIMEOUT and returns false so the
 // caller can unwind instead of spinning forever.
 #pragma once
@@ -24,8 +23,15 @@ constexpr int kLatentDim = KP_LATENT_DIM;
 constexpr int kNopeDim = KP_NOPE_DIM;
 constexpr int kKpool = KP_KPOOL;
 
-// A single wait longer than this (1 s) means something is broken.
+// A single wait longer than this (1 s) means something is broken.  Callers
+// can set a shorter limit per call (kp_config.wait_limit_us); the waits that
+// drain in-flight copies and MMAs before teardown always use this one.
 constexpr unsigned long long KP_WAIT_NS = 1000000000ull;
+
+// Limit of one wait for a call: wait_limit_us, or KP_WAIT_NS when it is 0.
+__host__ __device__ inline unsigned long long wait_limit_ns(int32_t wait_limit_us) {
+    return wait_limit_us > 0 ? static_cast<unsigned long long>(wait_limit_us) * 1000ull : KP_WAIT_NS;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -90,17 +96,17 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 // Waits for the phase of parity `parity` to complete.  Returns false (and
-// records a timeout in *status) after KP_WAIT_NS, or early when *abort is
-// set by another thread of the CTA.
+// records a timeout in *status) after limit_ns, or early when *abort is set
+// by another thread of the CTA.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
-                                          int32_t *status) {
+                                          int32_t *status, unsigned long long limit_ns = KP_WAIT_NS) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 63u) == 0) {
             if (abort && *abort) return false;
-            if (globaltimer_ns() - t0 > KP_WAIT_NS) {
+            if (globaltimer_ns() - t0 > limit_ns) {
                 set_status(status, KP_ERR_DEVICE_TIMEOUT);
                 if (abort) *abort = 1;
                 return false;
@@ -111,14 +117,15 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 // Same contract as mbar_wait, but polls with test_wait and never suspends:
 // for the one thread that feeds the tensor pipe, where a late wake-up leaves
 // the pipe idle.
-__device__ __forceinline__ bool mbar_spin(uint32_t bar, uint32_t parity, volatile int *abort, int32_t *status) {
+__device__ __forceinline__ bool mbar_spin(uint32_t bar, uint32_t parity, volatile int *abort, int32_t *status,
+                                          unsigned long long limit_ns = KP_WAIT_NS) {
     if (mbar_test(bar, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_test(bar, parity)) return true;
         if ((it & 255u) == 0) {
             if (abort && *abort) return false;
-            if (globaltimer_ns() - t0 > KP_WAIT_NS) {
+            if (globaltimer_ns() - t0 > limit_ns) {
                 set_status(status, KP_ERR_DEVICE_TIMEOUT);
                 if (abort) *abort = 1;
                 return false;
@@ -208,18 +215,6 @@ __device__ __forceinline__ void tmem_ld_16x256b_x4(uint32_t taddr, uint32_t (&r)
         : "r"(taddr));
 }
 
-// 32 TMEM lanes x 32 consecutive columns, written from the warp's registers.
-__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
-        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
-        "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
-        "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-        : "memory");
-}
 // 32 TMEM lanes x 16 consecutive columns (load and store).
 __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(
@@ -258,13 +253,6 @@ __device__ __forceinline__ float fast_log2(float x) {
     asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
     return r;
 }
-// Warp-wide max of a float (every lane gets the result).
-__device__ __forceinline__ float warp_max_f32(float v) {
-    float r;
-    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
-    return r;
-}
-
 // Shared-memory matrix descriptor, 128-byte swizzle, with explicit leading
 // and stride byte offsets.  K-major operands: LBO unused (16), SBO = bytes
 // between 8-row groups along M/N.  MN-major operands (64 contiguous M/N
@@ -309,11 +297,6 @@ __device__ __forceinline__ float4 dsmem_ld_f32x4(uint32_t addr) {
                  : "memory");
     return v;
 }
-__device__ __forceinline__ float2 dsmem_ld_f32x2(uint32_t addr) {
-    float2 v;
-    asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
-    return v;
-}
 
 // Shared-memory matrix descriptor for a K-major operand stored in the
 // 128-byte-swizzle canonical layout: rows of 64 bf16 (128 B), 8-row swizzle
@@ -341,41 +324,7 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n, bool a_mn = 
            | (static_cast<uint32_t>(m >> 4) << 24);   // M / 16
 }
 
-// ------------------------------------------------------------------ cp.async / ldmatrix / mma.sync
-__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint32_t src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-                 "r"(src_bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-    asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
-                                        uint32_t &r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
-                                          uint32_t &r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-// C[16x8] += A[16x16] * B[16x8], bf16 in, fp32 accumulate.
-__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a1,
-                                               uint32_t a2, uint32_t a3, uint32_t b0,
-                                               uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
+// bf16 pair (round to nearest even), lo in the low half.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);

@@ -79,6 +79,7 @@ struct ScorePlanArgs {
     int num_seqs;
     const int32_t *q_seq;
     const int32_t *q_pos;
+    const int32_t *seq_len;
     int max_tiles;
     int32_t *plan;     // nullptr: no plan to build
     int32_t *status;

@@ -11,9 +11,11 @@
 //
 // The array is loaded with the library and held by every GPU that loads it
 // until the process exits.  In host code its name is only a host-side
-// stand-in, so its device address is looked up once per device (with that
-// device current) by cudaGetSymbolAddress and cached; the kernels receive
-// that address.
+// stand-in, so its device address is looked up with the device current
+// (cudaGetSymbolAddress) and passed to the kernels.  The lookup is repeated on
+// every call made outside stream capture, so a device reset (which reloads the
+// module at another address) is picked up; a call made while its stream is
+// being captured uses the address cached by the last call outside capture.
 #include <mutex>
 
 #include "kp_common.cuh"
@@ -34,8 +36,9 @@ std::mutex g_noalloc_mutex;
 void *g_noalloc_addr[kMaxDevices] = {};
 
 // Device address of g_noalloc_plan on the current device (nullptr on error,
-// with the error recorded for kp_last_error).
-void *noalloc_plan_address() {
+// with the error recorded for kp_last_error).  Looked up afresh unless the
+// stream is capturing, then taken from the per-device cache.
+void *noalloc_plan_address(cudaStream_t stream) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) {
@@ -46,8 +49,14 @@ void *noalloc_plan_address() {
         record_error_text("kp_indexer_score_noalloc: device ordinal out of range");
         return nullptr;
     }
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    e = cudaStreamIsCapturing(stream, &cs);
+    if (e != cudaSuccess) {
+        record_cuda_error("cudaStreamIsCapturing", e);
+        return nullptr;
+    }
     std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-    if (!g_noalloc_addr[dev]) {
+    if (cs == cudaStreamCaptureStatusNone) {
         void *p = nullptr;
         e = cudaGetSymbolAddress(&p, g_noalloc_plan);
         if (e != cudaSuccess) {
@@ -55,6 +64,11 @@ void *noalloc_plan_address() {
             return nullptr;
         }
         g_noalloc_addr[dev] = p;
+    } else if (!g_noalloc_addr[dev]) {
+        record_error_text(
+            "kp_indexer_score_noalloc: first call on this device made during stream capture; "
+            "call it once outside capture first");
+        return nullptr;
     }
     return g_noalloc_addr[dev];
 }
@@ -70,7 +84,7 @@ extern "C" kp_status kp_indexer_score_noalloc(const kp_score_args *a, kp_stream_
         return KP_ERR_UNSUPPORTED;
     }
     if (a->q.num_queries <= 0) return kp_indexer_score(a, stream);
-    void *plan = kp::noalloc_plan_address();
+    void *plan = kp::noalloc_plan_address(reinterpret_cast<cudaStream_t>(stream));
     if (!plan) return KP_ERR_CUDA;
     // Every word of the plan that the scorer reads is rewritten by the plan
     // kernel of this call, so nothing has to be cleared between calls.

@@ -46,7 +46,7 @@ constexpr int kScQBoxBytes = kIndexHeads * 128;           // one query, one K bl
 constexpr int kScThreads = 192;
 constexpr int kScTmemCols = 512;
 constexpr int kScAccCols = 256;
-constexpr int kScNumBars = 2 * kScStages + 4 + 2;
+constexpr int kScNumBars = 2 * kScStages + 4 + 2 + 2;  // + drain, never
 constexpr int kScPlanStage = 4096;                        // plan words held in shared memory
 constexpr int kScLocalPlanMaxQ = (kScPlanStage - 5) / 4;  // queries whose whole plan fits there
 constexpr int kScSmemBytes = kScStages * kScAStageBytes + kScBBytes + kScNumBars * 8 + kScPlanStage * 4 + 1024;
@@ -55,11 +55,12 @@ constexpr int kScSmemBytes = kScStages * kScAStageBytes + kScBBytes + kScNumBars
 __global__ void __launch_bounds__(1024) score_plan_kernel(int nq, int num_seqs,
                                                           const int32_t *__restrict__ q_seq,
                                                           const int32_t *__restrict__ q_pos,
+                                                          const int32_t *__restrict__ seq_len,
                                                           int max_tiles, int32_t *plan_base,
                                                           int32_t *status) {
     __shared__ int scratch[33];
     pdl_wait_then_release();
-    build_score_plan(nq, num_seqs, q_seq, q_pos, max_tiles, plan_base, status, scratch);
+    build_score_plan(nq, num_seqs, q_seq, q_pos, seq_len, max_tiles, plan_base, status, scratch);
 }
 
 struct ScoreParams {
@@ -71,11 +72,14 @@ struct ScoreParams {
     const int32_t *q_seq;
     const int32_t *prev_len;   // tokens of each sequence before this step (nullptr: no early loads)
     const int32_t *q_pos;
+    const int32_t *seq_len;
     const float *w;
     const int64_t *pool_row_off;
     float *scores;
     int64_t stride;
     int32_t *status;
+    unsigned long long wait_ns;  // limit of one pipeline wait
+    int stall;                   // KP_DEBUG_STALL_FIRST_WAIT: the MMA warp's first wait never completes
 };
 
 // Barrier over the 4 epilogue warps (named barrier 1) that also ANDs a flag,
@@ -149,6 +153,8 @@ __global__ void __launch_bounds__(kScThreads, 1)
     auto acce_bar = [&](int a) { return bar0 + 8u * (2 * kScStages + 2 + a); };
     const uint32_t bfull_bar = bar0 + 8u * (2 * kScStages + 4);
     const uint32_t bempty_bar = bar0 + 8u * (2 * kScStages + 5);
+    const uint32_t drain_bar = bar0 + 8u * (2 * kScStages + 6);  // MMAs issued before a give-up are done
+    const uint32_t never_bar = bar0 + 8u * (2 * kScStages + 7);  // nothing arrives (failure-path tests)
 
     // Set-up that reads nothing an earlier kernel writes: before the grid
     // dependency resolves.  The query sequences and positions the local plan
@@ -173,6 +179,8 @@ __global__ void __launch_bounds__(kScThreads, 1)
         }
         mbar_init(bfull_bar, 1);
         mbar_init(bempty_bar, 1);
+        mbar_init(drain_bar, 1);
+        mbar_init(never_bar, 1);
         fence_mbar_init();
         abort_s = 0;
         tma_prefetch_desc(&tm_pool);
@@ -196,8 +204,8 @@ __global__ void __launch_bounds__(kScThreads, 1)
     bool dep_done = false;
     if (P.local_plan) {
         if (stage_q) __syncthreads();
-        build_score_plan(P.nq, P.num_seqs, stage_q ? qseq_s : P.q_seq, stage_q ? qpos_s : P.q_pos, P.max_tiles,
-                         unit0_s, P.status, plan_scratch);
+        build_score_plan(P.nq, P.num_seqs, stage_q ? qseq_s : P.q_seq, stage_q ? qpos_s : P.q_pos, P.seq_len,
+                         P.max_tiles, unit0_s, P.status, plan_scratch);
         plan_base = unit0_s;
     } else {
         pdl_wait_then_release();
@@ -233,12 +241,18 @@ __global__ void __launch_bounds__(kScThreads, 1)
             int64_t row_base = 0;
             uint32_t phase = 0;
             int old_pools = 0;  // pools of the group's sequence complete before this step
+            int a_phase[kScStages];  // phase of the last load issued into each stage (-1: none)
+#pragma unroll
+            for (int i = 0; i < kScStages; ++i) a_phase[i] = -1;
+            bool ok = true;
             for (int u = u_begin; u < u_end; ++u) {
                 if (gc.seek(u) || b_loads == 0) {
                     const int g = gc.g;
                     if (b_loads > 0 &&
-                        !mbar_wait(bempty_bar, (b_loads - 1) & 1, abort_flag, P.status))
+                        !mbar_wait(bempty_bar, (b_loads - 1) & 1, abort_flag, P.status, P.wait_ns)) {
+                        ok = false;
                         break;
+                    }
                     const int q0 = plan.q0[g], nq = plan.nq[g];
                     row_base = P.pool_row_off[plan.seq[g]];
                     old_pools = P.prev_len ? P.prev_len[plan.seq[g]] / kKpool : 0;
@@ -249,7 +263,10 @@ __global__ void __launch_bounds__(kScThreads, 1)
                                         bfull_bar, kb * 64, (q0 + qi) * kIndexHeads);
                     ++b_loads;
                 }
-                if (!mbar_wait(empty_bar(stage), phase ^ 1, abort_flag, P.status)) break;
+                if (!mbar_wait(empty_bar(stage), phase ^ 1, abort_flag, P.status, P.wait_ns)) {
+                    ok = false;
+                    break;
+                }
                 if (!dep_done && (u - gc.u0 + 1) * kScM > old_pools) {  // may hold pools written this step
                     pdl_wait_then_release();
                     dep_done = true;
@@ -259,6 +276,7 @@ __global__ void __launch_bounds__(kScThreads, 1)
                 const uint32_t dst = sA + stage * kScAStageBytes;
                 tma_load_2d(dst, &tm_pool, full_bar(stage), 0, row);
                 tma_load_2d(dst + kScABlockBytes, &tm_pool, full_bar(stage), 64, row);
+                a_phase[stage] = static_cast<int>(phase);
                 if (++stage == kScStages) {
                     stage = 0;
                     phase ^= 1;
@@ -267,6 +285,15 @@ __global__ void __launch_bounds__(kScThreads, 1)
             // This grid completes only after the previous one: kernels that wait
             // on this one may rely on everything before it.
             if (!dep_done) pdl_wait_then_release();
+            if (!ok) {
+                // Gave up: every load this thread issued lands before the shared
+                // memory and the CTA go away (the latest phase of each barrier it
+                // armed; bounded by the default limit).
+                if (b_loads > 0) mbar_wait(bfull_bar, (b_loads - 1) & 1, nullptr, P.status);
+#pragma unroll
+                for (int i = 0; i < kScStages; ++i)
+                    if (a_phase[i] >= 0) mbar_wait(full_bar(i), static_cast<uint32_t>(a_phase[i]), nullptr, P.status);
+            }
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -274,15 +301,16 @@ __global__ void __launch_bounds__(kScThreads, 1)
             gc.init(unit0, find_group(unit0, ng, u_begin));
             int b_loads = 0, stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0, idesc = 0;
-            for (int u = u_begin; u < u_end; ++u) {
+            bool ok = !P.stall || mbar_wait(never_bar, 0, abort_flag, P.status, P.wait_ns);
+            for (int u = u_begin; ok && u < u_end; ++u) {
                 if (gc.seek(u) || b_loads == 0) {
                     if (b_loads > 0) tc_commit(bempty_bar);
-                    if (!mbar_wait(bfull_bar, b_loads & 1, abort_flag, P.status)) break;
+                    if (!(ok = mbar_wait(bfull_bar, b_loads & 1, abort_flag, P.status, P.wait_ns))) break;
                     ++b_loads;
                     idesc = idesc_bf16_f32(kScM, kIndexHeads * plan.nq[gc.g]);
                 }
-                if (!mbar_wait(acce_bar(acc), acc_phase ^ 1, abort_flag, P.status)) break;
-                if (!mbar_wait(full_bar(stage), phase, abort_flag, P.status)) break;
+                if (!(ok = mbar_wait(acce_bar(acc), acc_phase ^ 1, abort_flag, P.status, P.wait_ns))) break;
+                if (!(ok = mbar_wait(full_bar(stage), phase, abort_flag, P.status, P.wait_ns))) break;
                 tc_fence_after();
                 const uint32_t a_base = sA + stage * kScAStageBytes;
                 const uint32_t d_tmem = tmem + acc * kScAccCols;
@@ -304,6 +332,11 @@ __global__ void __launch_bounds__(kScThreads, 1)
                     acc_phase ^= 1;
                 }
             }
+            if (!ok) {
+                // Gave up: every MMA already issued completes before the TMEM is freed.
+                tc_commit(drain_bar);
+                mbar_wait(drain_bar, 0, nullptr, P.status);
+            }
         }
     } else {
         // Epilogue: warp w may only touch TMEM lanes 32*(w%4) .. +31.  The head
@@ -318,7 +351,7 @@ __global__ void __launch_bounds__(kScThreads, 1)
         for (int u = u_begin; u < u_end; ++u) {
             const bool moved = gc.seek(u) || first;
             // every epilogue thread leaves together if any wait failed
-            if (!epi_bar_all(mbar_wait(accf_bar(acc), acc_phase, abort_flag, P.status))) break;
+            if (!epi_bar_all(mbar_wait(accf_bar(acc), acc_phase, abort_flag, P.status, P.wait_ns))) break;
             tc_fence_after();
             if (moved) {
                 q0 = plan.q0[gc.g];
@@ -377,6 +410,7 @@ ScorePlanArgs score_plan_args(const kp_score_args &a) {
     p.num_seqs = a.seqs.num_seqs;
     p.q_seq = a.q.q_seq;
     p.q_pos = a.q.q_pos;
+    p.seq_len = a.seqs.seq_len;
     p.max_tiles = (a.q.max_pools + kScM - 1) / kScM;
     p.plan = static_cast<int32_t *>(a.workspace);
     p.status = a.d_status;
@@ -397,7 +431,7 @@ kp_status launch_score(const kp_score_args &a, cudaStream_t s, bool plan_ready, 
     if (!plan_ready && !local_plan) {
         const kp_status st = launch_kernel("score_plan_kernel", score_plan_kernel,
                                            LaunchCfg(dim3(1), dim3(1024), 0, s), nq, a.seqs.num_seqs, a.q.q_seq,
-                                           a.q.q_pos, max_tiles, plan, a.d_status);
+                                           a.q.q_pos, a.seqs.seq_len, max_tiles, plan, a.d_status);
         if (st != KP_OK) return st;
     }
     if (max_tiles == 0) return KP_OK;
@@ -423,11 +457,14 @@ kp_status launch_score(const kp_score_args &a, cudaStream_t s, bool plan_ready, 
     P.q_seq = a.q.q_seq;
     P.prev_len = local_plan ? prev_len : nullptr;
     P.q_pos = a.q.q_pos;
+    P.seq_len = a.seqs.seq_len;
     P.w = a.w;
     P.pool_row_off = a.seqs.pool_row_off;
     P.scores = a.scores;
     P.stride = a.score_stride;
     P.status = a.d_status;
+    P.wait_ns = wait_limit_ns(a.cfg.wait_limit_us);
+    P.stall = (a.cfg.debug_flags & KP_DEBUG_STALL_FIRST_WAIT) ? 1 : 0;
     return launch_kernel("indexer_score_kernel", indexer_score_kernel,
                          LaunchCfg(dim3(sms), dim3(kScThreads), kScSmemBytes, s), tm_pool, tm_q, P);
 }

@@ -102,7 +102,17 @@ enum {
 
 enum { KP_COMPRESS_LEARNED = 0, KP_COMPRESS_MEAN = 1 };
 
-/* Method options. */
+/* debug_flags bits (tests of the failure paths; 0 in normal use). */
+enum {
+    /* The first pipeline wait of the scoring and attention kernels waits on a
+     * barrier that nothing completes, so it gives up after wait_limit_us: the
+     * kernel sets KP_ERR_DEVICE_TIMEOUT in d_status, lets every copy and MMA
+     * it issued finish, frees its tensor memory and returns (outputs of the
+     * call are then undefined).  Host-side only: no fault, no trap. */
+    KP_DEBUG_STALL_FIRST_WAIT = 1
+};
+
+/* Method and execution options. */
 typedef struct kp_config {
     int32_t kpool;              /* tokens per pool; must be 4 */
     int32_t topk_tokens;        /* token budget of the top-k (index_topk, 2048); a
@@ -110,6 +120,10 @@ typedef struct kp_config {
     int32_t compress_mode;      /* KP_COMPRESS_LEARNED (gate + ape softmax) or _MEAN */
     int32_t always_select_tail; /* 1: the query's incomplete pool is always attended */
     float sm_scale;             /* attention logit scale (1/16 = 1/sqrt(qk_head_dim 256)) */
+    int32_t wait_limit_us;      /* limit of any one device-side wait in microseconds; 0 =
+                                   1 s.  A wait that runs out sets KP_ERR_DEVICE_TIMEOUT
+                                   in d_status and the kernel returns early */
+    int32_t debug_flags;        /* KP_DEBUG_* bits; 0 in normal use */
 } kp_config;
 
 /* Per-sequence cache layout.  Sequence b's latent rows are rows
@@ -119,7 +133,9 @@ typedef struct kp_config {
  * sequences. */
 typedef struct kp_seqs {
     int32_t num_seqs;                /* host: B >= 1 */
-    const int32_t *seq_len;          /* [B] tokens in the caches, after this step's appends */
+    const int32_t *seq_len;          /* [B] tokens in the caches, after this step's appends; a
+                                        query at or past its sequence's length is skipped
+                                        (no scores, out 0, lse -inf) with KP_ERR_DEVICE_BOUNDS */
     const int64_t *latent_row_off;   /* [B] */
     const int64_t *pool_row_off;     /* [B] */
     int64_t latent_rows;             /* host: rows allocated in the latent cache */
@@ -275,9 +291,12 @@ KP_API kp_status kp_dsa_forward(const kp_forward_args *args, kp_stream_t stream)
  * the library until the process exits).  The call allocates nothing.
  *  - num_queries > KP_NOALLOC_MAX_QUERIES returns KP_ERR_UNSUPPORTED and
  *    launches nothing.
- *  - The first call on a device looks up the array's device address with
- *    that device current (cudaGetSymbolAddress) and caches it; make that
- *    first call before any stream capture on the device.
+ *  - Every call made outside stream capture looks up the array's device
+ *    address with the current device (cudaGetSymbolAddress) and caches it
+ *    per device; a call made while its stream is being captured uses that
+ *    cache, so make one call on the device outside capture first (a capture
+ *    before any such call returns KP_ERR_CUDA).  After cudaDeviceReset, make
+ *    one call outside capture again before capturing.
  *  - Every call shares the one array: calls whose kernels overlap on the GPU
  *    (different streams, or different host threads, without ordering between
  *    them) race and may produce wrong scores.  Calls in one stream are fine. */

@@ -167,8 +167,53 @@ def check_attend(g_out, g_lse, o_out, o_lse):
     return err / max(mx, 1e-30)
 
 
+def check_selection_fp64(g_sel, g_nsel, o_scores_row, k_pools):
+    """Selection of a path whose fp32 scores are not exposed (the fused step):
+    the count is exact, the list ascending and -1 padded, and every pool that
+    differs from the oracle's fp64 selection lies within the near-tie band."""
+    nf = o_scores_row.shape[0]
+    ns = int(g_nsel)
+    assert ns == min(k_pools, nf)
+    sel = np.asarray(g_sel[:ns])
+    assert (np.asarray(g_sel[ns:]) == -1).all()
+    assert (np.diff(sel) > 0).all() and (ns == 0 or (sel[0] >= 0 and sel[-1] < nf))
+    ref = oracle.topk_select(o_scores_row, k_pools)
+    diff = np.setxor1d(sel, ref)
+    if diff.size and ns < nf:
+        sK = np.sort(o_scores_row)[::-1][k_pools - 1]
+        gap = np.abs(o_scores_row[diff] - sK)
+        assert (gap <= NEAR_TIE * abs(sK)).all(), f"selection differs beyond near ties: {gap.max()}"
+    return int(diff.size)
+
+
+def _oracle_checks(sess, wl, queries, cfg, g_scores, g_idx, g_nsel, g_out, g_lse):
+    """Per-query comparison with the oracle on the GPU's own inputs to each
+    stage: scores (when given) on the GPU's pooled cache, the selection (exact
+    on the GPU's scores when given, near-tie band against fp64 scores always),
+    attention on the GPU's selection."""
+    report = dict(max_sel_diff=0, max_out_rel=0.0, checked=0)
+    for qi in queries:
+        b = int(wl.q_seq[qi])
+        pooled_gpu = gpu_pooled_of_seq(sess, wl, b)
+        o_sc = oracle_scores_on(pooled_gpu, wl, qi)
+        if g_scores is not None:
+            check_scores_row(g_scores[qi], o_sc)
+            d = check_selection(g_idx[qi], g_nsel[qi], g_scores[qi], o_sc, cfg.k_pools)
+        else:
+            d = check_selection_fp64(g_idx[qi], g_nsel[qi], o_sc, cfg.k_pools)
+        report["max_sel_diff"] = max(report["max_sel_diff"], d)
+        ns = int(g_nsel[qi])
+        o_out, o_lse = oracle_attend_on_selection(wl, qi, g_idx[qi][:ns], int(cfg.always_select_tail))
+        r = check_attend(g_out[qi], g_lse[qi], o_out, o_lse)
+        report["max_out_rel"] = max(report["max_out_rel"], r)
+        report["checked"] += 1
+    return report
+
+
 def full_check(wl, queries=None, cfg=None, stages=True, check_all_pooled=True):
-    """Runs the step on the GPU and checks every stage for the given queries."""
+    """Runs the step on the GPU (the four stage calls, or the fused
+    kp_dsa_forward when stages is False) and checks every stage for the given
+    queries."""
     cfg = cfg or cfg_of(wl)
     sess, step = make_gpu(wl, cfg)
     if stages:
@@ -178,26 +223,40 @@ def full_check(wl, queries=None, cfg=None, stages=True, check_all_pooled=True):
         scores = None
     torch.cuda.synchronize()
     assert int(sess.status.item()) == 0, f"device status {int(sess.status.item())}"
-    queries = range(wl.NQ) if queries is None else queries
-    mode = cfg.compress_mode
+    queries = list(range(wl.NQ) if queries is None else queries)
     seqs_needed = sorted({int(wl.q_seq[q]) for q in queries}) if not check_all_pooled else None
-    check_pooled(sess, wl, seqs_needed, mode)
+    check_pooled(sess, wl, seqs_needed, cfg.compress_mode)
     g_scores = host(scores).numpy() if scores is not None else None
-    g_idx = host(step.pool_idx).numpy()
-    g_nsel = host(step.n_sel).numpy()
-    g_out = host(step.out.float()).numpy()
-    g_lse = host(step.lse).numpy()
-    report = dict(max_sel_diff=0, max_out_rel=0.0)
-    for qi in queries:
-        b = int(wl.q_seq[qi])
-        pooled_gpu = gpu_pooled_of_seq(sess, wl, b)
-        o_sc = oracle_scores_on(pooled_gpu, wl, qi)
-        if g_scores is not None:
-            check_scores_row(g_scores[qi], o_sc)
-            d = check_selection(g_idx[qi], g_nsel[qi], g_scores[qi], o_sc, cfg.k_pools)
-            report["max_sel_diff"] = max(report["max_sel_diff"], d)
-        ns = int(g_nsel[qi])
-        o_out, o_lse = oracle_attend_on_selection(wl, qi, g_idx[qi][:ns], int(cfg.always_select_tail))
-        r = check_attend(g_out[qi], g_lse[qi], o_out, o_lse)
-        report["max_out_rel"] = max(report["max_out_rel"], r)
+    report = _oracle_checks(sess, wl, queries, cfg, g_scores, host(step.pool_idx).numpy(),
+                            host(step.n_sel).numpy(), host(step.out.float()).numpy(), host(step.lse).numpy())
+    assert report["checked"] == len(queries)
     return sess, step, report
+
+
+def fused_check(wl, queries=None, cfg=None, check_all_pooled=True):
+    """The path the bench times: kp_dsa_forward on fresh state, against the
+    four stage calls on other fresh state (bit for bit: pooled cache, tail
+    rings, selection, outputs) and against the oracle on the sampled queries
+    (scores from the staged run, selection and attention from the fused one)."""
+    cfg = cfg or cfg_of(wl)
+    sess_f, step_f = make_gpu(wl, cfg)
+    step_f.run()
+    sess_s, step_s = make_gpu(wl, cfg)
+    scores = step_s.run_stages()
+    torch.cuda.synchronize()
+    assert int(sess_f.status.item()) == 0, f"fused: device status {int(sess_f.status.item())}"
+    assert int(sess_s.status.item()) == 0, f"staged: device status {int(sess_s.status.item())}"
+    assert torch.equal(sess_f.pooled, sess_s.pooled), "pooled caches differ"
+    assert torch.equal(sess_f.tail_keys, sess_s.tail_keys) and torch.equal(sess_f.tail_gates, sess_s.tail_gates)
+    assert torch.equal(step_f.n_sel, step_s.n_sel), "n_sel differs"
+    assert torch.equal(step_f.pool_idx, step_s.pool_idx), "selection differs"
+    assert torch.equal(step_f.out, step_s.out), "outputs differ"
+    assert torch.equal(step_f.lse, step_s.lse), "lse differs"
+    queries = list(range(wl.NQ) if queries is None else queries)
+    seqs_needed = sorted({int(wl.q_seq[q]) for q in queries}) if not check_all_pooled else None
+    check_pooled(sess_f, wl, seqs_needed, cfg.compress_mode)
+    report = _oracle_checks(sess_f, wl, queries, cfg, host(scores).numpy(), host(step_f.pool_idx).numpy(),
+                            host(step_f.n_sel).numpy(), host(step_f.out.float()).numpy(),
+                            host(step_f.lse).numpy())
+    assert report["checked"] == len(queries)
+    return sess_f, step_f, report

@@ -30,7 +30,7 @@ def test_exports_every_declared_entry_point(L):
     for n in names:
         assert hasattr(L, n), n
     assert set(kp.EXPORTS) == set(names)
-    assert L.kp_version() == 100
+    assert L.kp_version() == 20000
 
 
 def test_status_strings(L):
@@ -60,6 +60,10 @@ def test_unsupported_kpool_and_bad_budget(L):
     assert L.kp_indexer_score(ctypes.byref(a), None) == 2
     t = kp.kp_topk_args()
     t.cfg = _cfg(compress_mode=7)
+    assert L.kp_topk_select(ctypes.byref(t), None) == 1
+    t.cfg = _cfg(wait_limit_us=-1)
+    assert L.kp_topk_select(ctypes.byref(t), None) == 1
+    t.cfg = _cfg(debug_flags=2)
     assert L.kp_topk_select(ctypes.byref(t), None) == 1
 
 

@@ -34,19 +34,36 @@ def test_tiny_all_stages_and_fused():
 
 
 def test_tiny_end_to_end_against_oracle_pipeline():
+    """The whole fused step against the oracle's whole pipeline (its own fp64
+    pooled keys, scores and selection): every query is compared; where the
+    two selections differ, every differing pool must be a near tie of the
+    oracle's K-th score, and the output is then compared with the oracle's
+    attention on the GPU's selection."""
     wl = KI.make(KI.named("tiny"))
     sess, step = PL.make_gpu(wl)
     step.run()
     torch.cuda.synchronize()
+    assert int(sess.status.item()) == 0
     pooled, _ = oracle.kpool_compress(KI.bits(wl.keys), KI.bits(wl.gates), KI.bits(wl.ape), 4)
     ref = oracle.dsa_queries(wl.q_seq, wl.q_pos, np.zeros(1, np.int64), np.zeros(1, np.int64), 4, wl.k_pools, 1,
                              KI.bits(wl.q_idx), wl.w.numpy(), pooled, KI.bits(wl.q_lat), KI.bits(wl.latent),
                              wl.spec.sm_scale)
     g_idx = step.pool_idx.cpu().numpy()
     assert np.array_equal(step.n_sel.cpu().numpy(), ref["n_sel"])
+    compared = 0
     for q in range(wl.NQ):
+        g_out, g_lse = step.out[q].float().cpu().numpy(), step.lse[q].cpu().numpy()
         if np.array_equal(g_idx[q], ref["sel"][q]):
-            PL.check_attend(step.out[q].float().cpu().numpy(), step.lse[q].cpu().numpy(), ref["out"][q], ref["lse"][q])
+            PL.check_attend(g_out, g_lse, ref["out"][q], ref["lse"][q])
+        else:
+            o_sc = oracle.indexer_score(KI.bits(wl.q_idx[q]), wl.w[q].numpy(), pooled,
+                                        (int(wl.q_pos[q]) + 1) // 4)
+            PL.check_selection_fp64(g_idx[q], step.n_sel[q].item(), o_sc, wl.k_pools)
+            ns = int(step.n_sel[q].item())
+            o_out, o_lse = PL.oracle_attend_on_selection(wl, q, g_idx[q][:ns])
+            PL.check_attend(g_out, g_lse, o_out, o_lse)
+        compared += 1
+    assert compared == wl.NQ
 
 
 @pytest.mark.parametrize("lens,n_q,topk", [
@@ -78,14 +95,18 @@ def test_very_short_sequences():
     PL.full_check(wl)
 
 
-def test_decode_config_sampled():
+# The four full-size workloads run through kp_dsa_forward -- the call the
+# bench times, in the launch configuration it times -- and are compared bit
+# for bit with the four stage calls on fresh state, and with the oracle on
+# sampled queries.
+def test_decode_config_fused_sampled():
     wl = KI.make(KI.named("decode"))
-    PL.full_check(wl, queries=[0, 13, 31], check_all_pooled=False)
+    PL.fused_check(wl, queries=[0, 13, 31], check_all_pooled=False)
 
 
-def test_ragged_config_sampled():
+def test_ragged_config_fused_sampled():
     wl = KI.make(KI.named("ragged"))
-    PL.full_check(wl, queries=[0, 5, 15], check_all_pooled=False)
+    PL.fused_check(wl, queries=[0, 5, 15], check_all_pooled=False)
 
 
 def test_large_logits_exercise_running_max_rescale():
@@ -104,21 +125,33 @@ def test_prefill_chunk_of_64_queries():
     PL.full_check(wl)
 
 
-def test_prefill_config_sampled():
+def test_prefill_config_fused_sampled():
+    # 4096 queries: above the scorer's shared-memory plan limit, so the fused
+    # step builds the plan in the compression launch's extra grid row and the
+    # scorer runs with the plan ready
     wl = KI.make(KI.named("prefill"))
-    PL.full_check(wl, queries=[0, 1, 2, 3, 2047, 4095], check_all_pooled=False)
+    PL.fused_check(wl, queries=[0, 1, 2, 3, 1023, 2047, 4095], check_all_pooled=False)
 
 
-def test_long_config_sampled():
+def test_long_config_fused_sampled():
     wl = KI.make(KI.named("long"))
-    PL.full_check(wl, queries=[0, 3], check_all_pooled=False)
+    PL.fused_check(wl, queries=[0, 1, 2, 3], check_all_pooled=False)
+
+
+def test_fused_over_1022_queries_small():
+    # 1,100 queries over two sequences: the fused step's plan-in-compression
+    # branch on a case the oracle checks in full at every 9th query
+    wl = KI.make(small_spec([3000, 2500], [700, 400], 256, seed=41))
+    assert wl.NQ > 1022
+    qs = sorted(set(range(0, wl.NQ, 9)) | {wl.NQ - 1, 699, 700})
+    PL.fused_check(wl, queries=qs)
 
 
 def test_exact_ties_in_scores():
-    # sequence 0: every pool identical -> all 5000 scores equal (more ties than
-    # the candidate buffer: the radix fallback); sequence 1: pooled keys repeat
-    # every 10 pools -> 75-fold ties at the threshold (candidate sort).  Ties go
-    # to the lower pool index in both.
+    # sequence 0: every pool identical -> all 5000 scores equal (the radix
+    # levels run down to a single key value shared by every pool); sequence 1:
+    # pooled keys repeat every 10 pools -> 75-fold ties at the threshold.  Ties
+    # go to the lower pool index in both.
     wl = KI.make(small_spec([20000, 3000], [1, 2], 256, seed=17))
     a, e = int(wl.tok_off[0]), int(wl.tok_off[0] + wl.lens[0])
     wl.keys[a:e] = wl.keys[a:a + 4].repeat((e - a) // 4, 1)
@@ -131,11 +164,15 @@ def test_exact_ties_in_scores():
     assert np.array_equal(sel0, np.arange(64)), "equal scores must select the lowest pool indices"
 
 
-def test_forward_without_new_tokens():
+@pytest.mark.parametrize("lens,n_q", [
+    ([1000, 1537], [2, 3]),          # scorer builds its plan in shared memory
+    ([2600, 2100], [600, 500]),      # 1,100 queries: the scorer's own plan kernel
+])
+def test_forward_without_new_tokens(lens, n_q):
     # every token is already cached: the step only queries, so there is no
-    # compression launch and the scorer builds its own plan
+    # compression launch
     from dsa_indexer_sparse_kpool_b300.session import Step, build_session
-    wl = KI.make(small_spec([1000, 1537], [2, 3], 256, seed=23))
+    wl = KI.make(small_spec(lens, n_q, 256, seed=23))
     cfg = PL.cfg_of(wl)
     lens = wl.lens.tolist()
     sess = build_session(cfg, lens, lens, wl.tok_off.tolist(), wl.pool_off.tolist(), wl.pool_rows, wl.latent,
@@ -143,23 +180,15 @@ def test_forward_without_new_tokens():
     empty = torch.zeros(0, 128, dtype=torch.bfloat16)
     step = Step(sess, lens, [0] * wl.B, empty, empty, wl.q_seq.tolist(), wl.q_pos.tolist(), wl.q_idx, wl.w,
                 wl.q_lat)
+    assert step.launches_per_step() == (3 if wl.NQ <= 1022 else 4)
     step.run()
     torch.cuda.synchronize()
     assert int(sess.status.item()) == 0
     PL.check_pooled(sess, wl)
-    g_idx, g_nsel = step.pool_idx.cpu().numpy(), step.n_sel.cpu().numpy()
-    for qi in range(wl.NQ):
-        b = int(wl.q_seq[qi])
-        o_sc = PL.oracle_scores_on(PL.gpu_pooled_of_seq(sess, wl, b), wl, qi)
-        ref = oracle.topk_select(o_sc, cfg.k_pools)
-        ns = int(g_nsel[qi])
-        assert ns == ref.size
-        diff = np.setxor1d(g_idx[qi][:ns], ref)
-        if diff.size:
-            sK = np.sort(o_sc)[::-1][cfg.k_pools - 1]
-            assert (np.abs(o_sc[diff] - sK) <= PL.NEAR_TIE * abs(sK)).all()
-        o_out, o_lse = PL.oracle_attend_on_selection(wl, qi, g_idx[qi][:ns])
-        PL.check_attend(step.out[qi].float().cpu().numpy(), step.lse[qi].cpu().numpy(), o_out, o_lse)
+    qs = range(wl.NQ) if wl.NQ < 64 else sorted(set(range(0, wl.NQ, 11)) | {wl.NQ - 1})
+    rep = PL._oracle_checks(sess, wl, qs, cfg, None, step.pool_idx.cpu().numpy(), step.n_sel.cpu().numpy(),
+                            step.out.float().cpu().numpy(), step.lse.cpu().numpy())
+    assert rep["checked"] == len(qs)
 
 
 def test_mtp_draft_layer_reuses_target_selection():

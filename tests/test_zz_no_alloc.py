@@ -54,3 +54,16 @@ def test_noalloc_scores_match_workspace_variant_twice():
     second = KI.make(KI.Spec("noalloc-b", [515, 4099, 600], [9, 8, 2], topk_tokens=256, seed=22))
     _compare(*_scores_both_ways(second))
 
+
+
+def test_noalloc_at_the_query_limit_and_past_the_shared_plan_stage():
+    # 8,192 queries (KP_NOALLOC_MAX_QUERIES: the plan fills the whole device
+    # array) and then 5,003: both too many for the scorer to hold the plan's
+    # group table in shared memory, so it reads the table from the array
+    assert kp.NOALLOC_MAX_QUERIES == 8192
+    full = KI.make(KI.Spec("noalloc-c", [2100, 2200, 2300, 2400], [2048] * 4, topk_tokens=256, seed=23))
+    assert full.NQ == kp.NOALLOC_MAX_QUERIES
+    _compare(*_scores_both_ways(full))
+    mid = KI.make(KI.Spec("noalloc-d", [2000, 2500, 1100], [2000, 2000, 1003], topk_tokens=256, seed=24))
+    assert 4096 < mid.NQ < kp.NOALLOC_MAX_QUERIES
+    _compare(*_scores_both_ways(mid))
