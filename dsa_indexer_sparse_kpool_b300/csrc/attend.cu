@@ -685,38 +685,70 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         }
         __syncthreads();
         // out[q][h][d] = (sum_s w_s O_s[h][d] + sum_j w_j c_j[d]) / L, 4 columns per item;
-        // a split with no tokens (w_s = 0) wrote no dump and is skipped.
+        // a split with no tokens (w_s = 0) wrote no dump and is skipped.  A thread
+        // takes kMrgItems items at a time and issues all their remote loads before
+        // using any, so the distributed-shared-memory latency is paid once per group.
         const uint32_t dump_u32 = smem_u32(dump);
-        for (int idx = tid; idx < nh * (kNopeDim / 4); idx += kAtThreads) {
-            const int hl = idx / (kNopeDim / 4), d = 4 * (idx % (kNopeDim / 4));
-            const float *w = wm_s + hl * 16;
-            const uint32_t off = static_cast<uint32_t>(((h0 + hl) * kNopeDim + d) * 4);
-            float4 v[kAtMaxSplits];
+        constexpr int kMrgItems = 2;
+        const int n_items = nh * (kNopeDim / 4);
+        for (int idx0 = tid; idx0 < n_items; idx0 += kMrgItems * kAtThreads) {
+            // weights of the items' heads into registers first (local reads), then
+            // every remote load of the group, then the arithmetic
+            float4 wv[kMrgItems][4];
 #pragma unroll
-            for (int s2 = 0; s2 < kAtMaxSplits; ++s2)
-                if (s2 < S && w[s2] > 0.f) v[s2] = dsmem_ld_f32x4(dsmem_addr(dump_u32 + off, s2));
-            float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int it = 0; it < kMrgItems; ++it) {
+                const int idx = min(idx0 + it * kAtThreads, n_items - 1);
+                const float4 *w4 = reinterpret_cast<const float4 *>(wm_s + (idx / (kNopeDim / 4)) * 16);
 #pragma unroll
-            for (int s2 = 0; s2 < kAtMaxSplits; ++s2) {
-                const float ws = s2 < S ? w[s2] : 0.f;
-                if (ws > 0.f) {
-                    a.x = fmaf(ws, v[s2].x, a.x);
-                    a.y = fmaf(ws, v[s2].y, a.y);
-                    a.z = fmaf(ws, v[s2].z, a.z);
-                    a.w = fmaf(ws, v[s2].w, a.w);
+                for (int k = 0; k < 4; ++k) wv[it][k] = w4[k];
+            }
+            float4 v[kMrgItems][kAtMaxSplits];
+#pragma unroll
+            for (int it = 0; it < kMrgItems; ++it) {
+                const int idx = idx0 + it * kAtThreads;
+                const float ws[8] = {wv[it][0].x, wv[it][0].y, wv[it][0].z, wv[it][0].w,
+                                     wv[it][1].x, wv[it][1].y, wv[it][1].z, wv[it][1].w};
+                if (idx < n_items) {
+                    const int hl = idx / (kNopeDim / 4), d = 4 * (idx % (kNopeDim / 4));
+                    const uint32_t off = static_cast<uint32_t>(((h0 + hl) * kNopeDim + d) * 4);
+#pragma unroll
+                    for (int s2 = 0; s2 < kAtMaxSplits; ++s2)
+                        if (s2 < S && ws[s2] > 0.f) v[it][s2] = dsmem_ld_f32x4(dsmem_addr(dump_u32 + off, s2));
                 }
             }
-            for (int j = 0; j < n_tail; ++j) {
-                const uint2 cv = *reinterpret_cast<const uint2 *>(tail_s + j * kNopeDim + d);
-                const float wt = w[8 + j];
-                a.x = fmaf(wt, bf16_lo(cv.x), a.x);
-                a.y = fmaf(wt, bf16_hi(cv.x), a.y);
-                a.z = fmaf(wt, bf16_lo(cv.y), a.z);
-                a.w = fmaf(wt, bf16_hi(cv.y), a.w);
+#pragma unroll
+            for (int it = 0; it < kMrgItems; ++it) {
+                const int idx = idx0 + it * kAtThreads;
+                if (idx >= n_items) break;
+                const int hl = idx / (kNopeDim / 4), d = 4 * (idx % (kNopeDim / 4));
+                const float ws[13] = {wv[it][0].x, wv[it][0].y, wv[it][0].z, wv[it][0].w,
+                                      wv[it][1].x, wv[it][1].y, wv[it][1].z, wv[it][1].w,
+                                      wv[it][2].x, wv[it][2].y, wv[it][2].z, wv[it][2].w, wv[it][3].x};
+                float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int s2 = 0; s2 < kAtMaxSplits; ++s2) {
+                    const float w_s = s2 < S ? ws[s2] : 0.f;
+                    if (w_s > 0.f) {
+                        a.x = fmaf(w_s, v[it][s2].x, a.x);
+                        a.y = fmaf(w_s, v[it][s2].y, a.y);
+                        a.z = fmaf(w_s, v[it][s2].z, a.z);
+                        a.w = fmaf(w_s, v[it][s2].w, a.w);
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < kAtMaxTail; ++j) {
+                    if (j >= n_tail) break;
+                    const uint2 cv = *reinterpret_cast<const uint2 *>(tail_s + j * kNopeDim + d);
+                    const float wt = ws[8 + j];
+                    a.x = fmaf(wt, bf16_lo(cv.x), a.x);
+                    a.y = fmaf(wt, bf16_hi(cv.x), a.y);
+                    a.z = fmaf(wt, bf16_lo(cv.y), a.z);
+                    a.w = fmaf(wt, bf16_hi(cv.y), a.w);
+                }
+                const float il = ws[12];
+                *reinterpret_cast<uint2 *>(P.out + (static_cast<int64_t>(q) * kMlaHeads + h0 + hl) * kNopeDim + d) =
+                    make_uint2(pack_bf16x2(a.x * il, a.y * il), pack_bf16x2(a.z * il, a.w * il));
             }
-            const float il = w[12];
-            *reinterpret_cast<uint2 *>(P.out + (static_cast<int64_t>(q) * kMlaHeads + h0 + hl) * kNopeDim + d) =
-                make_uint2(pack_bf16x2(a.x * il, a.y * il), pack_bf16x2(a.z * il, a.w * il));
         }
     } else if (!qvalid && merge_ok) {
         // Nothing to attend: out = 0, lse = -inf.

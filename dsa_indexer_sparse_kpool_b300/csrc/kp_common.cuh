@@ -284,17 +284,22 @@ __device__ __forceinline__ uint32_t dsmem_addr(uint32_t saddr, uint32_t rank) {
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
     return r;
 }
+// Loads from a peer's shared memory.  No memory clobber: callers order them
+// after the peer's writes with a cluster barrier (itself a volatile asm with a
+// memory clobber, which these volatile loads are not moved across), and
+// leaving ordinary shared-memory reads free to move lets the compiler issue a
+// group of remote loads back to back instead of interleaving local reads that
+// wait behind them.
 __device__ __forceinline__ float dsmem_ld_f32(uint32_t addr) {
     float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr));
     return v;
 }
 __device__ __forceinline__ float4 dsmem_ld_f32x4(uint32_t addr) {
     float4 v;
     asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
                  : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(addr)
-                 : "memory");
+                 : "r"(addr));
     return v;
 }
 
