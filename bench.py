@@ -55,6 +55,8 @@ def parse():
     ap.add_argument("--workload", default="decode", choices=["decode", "ragged", "prefill", "long"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the CPU-baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--paged", type=int, default=0, metavar="TOKENS",
+                    help="page the caches in pages of TOKENS positions (block table, shuffled pages)")
     return ap.parse_args()
 
 
@@ -330,7 +332,8 @@ def main():
     wl = workload(args.workload, rank)
     cfg = Config(topk_tokens=wl.spec.topk_tokens, sm_scale=wl.spec.sm_scale)
     sess = build_session(cfg, wl.lens.tolist(), wl.prev_len.tolist(), wl.tok_off.tolist(), wl.pool_off.tolist(),
-                         wl.pool_rows, wl.latent, wl.keys, wl.gates, wl.ape, device=dev)
+                         wl.pool_rows, wl.latent, wl.keys, wl.gates, wl.ape, device=dev,
+                         page_tokens=args.paged or None)
     step = build_step(sess, wl.lens.tolist(), wl.prev_len.tolist(), wl.tok_off.tolist(), wl.keys, wl.gates,
                       wl.q_seq, wl.q_pos, wl.q_idx, wl.w, wl.q_lat)
     NQ = wl.NQ
@@ -489,6 +492,7 @@ def main():
             "config": {"workload": DESCR[args.workload], "batch": wl.B, "queries": NQ,
                        "ctx": int(wl.lens.max()), "topk_tokens": wl.spec.topk_tokens,
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "caches": f"paged, {args.paged}-token pages (block table)" if args.paged else "contiguous",
                        "l2": "flushed between timed steps (256 MB read)", "timing": "CUDA-graph replay, events"},
             "roofline": roof,
             "stage_roofline": stage_roof,

@@ -38,7 +38,8 @@ class kp_config(ctypes.Structure):
 
 class kp_seqs(ctypes.Structure):
     _fields_ = [("num_seqs", _i32), ("seq_len", _vp), ("latent_row_off", _vp), ("pool_row_off", _vp),
-                ("latent_rows", _i64), ("pool_rows", _i64)]
+                ("latent_rows", _i64), ("pool_rows", _i64), ("block_table", _vp), ("page_tokens", _i32),
+                ("blocks_per_seq", _i32)]
 
 
 class kp_queries(ctypes.Structure):
@@ -48,8 +49,8 @@ class kp_queries(ctypes.Structure):
 class kp_compress_args(ctypes.Structure):
     _fields_ = [("cfg", kp_config), ("num_seqs", _i32), ("prev_len", _vp), ("new_off", _vp),
                 ("num_new", _i32), ("max_new_per_seq", _i32), ("keys", _vp), ("gates", _vp), ("ape", _vp),
-                ("tail_keys", _vp), ("tail_gates", _vp), ("pooled", _vp), ("pool_row_off", _vp),
-                ("pool_rows", _i64), ("d_status", _vp)]
+                ("tail_keys", _vp), ("tail_gates", _vp), ("pooled", _vp), ("seqs", kp_seqs),
+                ("d_status", _vp)]
 
 
 class kp_score_args(ctypes.Structure):
@@ -168,16 +169,22 @@ class Config:
 
 @dataclasses.dataclass
 class Seqs:
-    """Per-sequence cache layout (device int tensors)."""
+    """Per-sequence cache layout (device int tensors): contiguous rows per
+    sequence (row offsets), or pages of page_tokens positions named by a block
+    table [B, blocks_per_seq] (int32 physical page ids)."""
     seq_len: torch.Tensor           # [B] int32
-    latent_row_off: torch.Tensor    # [B] int64
-    pool_row_off: torch.Tensor      # [B] int64
+    latent_row_off: Optional[torch.Tensor]    # [B] int64 (contiguous)
+    pool_row_off: Optional[torch.Tensor]      # [B] int64 (contiguous)
     latent_rows: int
     pool_rows: int
+    block_table: Optional[torch.Tensor] = None   # [B, blocks_per_seq] int32 (paged)
+    page_tokens: int = 0
 
     def c(self) -> kp_seqs:
+        bt = self.block_table
         return kp_seqs(self.seq_len.numel(), _p(self.seq_len), _p(self.latent_row_off), _p(self.pool_row_off),
-                       self.latent_rows, self.pool_rows)
+                       self.latent_rows, self.pool_rows, _p(bt), int(self.page_tokens) if bt is not None else 0,
+                       int(bt.shape[1]) if bt is not None else 0)
 
 
 @dataclasses.dataclass
@@ -194,11 +201,11 @@ def score_stride(max_pools: int) -> int:
     return max(1, (max_pools + 127) // 128) * 128
 
 
-def kp_kpool_compress(cfg: Config, prev_len, new_off, keys, gates, ape, tail_keys, tail_gates, pooled,
-                      pool_row_off, max_new_per_seq: int, d_status=None, stream=None) -> None:
+def kp_kpool_compress(cfg: Config, seqs: Seqs, prev_len, new_off, keys, gates, ape, tail_keys, tail_gates, pooled,
+                      max_new_per_seq: int, d_status=None, stream=None) -> None:
     a = kp_compress_args(cfg.c(), prev_len.numel(), _p(prev_len), _p(new_off), keys.shape[0], int(max_new_per_seq),
-                         _p(keys), _p(gates), _p(ape), _p(tail_keys), _p(tail_gates), _p(pooled), _p(pool_row_off),
-                         pooled.shape[0], _p(d_status))
+                         _p(keys), _p(gates), _p(ape), _p(tail_keys), _p(tail_gates), _p(pooled), seqs.c(),
+                         _p(d_status))
     _check(lib().kp_kpool_compress(ctypes.byref(a), _stream(stream)), "kp_kpool_compress")
 
 

@@ -38,12 +38,26 @@ kp_status check_queries(const kp_queries &q) {
     return KP_OK;
 }
 
-kp_status check_seqs(const kp_seqs &s, bool latent, bool pooled) {
-    if (s.num_seqs < 1 || s.num_seqs > 65535 || !s.seq_len) return KP_ERR_INVALID_ARG;
-    if (latent && (!s.latent_row_off || s.latent_rows <= 0 || s.latent_rows >= (int64_t(1) << 40)))
+bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
+
+// Layout checks: latent / pooled say which cache the call reads or writes.
+// Paged mode: page_tokens a power of two in 16 .. 65536, the latent cache a
+// whole number of at least one page, the pooled cache as many pages of
+// page_tokens / kpool rows, and valid page ids that fit a TMA row coordinate.
+kp_status check_seqs(const kp_seqs &s, bool latent, bool pooled, bool need_seq_len = true) {
+    if (s.num_seqs < 1 || s.num_seqs > 65535 || (need_seq_len && !s.seq_len)) return KP_ERR_INVALID_ARG;
+    if (s.latent_rows <= 0 && (latent || s.block_table)) return KP_ERR_INVALID_ARG;
+    if (latent && s.latent_rows >= (int64_t(1) << 40)) return KP_ERR_INVALID_ARG;
+    if (pooled && (s.pool_rows <= 0 || s.pool_rows >= (int64_t(1) << 31))) return KP_ERR_INVALID_ARG;
+    if (!s.block_table) {
+        if ((latent && !s.latent_row_off) || (pooled && !s.pool_row_off)) return KP_ERR_INVALID_ARG;
+        return KP_OK;
+    }
+    if (!is_pow2(s.page_tokens) || s.page_tokens < 16 || s.page_tokens > 65536 || s.blocks_per_seq < 1)
         return KP_ERR_INVALID_ARG;
-    if (pooled && (!s.pool_row_off || s.pool_rows <= 0 || s.pool_rows >= (int64_t(1) << 31)))
-        return KP_ERR_INVALID_ARG;
+    const int64_t pages = s.latent_rows / s.page_tokens;
+    if (pages < 1 || pages > INT32_MAX) return KP_ERR_INVALID_ARG;
+    if (pooled && s.pool_rows < pages * (s.page_tokens / kKpool)) return KP_ERR_INVALID_ARG;
     return KP_OK;
 }
 
@@ -71,6 +85,23 @@ ForwardLayout forward_layout(const kp_forward_args &a, int sm_count) {
     return L;
 }
 }  // namespace
+
+CacheMap cache_map(const kp_seqs &s) {
+    CacheMap m;
+    m.latent_row_off = s.latent_row_off;
+    m.pool_row_off = s.pool_row_off;
+    m.block_table = s.block_table;
+    m.page_shift = 0;
+    m.blocks_per_seq = s.block_table ? s.blocks_per_seq : 0;
+    m.num_pages = 0;
+    if (s.block_table) {
+        while ((1 << m.page_shift) < s.page_tokens) ++m.page_shift;
+        m.num_pages = static_cast<int>(s.latent_rows / s.page_tokens);
+    }
+    m.latent_rows = s.latent_rows;
+    m.pool_rows = s.pool_rows;
+    return m;
+}
 
 void record_cuda_error(const char *where, cudaError_t err) {
     g_last_error = std::string(where) + ": " + cudaGetErrorName(err) + " (" + cudaGetErrorString(err) + ")";
@@ -153,9 +184,10 @@ kp_status validate_compress(const kp_compress_args *a) {
         return KP_ERR_INVALID_ARG;
     if (a->num_new == 0) return KP_OK;
     if (a->max_new_per_seq == 0 || a->max_new_per_seq > a->num_new) return KP_ERR_INVALID_ARG;
-    if (!a->prev_len || !a->new_off || !a->keys || !a->tail_keys || !a->pooled || !a->pool_row_off ||
-        a->pool_rows <= 0)
-        return KP_ERR_INVALID_ARG;
+    if (!a->prev_len || !a->new_off || !a->keys || !a->tail_keys || !a->pooled) return KP_ERR_INVALID_ARG;
+    if (a->seqs.num_seqs != a->num_seqs) return KP_ERR_INVALID_ARG;
+    const kp_status sst = check_seqs(a->seqs, false, true, false);
+    if (sst != KP_OK) return sst;
     if (a->cfg.compress_mode == KP_COMPRESS_LEARNED && (!a->gates || !a->ape || !a->tail_gates))
         return KP_ERR_INVALID_ARG;
     if (!aligned(a->keys, 8) || !aligned(a->pooled, 8) || !aligned(a->tail_keys, 8) ||
@@ -287,8 +319,7 @@ kp_status kp_dsa_forward(const kp_forward_args *a, kp_stream_t stream) {
     c.tail_keys = a->tail_keys;
     c.tail_gates = a->tail_gates;
     c.pooled = a->pooled;
-    c.pool_row_off = a->seqs.pool_row_off;
-    c.pool_rows = a->seqs.pool_rows;
+    c.seqs = a->seqs;
     c.d_status = a->d_status;
 
     kp_score_args sc;

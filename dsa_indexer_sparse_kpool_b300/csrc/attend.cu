@@ -140,11 +140,10 @@ static_assert(kBarNever + 1 == kNumBars, "barrier count");
 
 struct AttendParams {
     const uint16_t *latent;
-    int64_t latent_rows;
+    CacheMap cmap;               // where each sequence's latent rows live
     const int32_t *q_seq;
     const int32_t *q_pos;
     const int32_t *seq_len;
-    const int64_t *latent_row_off;
     int num_seqs;
     const int32_t *pool_idx;
     const int32_t *n_sel;
@@ -264,9 +263,11 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     const int b = P.q_seq[q];
     const int t = P.q_pos[q];
     bool qvalid = b >= 0 && b < P.num_seqs && t >= 0;
-    int64_t base_row = qvalid ? P.latent_row_off[b] : 0;
+    const bool paged = P.cmap.paged();
+    int64_t base_row = (qvalid && !paged) ? P.cmap.latent_row_off[b] : 0;
     if (qvalid && t >= P.seq_len[b]) qvalid = false;   // a query sits inside its sequence
-    if (qvalid && (base_row < 0 || base_row + t >= P.latent_rows)) qvalid = false;
+    if (qvalid && !paged && (base_row < 0 || base_row + t >= P.cmap.latent_rows)) qvalid = false;
+    if (qvalid && paged && (t >> P.cmap.page_shift) >= P.cmap.blocks_per_seq) qvalid = false;
     if (!qvalid && tid == 0) set_status(P.status, KP_ERR_DEVICE_BOUNDS);
     const int nf = qvalid ? (t + 1) / kKpool : 0;
     const int n_tail = (qvalid && P.tail) ? (t + 1) - nf * kKpool : 0;
@@ -394,8 +395,9 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         // starts on it while chunks 1-3 are still in flight.  Warp 0 posts each
         // chunk's byte count (boxes of other warps may land before it: the
         // transaction count may go negative, the phase cannot complete without
-        // this arrival).  Each lane reads its pool index one ring ahead of its
-        // slot, so no global read sits between a freed slot and its refill.
+        // this arrival).  Each lane reads its pool index two tiles ahead and,
+        // with paged caches, the page of that pool one tile ahead, so no
+        // global read sits between a freed slot and its refill.
         const int w = warp - kAtProdWarp0;
         const int my_chunk = lane >> 3, j = 4 * (lane & 7) + w;
         const int my_pool = j & 15, blk = 2 * my_chunk + (j >> 4);
@@ -403,12 +405,40 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         const int pool0 = tb * kAtPoolsPerTile;
         const int npools = min(nt * kAtPoolsPerTile, ns - pool0);
         const int32_t *plist = P.pool_idx + static_cast<int64_t>(q) * P.K + pool0 + my_pool;
-        auto fetch = [&](int t) -> int {
-            return (active && t * kAtPoolsPerTile + my_pool < npools) ? plist[t * kAtPoolsPerTile] : -1;
+        auto want = [&](int t) -> bool { return active && t * kAtPoolsPerTile + my_pool < npools; };
+        auto fetch_p = [&](int t) -> int { return want(t) ? plist[t * kAtPoolsPerTile] : -1; };
+        // Raw block-table entry of pool p's page (checked where it is used), -2
+        // when p itself is out of range; 0 for contiguous caches.
+        auto fetch_pg = [&](int p) -> int {
+            if (!paged) return 0;
+            if (p < 0 || p >= nf) return -2;
+            const int blk = (p * kKpool) >> P.cmap.page_shift;
+            if (blk >= P.cmap.blocks_per_seq) return -2;
+            return P.cmap.block_table[static_cast<int64_t>(b) * P.cmap.blocks_per_seq + blk];
         };
-        int pf[kAtSlots];
-#pragma unroll
-        for (int u = 0; u < kAtSlots; ++u) pf[u] = fetch(u);
+        // First row of this lane's pool in tile t, or a coordinate wholly above
+        // row 0 (zero fill) for a pool past the end of the list or out of range.
+        auto row_at = [&](int t, int p, int pg) -> int {
+            if (!want(t)) return -kKpool;
+            bool good = p >= 0 && p < nf;
+            int64_t r = 0;
+            if (good && !paged) r = base_row + static_cast<int64_t>(p) * kKpool;
+            if (good && paged) {
+                good = pg >= 0 && pg < P.cmap.num_pages;
+                r = (static_cast<int64_t>(pg) << P.cmap.page_shift) +
+                    ((p * kKpool) & ((1 << P.cmap.page_shift) - 1));
+            }
+            if (!good) {
+                set_status(P.status, KP_ERR_DEVICE_BOUNDS);
+                return -kKpool;
+            }
+            return static_cast<int>(r);
+        };
+        int pf_p[kAtSlots], pf_pg[kAtSlots];
+        pf_p[0] = fetch_p(0);
+        pf_p[1] = fetch_p(1);
+        pf_pg[0] = fetch_pg(pf_p[0]);
+        pf_pg[1] = 0;
         bool ok = true;
         int issued[kAtSlots][kAtChunks];   // latest tile whose chunk this warp loaded, per slot
 #pragma unroll
@@ -420,15 +450,9 @@ __global__ void __launch_bounds__(kAtThreads, 1)
             for (int u = 0; u < kAtSlots; ++u) {  // tile jj = j0 + u lives in slot u
                 const int jj = j0 + u;
                 if (!ok || jj >= nt) break;
-                const int p = pf[u];
-                pf[u] = fetch(jj + kAtSlots);
-                // First row of this lane's pool, or a coordinate wholly above row 0
-                // (zero fill) for a pool past the end of the list.
-                int y = -kKpool;
-                if (active && jj * kAtPoolsPerTile + my_pool < npools) {
-                    if (p >= 0 && p < nf) y = static_cast<int>(base_row + static_cast<int64_t>(p) * kKpool);
-                    else set_status(P.status, KP_ERR_DEVICE_BOUNDS);
-                }
+                const int y = row_at(jj, pf_p[u], pf_pg[u]);
+                pf_pg[u ^ 1] = fetch_pg(pf_p[u ^ 1]);   // page of tile jj + 1's pool
+                pf_p[u] = fetch_p(jj + kAtSlots);       // pool of tile jj + 2
                 const uint32_t dst = sTile + u * kAtTileBytes + blk * kAtBlockBytes + my_pool * kAtBoxBytes;
 #pragma unroll
                 for (int cc = 0; cc < kAtChunks; ++cc) {
@@ -616,9 +640,12 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         const int t2 = tid - kAtSoftThreads;
         for (int k = t2; k < n_tail * 64; k += kTailThreads) {
             const int j = k >> 6, piece = k & 63;
-            const int64_t row = base_row + static_cast<int64_t>(nf) * kKpool + j;
-            *reinterpret_cast<uint4 *>(tail_s + j * kNopeDim + piece * 8) =
-                *reinterpret_cast<const uint4 *>(P.latent + row * kLatentDim + piece * 8);
+            const int64_t row = paged ? P.cmap.latent_row(b, nf * kKpool + j)
+                                      : base_row + static_cast<int64_t>(nf) * kKpool + j;
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (row >= 0) v = *reinterpret_cast<const uint4 *>(P.latent + row * kLatentDim + piece * 8);
+            else if (piece == 0) set_status(P.status, KP_ERR_DEVICE_BOUNDS);
+            *reinterpret_cast<uint4 *>(tail_s + j * kNopeDim + piece * 8) = v;
         }
         // Q has landed (the tail logits read it; nothing may be in flight at exit).
         const bool have_q = mbar_wait(bar(kBarQ), 0, abort_flag, P.status, P.wait_ns);
@@ -854,11 +881,10 @@ kp_status launch_attend(const kp_attend_args &a, cudaStream_t s) {
         return KP_ERR_CUDA;
     AttendParams P;
     P.latent = a.latent;
-    P.latent_rows = a.seqs.latent_rows;
+    P.cmap = cache_map(a.seqs);
     P.q_seq = a.q.q_seq;
     P.q_pos = a.q.q_pos;
     P.seq_len = a.seqs.seq_len;
-    P.latent_row_off = a.seqs.latent_row_off;
     P.num_seqs = a.seqs.num_seqs;
     P.pool_idx = a.pool_idx;
     P.n_sel = a.n_sel;

@@ -17,6 +17,9 @@
 // gridDim.x, sequences on gridDim.y: no launch dimension scales with the
 // number of pools beyond gridDim.x's 2^31 limit.
 //
+// The pooled row of a pool comes from the sequence's row offset, or from its
+// block table when the caches are paged.
+//
 // Ring ownership: for sequence b, item 0 (the warp of the first pool touched)
 // is the only reader of the old ring rows AND the only writer of the new
 // ring rows; it reads before it writes, so no other warp can race with it.
@@ -49,8 +52,7 @@ __global__ void __launch_bounds__(kCompressWarps * 32)
                           const int32_t *__restrict__ new_off, const uint16_t *__restrict__ keys,
                           const uint16_t *__restrict__ gates, const uint16_t *__restrict__ ape,
                           uint16_t *__restrict__ tail_keys, uint16_t *__restrict__ tail_gates,
-                          uint16_t *__restrict__ pooled, const int64_t *__restrict__ pool_row_off,
-                          int64_t pool_rows, int32_t *status, ScorePlanArgs plan) {
+                          uint16_t *__restrict__ pooled, CacheMap cmap, int32_t *status, ScorePlanArgs plan) {
     constexpr int R = kKpool - 1;  // ring slots per sequence
     __shared__ int scratch[33];
     pdl_wait_then_release();
@@ -124,8 +126,8 @@ __global__ void __launch_bounds__(kCompressWarps * 32)
                 out[j] = s * (1.0f / kKpool);
             }
         }
-        const int64_t row = pool_row_off[b] + p;
-        if (row < 0 || row >= pool_rows) {
+        const int64_t row = cmap.pool_row(b, p);
+        if (row < 0) {
             if (lane == 0) set_status(status, KP_ERR_DEVICE_BOUNDS);
         } else {
             uint2 packed;
@@ -161,8 +163,8 @@ kp_status launch_compress(const kp_compress_args &a, cudaStream_t s, const Score
     dim3 grid((max_items + kCompressWarps - 1) / kCompressWarps, a.num_seqs + (pa.plan ? 1 : 0));
     return launch_kernel("kpool_compress_kernel", kpool_compress_kernel,
                          LaunchCfg(grid, dim3(kCompressWarps * 32), 0, s), a.cfg.compress_mode, a.prev_len,
-                         a.new_off, a.keys, a.gates, a.ape, a.tail_keys, a.tail_gates, a.pooled, a.pool_row_off,
-                         a.pool_rows, a.d_status, pa);
+                         a.new_off, a.keys, a.gates, a.ape, a.tail_keys, a.tail_gates, a.pooled, cache_map(a.seqs),
+                         a.d_status, pa);
 }
 
 }  // namespace kp

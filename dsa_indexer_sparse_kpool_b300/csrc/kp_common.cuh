@@ -52,6 +52,51 @@ __device__ __forceinline__ void pdl_wait_then_release() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Where a sequence's latent rows and pooled keys live: per-sequence row
+// offsets (contiguous mode) or a block table of pages (paged mode; a page of
+// 2^page_shift token positions holds as many latent rows and 2^page_shift / 4
+// pooled rows, at the same physical page id in both caches).
+struct CacheMap {
+    const int64_t *latent_row_off;
+    const int64_t *pool_row_off;
+    const int32_t *block_table;  // nullptr: contiguous mode
+    int page_shift;              // log2(tokens per page)
+    int blocks_per_seq;
+    int num_pages;               // valid page ids: 0 .. num_pages - 1
+    int64_t latent_rows;
+    int64_t pool_rows;
+
+    __device__ __forceinline__ bool paged() const { return block_table != nullptr; }
+    // Physical page of logical page `blk` of sequence b, or -1 when out of range.
+    __device__ __forceinline__ int page(int b, int blk) const {
+        if (blk < 0 || blk >= blocks_per_seq) return -1;
+        const int pg = block_table[static_cast<int64_t>(b) * blocks_per_seq + blk];
+        return (pg >= 0 && pg < num_pages) ? pg : -1;
+    }
+    // Latent-cache row of position `pos` of sequence b, or -1 when out of range.
+    __device__ __forceinline__ int64_t latent_row(int b, int pos) const {
+        if (!paged()) {
+            const int64_t r = latent_row_off[b] + pos;
+            return (pos >= 0 && r >= 0 && r < latent_rows) ? r : -1;
+        }
+        if (pos < 0) return -1;
+        const int pg = page(b, pos >> page_shift);
+        return pg < 0 ? -1 : (static_cast<int64_t>(pg) << page_shift) + (pos & ((1 << page_shift) - 1));
+    }
+    // Pooled-cache row of pool p of sequence b, or -1 when out of range.
+    __device__ __forceinline__ int64_t pool_row(int b, int p) const {
+        if (!paged()) {
+            const int64_t r = pool_row_off[b] + p;
+            return (p >= 0 && r >= 0 && r < pool_rows) ? r : -1;
+        }
+        if (p < 0) return -1;
+        const int ps = page_shift - 2;  // log2(pools per page); kpool = 4
+        const int pg = page(b, p >> ps);
+        return pg < 0 ? -1 : (static_cast<int64_t>(pg) << ps) + (p & ((1 << ps) - 1));
+    }
+};
+static_assert(KP_KPOOL == 4, "pooled rows per page are tokens per page / 4");
+
 // First error wins; later ones are dropped.
 __device__ __forceinline__ void set_status(int32_t *st, int code) {
     if (st) atomicCAS(st, 0, code);

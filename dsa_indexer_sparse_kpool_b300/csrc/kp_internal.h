@@ -9,8 +9,12 @@
 #include <utility>
 
 #include "kpool_dsa.h"
+#include "kp_common.cuh"
 
 namespace kp {
+
+// Device-side view of a kp_seqs layout (validated).
+CacheMap cache_map(const kp_seqs &s);
 
 // Records the text of a failed CUDA call for kp_last_error() (per host thread).
 void record_cuda_error(const char *where, cudaError_t err);

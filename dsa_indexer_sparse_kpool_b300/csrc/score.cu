@@ -74,7 +74,8 @@ struct ScoreParams {
     const int32_t *q_pos;
     const int32_t *seq_len;
     const float *w;
-    const int64_t *pool_row_off;
+    CacheMap cmap;             // where each sequence's pooled keys live
+    int seg;                   // pooled rows per TMA box: 128, or a page's pools when pages are shorter
     float *scores;
     int64_t stride;
     int32_t *status;
@@ -234,66 +235,101 @@ __global__ void __launch_bounds__(kScThreads, 1)
     }
 
     if (warp == 0) {
-        if (lane == 0) {
-            GroupCursor gc;
-            gc.init(unit0, find_group(unit0, ng, u_begin));
-            int b_loads = 0, stage = 0;
-            int64_t row_base = 0;
-            uint32_t phase = 0;
-            int old_pools = 0;  // pools of the group's sequence complete before this step
-            int a_phase[kScStages];  // phase of the last load issued into each stage (-1: none)
+        // TMA producer.  The whole warp walks the units (its control flow is
+        // uniform); lane 0 waits on the barriers and loads the queries, and the
+        // pooled-key tile is one box per K block (contiguous caches) or one box
+        // per page segment per K block, issued by lanes 0 .. segments - 1 (paged
+        // caches: a 128-pool tile spans 128 / (page_tokens / 4) pages when pages
+        // are shorter than 512 tokens).  Segments wholly past the group's last
+        // visible pool are zero-filled (negative row coordinate) instead of read
+        // through the block table.
+        const unsigned full = 0xffffffffu;
+        GroupCursor gc;
+        gc.init(unit0, find_group(unit0, ng, u_begin));
+        int b_loads = 0, stage = 0;
+        int64_t row_base = 0;
+        uint32_t phase = 0;
+        int old_pools = 0;  // pools of the group's sequence complete before this step
+        int need = 0;       // pools the group's queries can see
+        int bseq = 0;
+        int a_phase[kScStages];  // phase of the last load issued into each stage (-1: none)
 #pragma unroll
-            for (int i = 0; i < kScStages; ++i) a_phase[i] = -1;
-            bool ok = true;
-            for (int u = u_begin; u < u_end; ++u) {
-                if (gc.seek(u) || b_loads == 0) {
-                    const int g = gc.g;
-                    if (b_loads > 0 &&
-                        !mbar_wait(bempty_bar, (b_loads - 1) & 1, abort_flag, P.status, P.wait_ns)) {
-                        ok = false;
-                        break;
-                    }
-                    const int q0 = plan.q0[g], nq = plan.nq[g];
-                    row_base = P.pool_row_off[plan.seq[g]];
-                    old_pools = P.prev_len ? P.prev_len[plan.seq[g]] / kKpool : 0;
+        for (int i = 0; i < kScStages; ++i) a_phase[i] = -1;
+        bool ok = true;
+        const bool paged = P.cmap.paged();
+        const int nseg = kScM / P.seg;
+        for (int u = u_begin; u < u_end; ++u) {
+            if (gc.seek(u) || b_loads == 0) {
+                const int g = gc.g;
+                bool w_ok = true;
+                if (lane == 0 && b_loads > 0)
+                    w_ok = mbar_wait(bempty_bar, (b_loads - 1) & 1, abort_flag, P.status, P.wait_ns);
+                if (!__shfl_sync(full, w_ok, 0)) {
+                    ok = false;
+                    break;
+                }
+                const int q0 = plan.q0[g], nq = plan.nq[g];
+                bseq = plan.seq[g];
+                if (!paged) row_base = P.cmap.pool_row_off[bseq];
+                old_pools = P.prev_len ? P.prev_len[bseq] / kKpool : 0;
+                if (paged) need = __reduce_max_sync(full, lane < nq ? (P.q_pos[q0 + lane] + 1) / kKpool : 0);
+                if (lane == 0) {
                     mbar_expect_tx(bfull_bar, nq * 2 * kScQBoxBytes);
                     for (int qi = 0; qi < nq; ++qi)
                         for (int kb = 0; kb < 2; ++kb)
                             tma_load_2d(sB + kb * kScBBlockBytes + qi * kScQBoxBytes, &tm_q,
                                         bfull_bar, kb * 64, (q0 + qi) * kIndexHeads);
-                    ++b_loads;
                 }
-                if (!mbar_wait(empty_bar(stage), phase ^ 1, abort_flag, P.status, P.wait_ns)) {
-                    ok = false;
-                    break;
-                }
-                if (!dep_done && (u - gc.u0 + 1) * kScM > old_pools) {  // may hold pools written this step
-                    pdl_wait_then_release();
-                    dep_done = true;
-                }
-                mbar_expect_tx(full_bar(stage), kScAStageBytes);
-                const int row = static_cast<int>(row_base + static_cast<int64_t>(u - gc.u0) * kScM);
-                const uint32_t dst = sA + stage * kScAStageBytes;
-                tma_load_2d(dst, &tm_pool, full_bar(stage), 0, row);
-                tma_load_2d(dst + kScABlockBytes, &tm_pool, full_bar(stage), 64, row);
-                a_phase[stage] = static_cast<int>(phase);
-                if (++stage == kScStages) {
-                    stage = 0;
-                    phase ^= 1;
-                }
+                ++b_loads;
             }
-            // This grid completes only after the previous one: kernels that wait
-            // on this one may rely on everything before it.
-            if (!dep_done) pdl_wait_then_release();
-            if (!ok) {
-                // Gave up: every load this thread issued lands before the shared
-                // memory and the CTA go away (the latest phase of each barrier it
-                // armed; bounded by the default limit).
-                if (b_loads > 0) mbar_wait(bfull_bar, (b_loads - 1) & 1, nullptr, P.status);
+            bool w_ok = true;
+            if (lane == 0) w_ok = mbar_wait(empty_bar(stage), phase ^ 1, abort_flag, P.status, P.wait_ns);
+            if (!__shfl_sync(full, w_ok, 0)) {
+                ok = false;
+                break;
+            }
+            if (!dep_done && (u - gc.u0 + 1) * kScM > old_pools) {  // may hold pools written this step
+                pdl_wait_then_release();
+                dep_done = true;
+            }
+            const uint32_t dst = sA + stage * kScAStageBytes;
+            const int p0 = (u - gc.u0) * kScM;
+            if (lane == 0) mbar_expect_tx(full_bar(stage), kScAStageBytes);
+            if (!paged) {
+                if (lane == 0) {
+                    const int row = static_cast<int>(row_base + p0);
+                    tma_load_2d(dst, &tm_pool, full_bar(stage), 0, row);
+                    tma_load_2d(dst + kScABlockBytes, &tm_pool, full_bar(stage), 64, row);
+                }
+            } else if (lane < nseg) {
+                const int p = p0 + lane * P.seg;
+                int y = -P.seg;
+                if (p < need) {
+                    const int64_t r = P.cmap.pool_row(bseq, p);
+                    if (r >= 0) y = static_cast<int>(r);
+                    else set_status(P.status, KP_ERR_DEVICE_BOUNDS);
+                }
+                const uint32_t off = static_cast<uint32_t>(lane * P.seg * 128);
+                tma_load_2d(dst + off, &tm_pool, full_bar(stage), 0, y);
+                tma_load_2d(dst + kScABlockBytes + off, &tm_pool, full_bar(stage), 64, y);
+            }
+            a_phase[stage] = static_cast<int>(phase);
+            if (++stage == kScStages) {
+                stage = 0;
+                phase ^= 1;
+            }
+        }
+        // This grid completes only after the previous one: kernels that wait
+        // on this one may rely on everything before it.
+        if (!dep_done) pdl_wait_then_release();
+        if (!ok && lane == 0) {
+            // Gave up: every load the warp issued lands before the shared memory
+            // and the CTA go away (the latest phase of each barrier it armed;
+            // bounded by the default limit).
+            if (b_loads > 0) mbar_wait(bfull_bar, (b_loads - 1) & 1, nullptr, P.status);
 #pragma unroll
-                for (int i = 0; i < kScStages; ++i)
-                    if (a_phase[i] >= 0) mbar_wait(full_bar(i), static_cast<uint32_t>(a_phase[i]), nullptr, P.status);
-            }
+            for (int i = 0; i < kScStages; ++i)
+                if (a_phase[i] >= 0) mbar_wait(full_bar(i), static_cast<uint32_t>(a_phase[i]), nullptr, P.status);
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -436,9 +472,10 @@ kp_status launch_score(const kp_score_args &a, cudaStream_t s, bool plan_ready, 
     }
     if (max_tiles == 0) return KP_OK;
 
+    const int seg = a.seqs.block_table && a.seqs.page_tokens / kKpool < kScM ? a.seqs.page_tokens / kKpool : kScM;
     CUtensorMap tm_pool, tm_q;
     if (!make_tmap_bf16_sw128(&tm_pool, a.pooled, kIndexDim, static_cast<uint64_t>(a.seqs.pool_rows),
-                              kIndexDim * 2, 64, kScM) ||
+                              kIndexDim * 2, 64, static_cast<uint32_t>(seg)) ||
         !make_tmap_bf16_sw128(&tm_q, a.q_idx, kIndexDim, static_cast<uint64_t>(nq) * kIndexHeads,
                               kIndexDim * 2, 64, kIndexHeads))
         return KP_ERR_CUDA;
@@ -459,7 +496,8 @@ kp_status launch_score(const kp_score_args &a, cudaStream_t s, bool plan_ready, 
     P.q_pos = a.q.q_pos;
     P.seq_len = a.seqs.seq_len;
     P.w = a.w;
-    P.pool_row_off = a.seqs.pool_row_off;
+    P.cmap = cache_map(a.seqs);
+    P.seg = seg;
     P.scores = a.scores;
     P.stride = a.score_stride;
     P.status = a.d_status;

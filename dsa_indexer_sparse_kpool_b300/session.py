@@ -13,7 +13,7 @@ import torch
 
 from . import (Config, Queries, Seqs, forward_args, kp_dsa_forward, kp_indexer_score, kp_kpool_compress,
                kp_score_workspace_size, kp_attend_workspace_size, kp_sparse_mla_attend, kp_topk_select,
-               kp_workspace_size, score_stride, INDEX_DIM, MLA_HEADS, NOPE_DIM)
+               kp_workspace_size, score_stride, INDEX_DIM, LATENT_DIM, MLA_HEADS, NOPE_DIM)
 
 
 # Queries up to which the library's scorer builds its work plan in shared
@@ -32,36 +32,78 @@ def _dev_i64(x, device):
 class Session:
     """Caches of B sequences.
 
-    latent       [rows, 576] bf16, sequence b at rows latent_row_off[b] + position
-    keys, gates  [rows, 128] bf16 raw per-token indexer keys / gate logits laid out
-                 like the latent rows (kept on the host side of the caller; only the
-                 rows a step appends are uploaded per step)
-    pool_row_off first pooled-cache row of each sequence; pool_rows = capacity
+    latent       [rows, 576] bf16
+    pooled       [rows, 128] bf16, written by kp_kpool_compress
+    Contiguous layout (page_tokens None): sequence b at latent rows
+    latent_row_off[b] + position and pooled rows pool_row_off[b] + pool.
+    Paged layout (page_tokens P): the caches are pages of P positions (P / 4
+    pooled rows), handed to the sequences in a seeded random order, and a
+    block table [B, blocks_per_seq] names each sequence's pages; `latent` is
+    then given per token in the contiguous layout and scattered into pages.
     """
 
     def __init__(self, cfg: Config, lens: Sequence[int], latent_row_off: Sequence[int],
                  pool_row_off: Sequence[int], pool_rows: int, latent: torch.Tensor, ape: torch.Tensor,
-                 device="cuda"):
+                 device="cuda", page_tokens: Optional[int] = None, page_seed: int = 0):
         self.cfg = cfg
         self.device = torch.device(device)
         self.B = len(lens)
         self.lens = [int(x) for x in lens]
         self.latent_row_off_h = [int(x) for x in latent_row_off]
         self.pool_row_off_h = [int(x) for x in pool_row_off]
-        self.latent = latent.to(self.device).contiguous()
+        self.page_tokens = page_tokens
         self.ape = ape.to(self.device).contiguous()
-        self.pooled = torch.zeros(pool_rows, INDEX_DIM, dtype=torch.bfloat16, device=self.device)
+        if page_tokens is None:
+            self.latent = latent.to(self.device).contiguous()
+            self.pooled = torch.zeros(pool_rows, INDEX_DIM, dtype=torch.bfloat16, device=self.device)
+            self.block_table = None
+        else:
+            P = int(page_tokens)
+            need = [(L + P - 1) // P for L in self.lens]
+            self.blocks_per_seq = max(need) + 1
+            n_pages = sum(need) + max(1, sum(need) // 8)          # some pages stay free
+            perm = torch.randperm(n_pages, generator=torch.Generator().manual_seed(page_seed))
+            bt = torch.full((self.B, self.blocks_per_seq), -1, dtype=torch.int32)
+            k = 0
+            for b in range(self.B):
+                bt[b, :need[b]] = perm[k:k + need[b]].to(torch.int32)
+                k += need[b]
+            self.block_table_h = bt
+            self.block_table = bt.to(self.device).contiguous()
+            self.latent = torch.zeros(n_pages * P, LATENT_DIM, dtype=torch.bfloat16, device=self.device)
+            src = torch.cat([torch.arange(self.latent_row_off_h[b], self.latent_row_off_h[b] + self.lens[b])
+                             for b in range(self.B)])
+            dst = torch.cat([self.latent_rows_of(b, torch.arange(self.lens[b])) for b in range(self.B)])
+            self.latent.index_copy_(0, dst.to(self.device), latent[src].to(self.device))
+            self.pooled = torch.zeros(n_pages * (P // cfg.kpool), INDEX_DIM, dtype=torch.bfloat16,
+                                      device=self.device)
         R = cfg.kpool - 1
         self.tail_keys = torch.zeros(self.B, R, INDEX_DIM, dtype=torch.bfloat16, device=self.device)
         self.tail_gates = torch.zeros(self.B, R, INDEX_DIM, dtype=torch.bfloat16, device=self.device)
         self.seq_len = _dev_i32(self.lens, self.device)
-        self.latent_row_off = _dev_i64(self.latent_row_off_h, self.device)
-        self.pool_row_off = _dev_i64(self.pool_row_off_h, self.device)
+        self.latent_row_off = _dev_i64(self.latent_row_off_h, self.device) if page_tokens is None else None
+        self.pool_row_off = _dev_i64(self.pool_row_off_h, self.device) if page_tokens is None else None
         self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
+
+    def latent_rows_of(self, b: int, pos: torch.Tensor) -> torch.Tensor:
+        """Latent-cache rows of positions `pos` of sequence b (int64, host)."""
+        pos = pos.to(torch.int64)
+        if self.page_tokens is None:
+            return pos + self.latent_row_off_h[b]
+        P = int(self.page_tokens)
+        return self.block_table_h[b, pos // P].to(torch.int64) * P + pos % P
+
+    def pool_rows_of(self, b: int, pools: torch.Tensor) -> torch.Tensor:
+        """Pooled-cache rows of pools `pools` of sequence b (int64, host)."""
+        pools = pools.to(torch.int64)
+        if self.page_tokens is None:
+            return pools + self.pool_row_off_h[b]
+        pp = int(self.page_tokens) // self.cfg.kpool
+        return self.block_table_h[b, pools // pp].to(torch.int64) * pp + pools % pp
 
     def seqs(self) -> Seqs:
         return Seqs(self.seq_len, self.latent_row_off, self.pool_row_off, self.latent.shape[0],
-                    self.pooled.shape[0])
+                    self.pooled.shape[0], self.block_table, self.page_tokens or 0)
 
     def append(self, prev_len: Sequence[int], new_counts: Sequence[int], keys: torch.Tensor,
                gates: Optional[torch.Tensor], stream=None) -> None:
@@ -71,9 +113,9 @@ class Session:
             new_off.append(new_off[-1] + int(n))
         keys = keys.to(self.device).contiguous()
         gates = gates.to(self.device).contiguous() if gates is not None else None
-        kp_kpool_compress(self.cfg, _dev_i32(list(prev_len), self.device), _dev_i32(new_off, self.device),
-                          keys, gates, self.ape, self.tail_keys, self.tail_gates, self.pooled, self.pool_row_off,
-                          max(1, max(int(n) for n in new_counts)), d_status=self.status, stream=stream)
+        kp_kpool_compress(self.cfg, self.seqs(), _dev_i32(list(prev_len), self.device),
+                          _dev_i32(new_off, self.device), keys, gates, self.ape, self.tail_keys, self.tail_gates,
+                          self.pooled, max(1, max(int(n) for n in new_counts)), d_status=self.status, stream=stream)
 
 
 class Step:
@@ -179,8 +221,8 @@ class Step:
                 torch.empty(max(256, kp_attend_workspace_size(cfg, NQ)), dtype=torch.uint8, device=s.device))
         scores, ws, aws = self._stage_bufs
         calls = [
-            lambda: kp_kpool_compress(cfg, self.prev_len, self.new_off, self.keys, self.gates, s.ape, s.tail_keys,
-                                      s.tail_gates, s.pooled, s.pool_row_off, self.max_new, d_status=s.status),
+            lambda: kp_kpool_compress(cfg, self.seqs, self.prev_len, self.new_off, self.keys, self.gates, s.ape,
+                                      s.tail_keys, s.tail_gates, s.pooled, self.max_new, d_status=s.status),
             lambda: kp_indexer_score(cfg, self.seqs, self.queries, self.q_idx, self.w, s.pooled, scores, ws,
                                      d_status=s.status),
             lambda: kp_topk_select(cfg, self.queries, scores, self.pool_idx, self.n_sel, d_status=s.status),
@@ -192,8 +234,8 @@ class Step:
     # ---- the four stages one by one (same buffers), for stage-level checks
     def run_stages(self, stream=None):
         s, cfg = self.sess, self.sess.cfg
-        kp_kpool_compress(cfg, self.prev_len, self.new_off, self.keys, self.gates, s.ape, s.tail_keys,
-                          s.tail_gates, s.pooled, s.pool_row_off, self.max_new, d_status=s.status, stream=stream)
+        kp_kpool_compress(cfg, self.seqs, self.prev_len, self.new_off, self.keys, self.gates, s.ape, s.tail_keys,
+                          s.tail_gates, s.pooled, self.max_new, d_status=s.status, stream=stream)
         NQ = self.queries.q_seq.numel()
         stride = score_stride(self.queries.max_pools)
         scores = torch.empty(NQ, stride, dtype=torch.float32, device=s.device)
@@ -213,13 +255,15 @@ def _ranges(starts, ends):
 
 
 def build_session(cfg: Config, lens, prev_len, tok_off, pool_off, pool_rows: int, latent: torch.Tensor,
-                  keys: torch.Tensor, gates: torch.Tensor, ape: torch.Tensor, device="cuda") -> Session:
+                  keys: torch.Tensor, gates: torch.Tensor, ape: torch.Tensor, device="cuda",
+                  page_tokens: Optional[int] = None, page_seed: int = 0) -> Session:
     """Session whose caches hold positions [0, prev_len[b]) of each sequence.
 
     `keys`, `gates` and `latent` are per-token arrays laid out like the latent
     cache (sequence b at rows tok_off[b] + position).  The pooled cache and the
-    tail rings are built on the device by kp_kpool_compress."""
-    sess = Session(cfg, lens, tok_off, pool_off, pool_rows, latent, ape, device)
+    tail rings are built on the device by kp_kpool_compress.  With page_tokens
+    the caches are paged (block table, pages in a seeded random order)."""
+    sess = Session(cfg, lens, tok_off, pool_off, pool_rows, latent, ape, device, page_tokens, page_seed)
     B = len(lens)
     idx = _ranges([tok_off[b] for b in range(B)], [tok_off[b] + prev_len[b] for b in range(B)])
     if idx.numel():

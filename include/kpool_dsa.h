@@ -126,21 +126,42 @@ typedef struct kp_config {
     int32_t debug_flags;        /* KP_DEBUG_* bits; 0 in normal use */
 } kp_config;
 
-/* Per-sequence cache layout.  Sequence b's latent rows are rows
+/* Per-sequence cache layout, in one of two modes.
+ *
+ * Contiguous (block_table == NULL): sequence b's latent rows are rows
  * latent_row_off[b] .. + seq_len[b] - 1 of the latent cache (row i = token
  * position i), and its pooled keys are rows pool_row_off[b] + p of the pooled
- * cache (p = pool index).  Both caches are single buffers shared by all
- * sequences. */
+ * cache (p = pool index).
+ *
+ * Paged (block_table != NULL): both caches are split into pages of
+ * page_tokens token positions; the latent cache holds page j at rows
+ * j * page_tokens .. + page_tokens - 1 and the pooled cache holds the same
+ * page's pooled keys at rows j * (page_tokens / kpool) .. + page_tokens /
+ * kpool - 1, so one physical page id addresses both (the KV-pool pages of the
+ * MAX docs, Glm5NextConfig.infer_optimal_batch_size; the persistent block
+ * table of the Rust loader's Mixer::Dsa).  Position i of sequence b lives in
+ * physical page block_table[b * blocks_per_seq + i / page_tokens], pool p in
+ * page block_table[b * blocks_per_seq + p / (page_tokens / kpool)].  A pool
+ * never straddles two pages.  latent_row_off / pool_row_off are unused.  The
+ * valid page ids are 0 .. latent_rows / page_tokens - 1, and the pooled cache
+ * needs at least that many pages of rows; a page id out of range, or a
+ * position past blocks_per_seq pages, is skipped and reported as
+ * KP_ERR_DEVICE_BOUNDS.  Entries of pages past a sequence's length are never
+ * read. */
 typedef struct kp_seqs {
     int32_t num_seqs;                /* host: B >= 1 */
     const int32_t *seq_len;          /* [B] tokens in the caches, after this step's appends; a
                                         query at or past its sequence's length is skipped
                                         (no scores, out 0, lse -inf) with KP_ERR_DEVICE_BOUNDS */
-    const int64_t *latent_row_off;   /* [B] */
-    const int64_t *pool_row_off;     /* [B] */
+    const int64_t *latent_row_off;   /* [B] (contiguous mode) */
+    const int64_t *pool_row_off;     /* [B] (contiguous mode) */
     int64_t latent_rows;             /* host: rows allocated in the latent cache */
     int64_t pool_rows;               /* host: rows allocated in the pooled cache (< 2^31:
                                         TMA row coordinates are signed 32-bit) */
+    const int32_t *block_table;      /* [B][blocks_per_seq] physical page ids (paged mode), or NULL */
+    int32_t page_tokens;             /* host, paged mode: tokens per page, a power of two in
+                                        16 .. 65536 */
+    int32_t blocks_per_seq;          /* host, paged mode: row length of block_table, >= 1 */
 } kp_seqs;
 
 /* The query tokens of this step, flattened over sequences.  Queries of one
@@ -179,8 +200,8 @@ typedef struct kp_compress_args {
     uint16_t *tail_keys;          /* [B][kpool-1][128] bf16, in/out */
     uint16_t *tail_gates;         /* [B][kpool-1][128] bf16, in/out */
     uint16_t *pooled;             /* [pool_rows][128] bf16, out (completed pools only) */
-    const int64_t *pool_row_off;  /* [B] */
-    int64_t pool_rows;            /* host */
+    kp_seqs seqs;                 /* pooled-cache addressing: uses num_seqs (== num_seqs above),
+                                     pool_row_off and pool_rows, or the block table */
     int32_t *d_status;            /* optional */
 } kp_compress_args;
 
@@ -191,7 +212,7 @@ typedef struct kp_compress_args {
  * row are left as they were. */
 typedef struct kp_score_args {
     kp_config cfg;
-    kp_seqs seqs;                 /* uses num_seqs, pool_row_off, pool_rows */
+    kp_seqs seqs;                 /* uses num_seqs, seq_len, pool_row_off, pool_rows or the block table */
     kp_queries q;
     const uint16_t *q_idx;        /* [NQ][32][128] bf16 */
     const float *w;               /* [NQ][32] fp32 head weights */
@@ -230,7 +251,7 @@ typedef struct kp_topk_args {
  * by TMA, whose coordinates are signed 32-bit). */
 typedef struct kp_attend_args {
     kp_config cfg;
-    kp_seqs seqs;                 /* uses latent_row_off, latent_rows */
+    kp_seqs seqs;                 /* uses seq_len, latent_row_off, latent_rows or the block table */
     kp_queries q;
     const uint16_t *q_lat;        /* [NQ][64][576] bf16 (columns 512.. ignored) */
     const uint16_t *latent;       /* [latent_rows][576] bf16 */

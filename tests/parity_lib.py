@@ -40,10 +40,11 @@ def cfg_of(wl, **kw) -> Config:
     return c
 
 
-def make_gpu(wl, cfg=None, max_pools=None):
+def make_gpu(wl, cfg=None, max_pools=None, page_tokens=None, page_seed=0):
     cfg = cfg or cfg_of(wl)
     sess = build_session(cfg, wl.lens.tolist(), wl.prev_len.tolist(), wl.tok_off.tolist(), wl.pool_off.tolist(),
-                         wl.pool_rows, wl.latent, wl.keys, wl.gates, wl.ape)
+                         wl.pool_rows, wl.latent, wl.keys, wl.gates, wl.ape, page_tokens=page_tokens,
+                         page_seed=page_seed)
     step = build_step(sess, wl.lens.tolist(), wl.prev_len.tolist(), wl.tok_off.tolist(), wl.keys, wl.gates,
                       wl.q_seq, wl.q_pos, wl.q_idx, wl.w, wl.q_lat, max_pools)
     return sess, step
@@ -58,9 +59,11 @@ def bf16_bits(t):
 
 
 def gpu_pooled_of_seq(sess, wl, b):
+    """The pooled keys of sequence b's complete pools, in pool order, wherever
+    the session keeps them (row offsets or pages)."""
     n = int(wl.lens[b]) // wl.spec.kpool
-    o = int(wl.pool_off[b])
-    return bf16_bits(sess.pooled[o:o + n])
+    rows = sess.pool_rows_of(b, torch.arange(n)).to(sess.pooled.device)
+    return bf16_bits(sess.pooled.index_select(0, rows))
 
 
 def oracle_pooled_of_seq(wl, b, mode=0):
@@ -210,12 +213,12 @@ def _oracle_checks(sess, wl, queries, cfg, g_scores, g_idx, g_nsel, g_out, g_lse
     return report
 
 
-def full_check(wl, queries=None, cfg=None, stages=True, check_all_pooled=True):
+def full_check(wl, queries=None, cfg=None, stages=True, check_all_pooled=True, page_tokens=None):
     """Runs the step on the GPU (the four stage calls, or the fused
     kp_dsa_forward when stages is False) and checks every stage for the given
     queries."""
     cfg = cfg or cfg_of(wl)
-    sess, step = make_gpu(wl, cfg)
+    sess, step = make_gpu(wl, cfg, page_tokens=page_tokens)
     if stages:
         scores = step.run_stages()
     else:
@@ -233,15 +236,15 @@ def full_check(wl, queries=None, cfg=None, stages=True, check_all_pooled=True):
     return sess, step, report
 
 
-def fused_check(wl, queries=None, cfg=None, check_all_pooled=True):
+def fused_check(wl, queries=None, cfg=None, check_all_pooled=True, page_tokens=None):
     """The path the bench times: kp_dsa_forward on fresh state, against the
     four stage calls on other fresh state (bit for bit: pooled cache, tail
     rings, selection, outputs) and against the oracle on the sampled queries
     (scores from the staged run, selection and attention from the fused one)."""
     cfg = cfg or cfg_of(wl)
-    sess_f, step_f = make_gpu(wl, cfg)
+    sess_f, step_f = make_gpu(wl, cfg, page_tokens=page_tokens)
     step_f.run()
-    sess_s, step_s = make_gpu(wl, cfg)
+    sess_s, step_s = make_gpu(wl, cfg, page_tokens=page_tokens)
     scores = step_s.run_stages()
     torch.cuda.synchronize()
     assert int(sess_f.status.item()) == 0, f"fused: device status {int(sess_f.status.item())}"

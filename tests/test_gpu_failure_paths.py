@@ -106,7 +106,7 @@ def test_query_past_its_sequence_is_skipped_and_reported():
     wl, sess, step = _ready([1000, 1537], [2, 3], seed=54)
     short = sess.seq_len.clone()
     short[1] = int(wl.q_pos[4])          # the last query of sequence 1 sits at its length
-    seqs = kp.Seqs(short, sess.latent_row_off, sess.pool_row_off, sess.latent.shape[0], sess.pooled.shape[0])
+    seqs = dataclasses.replace(sess.seqs(), seq_len=short)
     out, lse = torch.empty_like(step.out), torch.empty_like(step.lse)
     _attend(sess, step, sess.cfg, out, lse, seqs=seqs)
     assert kp.kp_read_device_status(sess.status) == BOUNDS
