@@ -18,10 +18,10 @@
 // and chunked prefill (8 queries per group) run the same kernel: decode is
 // bound by streaming pooled keys from HBM, prefill by the tensor pipe.
 //
-// Warp roles (192 threads, one CTA per SM, persistent):
+// Warp roles (320 threads, one CTA per SM, persistent):
 //   warp 0     TMA producer (one elected lane)
 //   warp 1     TMEM allocator + MMA issuer (one elected lane)
-//   warps 2-5  epilogue: TMEM -> registers -> masked scores -> global
+//   warps 2-9  epilogue: TMEM -> registers -> masked scores -> global (two per lane quadrant)
 // Work units are (query group, 128-pool tile) pairs laid out by a work plan:
 // built by every CTA in shared memory for up to 1,022 queries, else by a plan
 // kernel or an extra row of the compression launch; each CTA takes a
@@ -43,7 +43,8 @@ constexpr int kScAStageBytes = 2 * kScABlockBytes;        // K = 128 -> two swiz
 constexpr int kScBBlockBytes = kScMaxN * 128;             // [256 rows][64 bf16] = 32 KB
 constexpr int kScBBytes = 2 * kScBBlockBytes;
 constexpr int kScQBoxBytes = kIndexHeads * 128;           // one query, one K block: 4 KB
-constexpr int kScThreads = 192;
+constexpr int kScEpiThreads = 256;                       // 8 epilogue warps, two per TMEM lane quadrant
+constexpr int kScThreads = 64 + kScEpiThreads;
 constexpr int kScTmemCols = 512;
 constexpr int kScAccCols = 256;
 constexpr int kScNumBars = 2 * kScStages + 4 + 2 + 2;  // + drain, never
@@ -90,7 +91,7 @@ __device__ __forceinline__ bool epi_bar_all(bool v) {
     asm volatile(
         "{\n\t.reg .pred p, q;\n\t"
         "setp.ne.u32 q, %1, 0;\n\t"
-        "bar.red.and.pred p, 1, 128, q;\n\t"
+        "bar.red.and.pred p, 1, 256, q;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}\n"
         : "=r"(r)
         : "r"(static_cast<uint32_t>(v))
@@ -176,7 +177,7 @@ __global__ void __launch_bounds__(kScThreads, 1)
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(accf_bar(a), 1);
-            mbar_init(acce_bar(a), 128);
+            mbar_init(acce_bar(a), kScEpiThreads);
         }
         mbar_init(bfull_bar, 1);
         mbar_init(bempty_bar, 1);
@@ -375,15 +376,32 @@ __global__ void __launch_bounds__(kScThreads, 1)
             }
         }
     } else {
-        // Epilogue: warp w may only touch TMEM lanes 32*(w%4) .. +31.  The head
+        // Epilogue: warp w may only touch TMEM lanes 32*(w%4) .. +31.  Two warps
+        // share each lane quadrant and split the group's queries (even / odd),
+        // so each scheduler has two epilogue warps to interleave.  A thread owns
+        // one pool row: it loads two queries' 32 head columns before waiting,
+        // then reduces ReLU(.) * w over the heads with packed fp32x2 FMAs into
+        // eight independent partial sums (fp32, round to nearest).  The head
         // weights and causal limits of the current query group are staged in
         // shared memory when the group changes.
-        const int quad = warp & 3, et = threadIdx.x - 64;
+        const int quad = warp & 3, et = threadIdx.x - 64, half = et >> 7;
         GroupCursor gc;
         gc.init(unit0, find_group(unit0, ng, u_begin));
         int acc = 0, q0 = 0, nq = 0;
         bool first = true;
         uint32_t acc_phase = 0;
+        auto reduce = [&](const uint32_t (&r)[32], int qi) -> float {
+            const uint64_t *wq = reinterpret_cast<const uint64_t *>(w_s + qi * kIndexHeads);
+            uint64_t a[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+            for (int h2 = 0; h2 < kIndexHeads / 2; ++h2)
+                a[h2 & 3] = fma_f32x2(wq[h2], pack_f32x2(fmaxf(__uint_as_float(r[2 * h2]), 0.f),
+                                                           fmaxf(__uint_as_float(r[2 * h2 + 1]), 0.f)),
+                                      a[h2 & 3]);
+            const float2 s0 = unpack_f32x2(a[0]), s1 = unpack_f32x2(a[1]), s2 = unpack_f32x2(a[2]),
+                         s3 = unpack_f32x2(a[3]);
+            return ((s0.x + s0.y) + (s1.x + s1.y)) + ((s2.x + s2.y) + (s3.x + s3.y));
+        };
         for (int u = u_begin; u < u_end; ++u) {
             const bool moved = gc.seek(u) || first;
             // every epilogue thread leaves together if any wait failed
@@ -392,30 +410,28 @@ __global__ void __launch_bounds__(kScThreads, 1)
             if (moved) {
                 q0 = plan.q0[gc.g];
                 nq = plan.nq[gc.g];
-                for (int k = et; k < nq * kIndexHeads; k += 128) w_s[k] = P.w[static_cast<int64_t>(q0) * kIndexHeads + k];
+                for (int k = et; k < nq * kIndexHeads; k += kScEpiThreads)
+                    w_s[k] = P.w[static_cast<int64_t>(q0) * kIndexHeads + k];
                 if (et < nq) nf_s[et] = (P.q_pos[q0 + et] + 1) / kKpool;
                 epi_bar_all(true);
                 first = false;
             }
             const int p = (u - gc.u0) * kScM + quad * 32 + lane;
-            for (int qi = 0; qi < nq; ++qi) {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(tmem + acc * kScAccCols + qi * kIndexHeads +
-                                       (static_cast<uint32_t>(quad * 32) << 16),
-                                   r);
+            const uint32_t tbase = tmem + acc * kScAccCols + (static_cast<uint32_t>(quad * 32) << 16);
+            for (int qi = half; qi < nq; qi += 4) {
+                const int qj = qi + 2;                   // the warp's next query, if any
+                uint32_t r0[32], r1[32];
+                tmem_ld_32x32b_x32(tbase + qi * kIndexHeads, r0);
+                if (qj < nq) tmem_ld_32x32b_x32(tbase + qj * kIndexHeads, r1);
                 tmem_ld_wait();
-                const float4 *wq = reinterpret_cast<const float4 *>(w_s + qi * kIndexHeads);
-                float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-                for (int h4 = 0; h4 < kIndexHeads / 4; ++h4) {
-                    const float4 wv = wq[h4];
-                    s0 = fmaf(wv.x, fmaxf(__uint_as_float(r[4 * h4]), 0.f), s0);
-                    s1 = fmaf(wv.y, fmaxf(__uint_as_float(r[4 * h4 + 1]), 0.f), s1);
-                    s0 = fmaf(wv.z, fmaxf(__uint_as_float(r[4 * h4 + 2]), 0.f), s0);
-                    s1 = fmaf(wv.w, fmaxf(__uint_as_float(r[4 * h4 + 3]), 0.f), s1);
+                const float v0 = reduce(r0, qi);
+                if (p < P.stride)
+                    P.scores[static_cast<int64_t>(q0 + qi) * P.stride + p] = p < nf_s[qi] ? v0 : -INFINITY;
+                if (qj < nq) {
+                    const float v1 = reduce(r1, qj);
+                    if (p < P.stride)
+                        P.scores[static_cast<int64_t>(q0 + qj) * P.stride + p] = p < nf_s[qj] ? v1 : -INFINITY;
                 }
-                const int q = q0 + qi;
-                if (p < P.stride) P.scores[static_cast<int64_t>(q) * P.stride + p] = p < nf_s[qi] ? s0 + s1 : -INFINITY;
             }
             tc_fence_before();
             mbar_arrive(acce_bar(acc));
