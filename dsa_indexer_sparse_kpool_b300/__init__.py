@@ -79,10 +79,34 @@ class kp_forward_args(ctypes.Structure):
                 ("workspace", _vp), ("workspace_bytes", _sz), ("d_status", _vp)]
 
 
+class kp_gemm_args(ctypes.Structure):
+    _fields_ = [("m", _i32), ("n", _i32), ("k", _i32), ("batch", _i32), ("a", _vp), ("lda", _i64),
+                ("a_batch_off", _i64), ("b", _vp), ("ldb", _i64), ("b_batch_off", _i64), ("c", _vp),
+                ("ldc", _i64), ("c_batch_off", _i64), ("c_dtype", _i32), ("wait_limit_us", _i32),
+                ("d_status", _vp)]
+
+
+class kp_indexer_project_args(ctypes.Structure):
+    _fields_ = [("num_tokens", _i32), ("hidden", _vp), ("q_lora", _vp), ("w_iq", _vp), ("w_ik", _vp),
+                ("w_ig", _vp), ("w_iw", _vp), ("q_idx", _vp), ("keys", _vp), ("gates", _vp), ("w", _vp),
+                ("wait_limit_us", _i32), ("d_status", _vp)]
+
+
+class kp_mla_absorb_q_args(ctypes.Structure):
+    _fields_ = [("num_tokens", _i32), ("q_nope", _vp), ("w_uk", _vp), ("q_lat", _vp), ("wait_limit_us", _i32),
+                ("d_status", _vp)]
+
+
+class kp_mla_absorb_out_args(ctypes.Structure):
+    _fields_ = [("num_tokens", _i32), ("out", _vp), ("w_uv", _vp), ("w_o", _vp), ("o", _vp),
+                ("hidden_out", _vp), ("wait_limit_us", _i32), ("d_status", _vp)]
+
+
 EXPORTS = ("kp_kpool_compress", "kp_indexer_score", "kp_topk_select", "kp_sparse_mla_attend",
            "kp_dsa_forward", "kp_indexer_score_noalloc", "kp_score_workspace_size", "kp_attend_workspace_size",
-           "kp_workspace_size",
+           "kp_workspace_size", "kp_gemm_bf16", "kp_indexer_project", "kp_mla_absorb_q", "kp_mla_absorb_out",
            "kp_status_string", "kp_last_error", "kp_read_device_status", "kp_version")
+DTYPE_BF16, DTYPE_F32 = 0, 1
 
 _lib = None
 
@@ -97,7 +121,10 @@ def lib() -> ctypes.CDLL:
         for name, argt in (("kp_kpool_compress", kp_compress_args), ("kp_indexer_score", kp_score_args),
                            ("kp_indexer_score_noalloc", kp_score_args),
                            ("kp_topk_select", kp_topk_args), ("kp_sparse_mla_attend", kp_attend_args),
-                           ("kp_dsa_forward", kp_forward_args)):
+                           ("kp_dsa_forward", kp_forward_args), ("kp_gemm_bf16", kp_gemm_args),
+                           ("kp_indexer_project", kp_indexer_project_args),
+                           ("kp_mla_absorb_q", kp_mla_absorb_q_args),
+                           ("kp_mla_absorb_out", kp_mla_absorb_out_args)):
             f = getattr(L, name)
             f.argtypes = [ctypes.POINTER(argt), _vp]
             f.restype = ctypes.c_int
@@ -273,3 +300,32 @@ def kp_read_device_status(d_status: torch.Tensor, stream=None) -> int:
 
 def kp_version() -> int:
     return int(lib().kp_version())
+
+
+# ---------------------------------------------------------------- the steps either side
+
+def kp_gemm_bf16(a, b, c, m, n, k, batch=1, lda=None, a_batch_off=0, ldb=None, b_batch_off=0, ldc=None,
+                 c_batch_off=0, d_status=None, stream=None, wait_limit_us=0) -> None:
+    """C[b][m][n] = sum_k A[b][m][k] B[b][n][k] (bf16 tensors A, B; C bf16 or fp32)."""
+    c_dtype = DTYPE_F32 if c.dtype == torch.float32 else DTYPE_BF16
+    g = kp_gemm_args(m, n, k, batch, _p(a), lda if lda is not None else k, a_batch_off, _p(b),
+                     ldb if ldb is not None else k, b_batch_off, _p(c), ldc if ldc is not None else n, c_batch_off,
+                     c_dtype, int(wait_limit_us), _p(d_status))
+    _check(lib().kp_gemm_bf16(ctypes.byref(g), _stream(stream)), "kp_gemm_bf16")
+
+
+def kp_indexer_project(hidden, q_lora, w_iq, w_ik, w_ig, w_iw, q_idx, keys, gates, w, d_status=None,
+                       stream=None) -> None:
+    a = kp_indexer_project_args(hidden.shape[0], _p(hidden), _p(q_lora), _p(w_iq), _p(w_ik), _p(w_ig), _p(w_iw),
+                                _p(q_idx), _p(keys), _p(gates), _p(w), 0, _p(d_status))
+    _check(lib().kp_indexer_project(ctypes.byref(a), _stream(stream)), "kp_indexer_project")
+
+
+def kp_mla_absorb_q(q_nope, w_uk, q_lat, d_status=None, stream=None) -> None:
+    a = kp_mla_absorb_q_args(q_nope.shape[0], _p(q_nope), _p(w_uk), _p(q_lat), 0, _p(d_status))
+    _check(lib().kp_mla_absorb_q(ctypes.byref(a), _stream(stream)), "kp_mla_absorb_q")
+
+
+def kp_mla_absorb_out(out, w_uv, w_o, o, hidden_out, d_status=None, stream=None) -> None:
+    a = kp_mla_absorb_out_args(out.shape[0], _p(out), _p(w_uv), _p(w_o), _p(o), _p(hidden_out), 0, _p(d_status))
+    _check(lib().kp_mla_absorb_out(ctypes.byref(a), _stream(stream)), "kp_mla_absorb_out")

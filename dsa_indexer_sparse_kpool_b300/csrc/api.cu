@@ -390,6 +390,115 @@ kp_status kp_dsa_forward(const kp_forward_args *a, kp_stream_t stream) {
     return launch_attend(at, s);
 }
 
+// ---- the steps either side: dense products -------------------------------
+
+namespace {
+kp_status validate_gemm(const kp_gemm_args *g) {
+    if (!g) return KP_ERR_INVALID_ARG;
+    if (g->m < 0 || g->n < 0 || g->k <= 0 || g->k % 64 != 0 || g->batch < 1) return KP_ERR_INVALID_ARG;
+    if (g->c_dtype != KP_DTYPE_BF16 && g->c_dtype != KP_DTYPE_F32) return KP_ERR_INVALID_ARG;
+    if (g->wait_limit_us < 0) return KP_ERR_INVALID_ARG;
+    if (g->m == 0 || g->n == 0) return KP_OK;
+    if (!g->a || !g->b || !g->c) return KP_ERR_INVALID_ARG;
+    if (!aligned(g->a, 16) || !aligned(g->b, 16) || !aligned(g->c, g->c_dtype == KP_DTYPE_F32 ? 4 : 2))
+        return KP_ERR_INVALID_ARG;
+    if (g->lda % 8 != 0 || g->ldb % 8 != 0 || g->ldb < g->k || g->ldc < 1) return KP_ERR_INVALID_ARG;
+    if (g->a_batch_off < 0 || g->b_batch_off < 0 || g->c_batch_off < 0) return KP_ERR_INVALID_ARG;
+    if (g->batch > 1 && (g->a_batch_off % 64 != 0 || g->b_batch_off < g->n)) return KP_ERR_INVALID_ARG;
+    // every batch's K slice inside A's rows, and TMA row coordinates in int32
+    if (g->a_batch_off * (g->batch - 1) + g->k > g->lda) return KP_ERR_INVALID_ARG;
+    if (g->b_batch_off * (g->batch - 1) + g->n > INT32_MAX || g->m > INT32_MAX - 128) return KP_ERR_UNSUPPORTED;
+    if (g->ldc < g->c_batch_off * (g->batch - 1) + g->n) return KP_ERR_INVALID_ARG;
+    return KP_OK;
+}
+
+kp_gemm_args gemm_args(int m, int n, int k, int batch, const uint16_t *a, int64_t lda, int64_t a_off,
+                       const uint16_t *b, int64_t ldb, int64_t b_off, void *c, int64_t ldc, int64_t c_off,
+                       int32_t c_dtype, int32_t wait_limit_us, int32_t *d_status) {
+    kp_gemm_args g;
+    std::memset(&g, 0, sizeof g);
+    g.m = m;
+    g.n = n;
+    g.k = k;
+    g.batch = batch;
+    g.a = a;
+    g.lda = lda;
+    g.a_batch_off = a_off;
+    g.b = b;
+    g.ldb = ldb;
+    g.b_batch_off = b_off;
+    g.c = c;
+    g.ldc = ldc;
+    g.c_batch_off = c_off;
+    g.c_dtype = c_dtype;
+    g.wait_limit_us = wait_limit_us;
+    g.d_status = d_status;
+    return g;
+}
+
+kp_status run_gemms(const kp_gemm_args *gs, int n, cudaStream_t s) {
+    for (int i = 0; i < n; ++i) {
+        const kp_status st = validate_gemm(&gs[i]);
+        if (st != KP_OK) return st;
+    }
+    for (int i = 0; i < n; ++i) {
+        const kp_status st = launch_gemm(gs[i], s);
+        if (st != KP_OK) return st;
+    }
+    return KP_OK;
+}
+}  // namespace
+
+kp_status kp_gemm_bf16(const kp_gemm_args *g, kp_stream_t stream) {
+    const kp_status st = validate_gemm(g);
+    if (st != KP_OK || g->m == 0 || g->n == 0) return st;
+    return launch_gemm(*g, reinterpret_cast<cudaStream_t>(stream));
+}
+
+kp_status kp_indexer_project(const kp_indexer_project_args *a, kp_stream_t stream) {
+    if (!a || a->num_tokens < 0) return KP_ERR_INVALID_ARG;
+    if (a->num_tokens == 0) return KP_OK;
+    const int T = a->num_tokens;
+    const kp_gemm_args gs[4] = {
+        gemm_args(T, KP_INDEX_HEADS * KP_INDEX_DIM, KP_Q_LORA, 1, a->q_lora, KP_Q_LORA, 0, a->w_iq, KP_Q_LORA, 0,
+                  a->q_idx, KP_INDEX_HEADS * KP_INDEX_DIM, 0, KP_DTYPE_BF16, a->wait_limit_us, a->d_status),
+        gemm_args(T, KP_INDEX_DIM, KP_HIDDEN, 1, a->hidden, KP_HIDDEN, 0, a->w_ik, KP_HIDDEN, 0, a->keys,
+                  KP_INDEX_DIM, 0, KP_DTYPE_BF16, a->wait_limit_us, a->d_status),
+        gemm_args(T, KP_INDEX_DIM, KP_HIDDEN, 1, a->hidden, KP_HIDDEN, 0, a->w_ig, KP_HIDDEN, 0, a->gates,
+                  KP_INDEX_DIM, 0, KP_DTYPE_BF16, a->wait_limit_us, a->d_status),
+        gemm_args(T, KP_INDEX_HEADS, KP_HIDDEN, 1, a->hidden, KP_HIDDEN, 0, a->w_iw, KP_HIDDEN, 0, a->w,
+                  KP_INDEX_HEADS, 0, KP_DTYPE_F32, a->wait_limit_us, a->d_status)};
+    return run_gemms(gs, 4, reinterpret_cast<cudaStream_t>(stream));
+}
+
+kp_status kp_mla_absorb_q(const kp_mla_absorb_q_args *a, kp_stream_t stream) {
+    if (!a || a->num_tokens < 0) return KP_ERR_INVALID_ARG;
+    if (a->num_tokens == 0) return KP_OK;
+    // batch = head: A = q_nope [T][64 * 256] (head h at column 256 h), B = W_UK
+    // [64 * 512][256] (head h at row 512 h), C = q_lat [T][64 * 576] (head h at column 576 h)
+    const kp_gemm_args g = gemm_args(a->num_tokens, KP_NOPE_DIM, KP_QK_NOPE, KP_MLA_HEADS, a->q_nope,
+                                     KP_MLA_HEADS * KP_QK_NOPE, KP_QK_NOPE, a->w_uk, KP_QK_NOPE, KP_NOPE_DIM,
+                                     a->q_lat, KP_MLA_HEADS * KP_LATENT_DIM, KP_LATENT_DIM, KP_DTYPE_BF16,
+                                     a->wait_limit_us, a->d_status);
+    return run_gemms(&g, 1, reinterpret_cast<cudaStream_t>(stream));
+}
+
+kp_status kp_mla_absorb_out(const kp_mla_absorb_out_args *a, kp_stream_t stream) {
+    if (!a || a->num_tokens < 0) return KP_ERR_INVALID_ARG;
+    if (a->num_tokens == 0) return KP_OK;
+    const int T = a->num_tokens;
+    const kp_gemm_args gs[2] = {
+        // batch = head: A = out [T][64 * 512], B = W_UV [64 * 256][512], C = o [T][64 * 256]
+        gemm_args(T, KP_V_HEAD, KP_NOPE_DIM, KP_MLA_HEADS, a->out, KP_MLA_HEADS * KP_NOPE_DIM, KP_NOPE_DIM, a->w_uv,
+                  KP_NOPE_DIM, KP_V_HEAD, a->o, KP_MLA_HEADS * KP_V_HEAD, KP_V_HEAD, KP_DTYPE_BF16,
+                  a->wait_limit_us, a->d_status),
+        // o_proj: A = o [T][16384], B = W_O [4096][16384], C = hidden_out [T][4096]
+        gemm_args(T, KP_HIDDEN, KP_MLA_HEADS * KP_V_HEAD, 1, a->o, KP_MLA_HEADS * KP_V_HEAD, 0, a->w_o,
+                  KP_MLA_HEADS * KP_V_HEAD, 0, a->hidden_out, KP_HIDDEN, 0, KP_DTYPE_BF16, a->wait_limit_us,
+                  a->d_status)};
+    return run_gemms(gs, 2, reinterpret_cast<cudaStream_t>(stream));
+}
+
 const char *kp_status_string(kp_status s) {
     switch (s) {
         case KP_OK: return "ok";

@@ -1,0 +1,308 @@
+// gemm.cu -- bf16 GEMM on tcgen05 tensor cores for the steps either side of
+// the DSA step: the lightning indexer's projections from the hidden state
+// and the MLA absorption of W_UK into the query and of W_UV / o_proj out of
+// the latent output (MAX docs, max.pipelines.architectures.glm5_next:
+// Glm5NextConfig q_lora_rank, kv_lora_rank, qk_nope_head_dim, v_head_dim,
+// index_n_heads, index_head_dim; llm-atlas GLM-5.3-Flash card, raw config:
+// hidden_size 4096, q_lora_rank 1536, qk_nope_head_dim 256).
+//
+//   C[b][m][n] = sum_k A[b][m][k] * B[b][n][k]      (bf16 in, fp32 accumulate)
+//
+// Batch b selects a column block of A (A's row holds every batch's K slice
+// side by side, as a per-head query [T][heads * dim] does), a row block of B
+// (B holds every batch's [N][K] weight one after another) and a column block
+// of C.  Output bf16 (round to nearest even) or fp32.
+//
+// B300 design: persistent CTAs, one per SM, over (batch, 128-row tile,
+// BN-column tile) units.  Warp 0 streams 64-wide K slices of A (128 x 64) and
+// B (BN x 64) by TMA with 128-byte swizzle into a 4-stage ring; warp 1 issues
+// tcgen05.mma (M 128, N = BN <= 256, K 16) into one of two TMEM accumulators,
+// so the epilogue of one unit overlaps the MMAs of the next; warps 2-9 read
+// the accumulator back with tcgen05.ld (two warps per TMEM lane quadrant,
+// splitting the 32-column chunks) and store converted rows.
+#include <cuda.h>
+
+#include "kp_common.cuh"
+#include "kp_internal.h"
+
+namespace kp {
+
+namespace {
+
+constexpr int kGmM = 128;                       // rows per tile (MMA M)
+constexpr int kGmMaxN = 256;                    // columns per tile (MMA N max)
+constexpr int kGmK = 64;                        // K per stage: one 128-byte swizzle row of bf16
+constexpr int kGmStages = 4;
+constexpr int kGmABytes = kGmM * 128;           // 16 KB
+constexpr int kGmBBytes = kGmMaxN * 128;        // 32 KB
+constexpr int kGmStageBytes = kGmABytes + kGmBBytes;
+constexpr int kGmEpiThreads = 256;
+constexpr int kGmThreads = 64 + kGmEpiThreads;
+constexpr int kGmNumBars = 2 * kGmStages + 4 + 1;
+constexpr int kGmSmemBytes = kGmStages * kGmStageBytes + kGmNumBars * 8 + 1024;
+
+struct GemmParams {
+    int m, n, k, batch;
+    int bn;                      // columns per tile (multiple of 32, <= 256)
+    int m_tiles, n_tiles;
+    int64_t a_batch_off;         // A columns between batches
+    int64_t b_batch_off;         // B rows between batches
+    void *c;
+    int64_t ldc, c_batch_off;    // C row pitch and columns between batches (elements)
+    int c_f32;                   // 1: fp32 output, 0: bf16
+    unsigned long long wait_ns;
+    int32_t *status;
+};
+
+__device__ __forceinline__ bool gm_epi_bar_all(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.and.pred p, 1, 256, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(v))
+        : "memory");
+    return r != 0;
+}
+
+// Stores columns col0 .. col0 + 31 (clipped to n) of one row of batch b.
+__device__ __forceinline__ void store_row_chunk(const GemmParams &P, int b, int row, int col0,
+                                                const uint32_t (&r)[32]) {
+    const int64_t off = static_cast<int64_t>(row) * P.ldc + b * P.c_batch_off + col0;
+    const int ncol = min(32, P.n - col0);
+    if (P.c_f32) {
+        float *c = static_cast<float *>(P.c) + off;
+        if (ncol == 32 && (reinterpret_cast<uintptr_t>(c) & 15) == 0) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+                *reinterpret_cast<float4 *>(c + j) = make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
+                                                                 __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (j < ncol) c[j] = __uint_as_float(r[j]);
+        }
+    } else {
+        uint16_t *c = static_cast<uint16_t *>(P.c) + off;
+        if (ncol == 32 && (reinterpret_cast<uintptr_t>(c) & 15) == 0) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 8)
+                *reinterpret_cast<uint4 *>(c + j) =
+                    make_uint4(pack_bf16x2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])),
+                               pack_bf16x2(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3])),
+                               pack_bf16x2(__uint_as_float(r[j + 4]), __uint_as_float(r[j + 5])),
+                               pack_bf16x2(__uint_as_float(r[j + 6]), __uint_as_float(r[j + 7])));
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (j < ncol) c[j] = static_cast<uint16_t>(pack_bf16x2(__uint_as_float(r[j]), 0.f) & 0xffffu);
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kGmThreads, 1)
+    gemm_bf16_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                     GemmParams P) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ uint32_t tmem_base_s;
+    __shared__ int abort_s;
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    const uint32_t s0 = smem_u32(smem);
+    const uint32_t bar0 = s0 + kGmStages * kGmStageBytes;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (kGmStages + s); };
+    auto accf_bar = [&](int a) { return bar0 + 8u * (2 * kGmStages + a); };
+    auto acce_bar = [&](int a) { return bar0 + 8u * (2 * kGmStages + 2 + a); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * kGmStages + 4);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kGmStages; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(accf_bar(a), 1);
+            mbar_init(acce_bar(a), kGmEpiThreads);
+        }
+        mbar_init(drain_bar, 1);
+        fence_mbar_init();
+        abort_s = 0;
+        tma_prefetch_desc(&tm_a);
+        tma_prefetch_desc(&tm_b);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&tmem_base_s), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    pdl_wait_then_release();
+    const uint32_t tmem = tmem_base_s;
+    volatile int *abort_flag = &abort_s;
+    const int units = P.batch * P.m_tiles * P.n_tiles;
+    const int k_steps = P.k / kGmK;
+    // unit u: batch, then column tile, then row tile (row tiles of one column
+    // tile run on neighbouring CTAs and share the B tile in L2)
+    auto decode = [&](int u, int &b, int &mt, int &nt) {
+        mt = u % P.m_tiles;
+        const int r = u / P.m_tiles;
+        nt = r % P.n_tiles;
+        b = r / P.n_tiles;
+    };
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int stage = 0, a_phase[kGmStages];
+            uint32_t phase = 0;
+            for (int i = 0; i < kGmStages; ++i) a_phase[i] = -1;
+            bool ok = true;
+            const uint32_t bytes = kGmABytes + static_cast<uint32_t>(P.bn) * 128u;
+            for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+                int b, mt, nt;
+                decode(u, b, mt, nt);
+                const int ya = mt * kGmM;
+                const int yb = static_cast<int>(b * P.b_batch_off) + nt * P.bn;
+                for (int ks = 0; ks < k_steps; ++ks) {
+                    if (!mbar_wait(empty_bar(stage), phase ^ 1, abort_flag, P.status, P.wait_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t dst = s0 + stage * kGmStageBytes;
+                    mbar_expect_tx(full_bar(stage), bytes);
+                    tma_load_2d(dst, &tm_a, full_bar(stage), static_cast<int>(b * P.a_batch_off) + ks * kGmK, ya);
+                    tma_load_2d(dst + kGmABytes, &tm_b, full_bar(stage), ks * kGmK, yb);
+                    a_phase[stage] = static_cast<int>(phase);
+                    if (++stage == kGmStages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            if (!ok)  // gave up: every load issued lands before the CTA goes away
+                for (int i = 0; i < kGmStages; ++i)
+                    if (a_phase[i] >= 0) mbar_wait(full_bar(i), static_cast<uint32_t>(a_phase[i]), nullptr, P.status);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            int stage = 0, acc = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            const uint32_t idesc = idesc_bf16_f32(kGmM, P.bn);
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+                if (!(ok = mbar_wait(acce_bar(acc), acc_phase ^ 1, abort_flag, P.status, P.wait_ns))) break;
+                const uint32_t d_tmem = tmem + acc * kGmMaxN;
+                for (int ks = 0; ks < k_steps; ++ks) {
+                    if (!(ok = mbar_wait(full_bar(stage), phase, abort_flag, P.status, P.wait_ns))) break;
+                    tc_fence_after();
+                    const uint32_t a_base = s0 + stage * kGmStageBytes;
+#pragma unroll
+                    for (int kk = 0; kk < kGmK / 16; ++kk) {
+                        const uint64_t ad = desc_kmajor_sw128(a_base + kk * 32);
+                        const uint64_t bd = desc_kmajor_sw128(a_base + kGmABytes + kk * 32);
+                        tc_mma_bf16(d_tmem, ad, bd, idesc, (ks | kk) ? 1u : 0u);
+                    }
+                    tc_commit(empty_bar(stage));
+                    if (++stage == kGmStages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok) break;
+                tc_commit(accf_bar(acc));
+                if (++acc == 2) {
+                    acc = 0;
+                    acc_phase ^= 1;
+                }
+            }
+            if (!ok) {  // gave up: every MMA issued completes before the TMEM is freed
+                tc_commit(drain_bar);
+                mbar_wait(drain_bar, 0, nullptr, P.status);
+            }
+        }
+    } else {
+        // Epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 (its tile rows);
+        // the two warps of a lane quadrant take alternate 32-column chunks.
+        const int quad = warp & 3, et = threadIdx.x - 64, half = et >> 7;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int u = blockIdx.x; u < units; u += gridDim.x) {
+            int b, mt, nt;
+            decode(u, b, mt, nt);
+            if (!gm_epi_bar_all(mbar_wait(accf_bar(acc), acc_phase, abort_flag, P.status, P.wait_ns))) break;
+            tc_fence_after();
+            const int row = mt * kGmM + quad * 32 + lane;
+            const uint32_t tbase = tmem + acc * kGmMaxN + (static_cast<uint32_t>(quad * 32) << 16);
+            for (int ch = half; ch < P.bn / 32; ch += 2) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(tbase + ch * 32, r);
+                tmem_ld_wait();
+                const int col0 = nt * P.bn + ch * 32;  // column inside the batch
+                if (row < P.m && col0 < P.n) store_row_chunk(P, b, row, col0, r);
+            }
+            tc_fence_before();
+            mbar_arrive(acce_bar(acc));
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+}  // namespace
+
+kp_status launch_gemm(const kp_gemm_args &g, cudaStream_t s) {
+    if (g.m == 0 || g.n == 0) return KP_OK;
+    const int sms = device_sm_count();
+    if (sms <= 0) return KP_ERR_CUDA;
+    // Columns per tile: the whole batch's N when it fits, else 256; a multiple of 32.
+    int bn = ((g.n + 31) / 32) * 32;
+    if (bn > kGmMaxN) bn = kGmMaxN;
+    CUtensorMap tm_a, tm_b;
+    const uint64_t a_cols = static_cast<uint64_t>(g.a_batch_off) * (g.batch - 1) + g.k;
+    const uint64_t b_rows = static_cast<uint64_t>(g.b_batch_off) * (g.batch - 1) + g.n;
+    if (!make_tmap_bf16_sw128(&tm_a, g.a, a_cols, static_cast<uint64_t>(g.m), static_cast<uint64_t>(g.lda) * 2,
+                              kGmK, kGmM) ||
+        !make_tmap_bf16_sw128(&tm_b, g.b, static_cast<uint64_t>(g.k), b_rows, static_cast<uint64_t>(g.ldb) * 2, kGmK,
+                              static_cast<uint32_t>(bn)))
+        return KP_ERR_CUDA;
+    cudaError_t e = cudaFuncSetAttribute(gemm_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGmSmemBytes);
+    if (e != cudaSuccess) {
+        record_cuda_error("cudaFuncSetAttribute(gemm_bf16_kernel)", e);
+        return KP_ERR_CUDA;
+    }
+    GemmParams P;
+    P.m = g.m;
+    P.n = g.n;
+    P.k = g.k;
+    P.batch = g.batch;
+    P.bn = bn;
+    P.m_tiles = (g.m + kGmM - 1) / kGmM;
+    P.n_tiles = (g.n + bn - 1) / bn;
+    P.a_batch_off = g.a_batch_off;
+    P.b_batch_off = g.b_batch_off;
+    P.c = g.c;
+    P.ldc = g.ldc;
+    P.c_batch_off = g.c_batch_off;
+    P.c_f32 = g.c_dtype == KP_DTYPE_F32 ? 1 : 0;
+    P.wait_ns = wait_limit_ns(g.wait_limit_us);
+    P.status = g.d_status;
+    const int64_t units = static_cast<int64_t>(g.batch) * P.m_tiles * P.n_tiles;
+    const int grid = static_cast<int>(units < sms ? units : sms);
+    return launch_kernel("gemm_bf16_kernel", gemm_bf16_kernel, LaunchCfg(dim3(grid), dim3(kGmThreads), kGmSmemBytes, s),
+                         tm_a, tm_b, P);
+}
+
+}  // namespace kp

@@ -105,6 +105,7 @@ kp_status launch_topk(const kp_topk_args &a, cudaStream_t s);
 // kp_indexer_score with its plan always in the caller's workspace (validated).
 kp_status score_with_workspace_plan(const kp_score_args *a, cudaStream_t stream);
 kp_status launch_attend(const kp_attend_args &a, cudaStream_t s);
+kp_status launch_gemm(const kp_gemm_args &g, cudaStream_t s);
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 

@@ -301,6 +301,99 @@ KP_API kp_status kp_topk_select(const kp_topk_args *args, kp_stream_t stream);
 KP_API kp_status kp_sparse_mla_attend(const kp_attend_args *args, kp_stream_t stream);
 KP_API kp_status kp_dsa_forward(const kp_forward_args *args, kp_stream_t stream);
 
+/* ---- the steps either side: projections and MLA absorption ----
+ * Dense bf16 products around the DSA step, with the GLM-5.3-Flash widths
+ * (llm-atlas GLM-5.3-Flash card, raw config: hidden_size 4096, q_lora_rank
+ * 1536, qk_nope_head_dim 256, kv_lora_rank 512, num_attention_heads 64,
+ * index_n_heads 32, index_head_dim 128; v_head_dim 256 from the NeMo
+ * AutoModel Glm5NextTextConfig defaults).  fp32 accumulation; bf16 outputs
+ * are rounded to nearest even. */
+enum {
+    KP_HIDDEN = 4096,       /* hidden size */
+    KP_Q_LORA = 1536,       /* compressed query width (q_lora_rank) */
+    KP_QK_NOPE = 256,       /* per-head query / key width (qk_nope_head_dim) */
+    KP_V_HEAD = 256         /* per-head value width (v_head_dim) */
+};
+enum { KP_DTYPE_BF16 = 0, KP_DTYPE_F32 = 1 };
+
+/* C[b][m][n] = sum_k A[b][m][k] * B[b][n][k] for b < batch (both operands
+ * K-contiguous, "A times B transposed").  Batch b reads columns
+ * b * a_batch_off .. + k - 1 of A's rows, rows b * b_batch_off .. + n - 1 of
+ * B, and writes columns b * c_batch_off .. + n - 1 of C's rows. */
+typedef struct kp_gemm_args {
+    int32_t m, n, k;              /* host: per-batch sizes; m, n >= 0, k a positive multiple of 64 */
+    int32_t batch;                /* host: >= 1 */
+    const uint16_t *a;            /* bf16, row r at a + r * lda (16-byte aligned) */
+    int64_t lda, a_batch_off;     /* host: elements; lda a multiple of 8 */
+    const uint16_t *b;            /* bf16, row r at b + r * ldb (16-byte aligned) */
+    int64_t ldb, b_batch_off;     /* host: elements; ldb a multiple of 8, >= k */
+    void *c;                      /* bf16 or fp32, row r of batch b at c + r * ldc + b * c_batch_off */
+    int64_t ldc, c_batch_off;     /* host: elements */
+    int32_t c_dtype;              /* KP_DTYPE_BF16 or KP_DTYPE_F32 */
+    int32_t wait_limit_us;        /* as kp_config.wait_limit_us */
+    int32_t *d_status;            /* optional */
+} kp_gemm_args;
+
+/* The lightning indexer's inputs from a layer's hidden state, for T tokens
+ * (DeepSeek-V3.2 lineage of Glm5NextConfig; the gate feeds the pooled-key
+ * compression, index_kpool_compress):
+ *   q_idx[t] = W_iq . q_lora[t]      [T][32][128] bf16   (W_iq  [32 * 128][1536])
+ *   keys[t]  = W_ik . hidden[t]      [T][128] bf16       (W_ik  [128][4096])
+ *   gates[t] = W_ig . hidden[t]      [T][128] bf16       (W_ig  [128][4096])
+ *   w[t]     = W_iw . hidden[t]      [T][32] fp32        (W_iw  [32][4096])
+ * Any scale of the score is folded into W_iw.  Weights are row-major [out][in]
+ * bf16. */
+typedef struct kp_indexer_project_args {
+    int32_t num_tokens;           /* host: T >= 0 */
+    const uint16_t *hidden;       /* [T][4096] */
+    const uint16_t *q_lora;       /* [T][1536] */
+    const uint16_t *w_iq, *w_ik, *w_ig, *w_iw;
+    uint16_t *q_idx;              /* [T][32][128] out */
+    uint16_t *keys;               /* [T][128] out */
+    uint16_t *gates;              /* [T][128] out */
+    float *w;                     /* [T][32] out */
+    int32_t wait_limit_us;
+    int32_t *d_status;
+} kp_indexer_project_args;
+
+/* Absorbed query: the key up-projection W_UK folded into the query, so the
+ * attention runs on the latent cache (MAX docs Glm5NextConfig mla_use_nope,
+ * kv_lora_rank; the cache stores the latent width):
+ *   q_lat[t][h][c] = sum_d W_UK[h][c][d] * q_nope[t][h][d],  c < 512
+ * q_nope [T][64][256] bf16, W_UK [64][512][256] bf16, q_lat [T][64][576] bf16
+ * (columns 512..575 are left as they are: the attention does not read them). */
+typedef struct kp_mla_absorb_q_args {
+    int32_t num_tokens;
+    const uint16_t *q_nope;
+    const uint16_t *w_uk;
+    uint16_t *q_lat;
+    int32_t wait_limit_us;
+    int32_t *d_status;
+} kp_mla_absorb_q_args;
+
+/* Output side: the value up-projection W_UV applied to the latent-space
+ * attention output, then o_proj:
+ *   o[t][h][v]      = sum_c W_UV[h][v][c] * out[t][h][c]       v < 256 (bf16)
+ *   hidden_out[t]   = W_O . o[t]                               [T][4096] bf16
+ * out [T][64][512] bf16 (kp_sparse_mla_attend's output), W_UV [64][256][512]
+ * bf16, W_O [4096][64 * 256] bf16; o [T][64][256] bf16 is a caller buffer
+ * (also an output). */
+typedef struct kp_mla_absorb_out_args {
+    int32_t num_tokens;
+    const uint16_t *out;
+    const uint16_t *w_uv;
+    const uint16_t *w_o;
+    uint16_t *o;
+    uint16_t *hidden_out;
+    int32_t wait_limit_us;
+    int32_t *d_status;
+} kp_mla_absorb_out_args;
+
+KP_API kp_status kp_gemm_bf16(const kp_gemm_args *args, kp_stream_t stream);
+KP_API kp_status kp_indexer_project(const kp_indexer_project_args *args, kp_stream_t stream);
+KP_API kp_status kp_mla_absorb_q(const kp_mla_absorb_q_args *args, kp_stream_t stream);
+KP_API kp_status kp_mla_absorb_out(const kp_mla_absorb_out_args *args, kp_stream_t stream);
+
 /* ---- scoring without a caller workspace ----
  * The pages describe no such call: it exists for callers that cannot
  * allocate device memory when they score (a host framework whose allocator

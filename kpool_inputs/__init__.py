@@ -218,3 +218,50 @@ def bits(t: torch.Tensor) -> np.ndarray:
     """Raw 16-bit patterns of a CPU bf16 tensor as numpy uint16 (no copy of values' meaning)."""
     assert t.dtype == torch.bfloat16
     return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+# ---------------------------------------------------------------- the steps either side
+
+HIDDEN = 4096
+Q_LORA = 1536
+QK_NOPE = 256
+V_HEAD = 256
+
+
+@dataclasses.dataclass
+class Projections:
+    """Random-weight inputs of the dense steps around the DSA step, for T tokens.
+
+    Activations ~ N(0, 1); every weight ~ N(0, 1) / sqrt(fan_in), times the
+    width the DSA step's own synthetic inputs use for that output (so the
+    projected q_idx, keys, w and q_lat have the distributions of the workloads
+    above).  Weights are stored [out][in]."""
+    hidden: torch.Tensor       # [T, 4096] bf16
+    q_lora: torch.Tensor       # [T, 1536] bf16
+    q_nope: torch.Tensor       # [T, 64, 256] bf16
+    out_lat: torch.Tensor      # [T, 64, 512] bf16 (a stand-in attention output)
+    w_iq: torch.Tensor         # [32 * 128, 1536]
+    w_ik: torch.Tensor         # [128, 4096]
+    w_ig: torch.Tensor         # [128, 4096]
+    w_iw: torch.Tensor         # [32, 4096]
+    w_uk: torch.Tensor         # [64, 512, 256]
+    w_uv: torch.Tensor         # [64, 256, 512]
+    w_o: torch.Tensor          # [4096, 64 * 256]
+
+
+def make_projections(T: int, seed: int = 5, heads: int = MLA_HEADS) -> Projections:
+    sd = 1000 + seed
+    r = lambda tag, shape, std: _randn(sd, tag, shape, std)  # noqa: E731
+    return Projections(
+        hidden=r(1, (T, HIDDEN), 1.0),
+        q_lora=r(2, (T, Q_LORA), 1.0),
+        q_nope=r(3, (T, heads, QK_NOPE), 1.0),
+        out_lat=r(4, (T, heads, NOPE_DIM), 1.0 / math.sqrt(NOPE_DIM)),
+        w_iq=r(5, (INDEX_HEADS * INDEX_DIM, Q_LORA), 1.0 / math.sqrt(Q_LORA) / math.sqrt(INDEX_DIM)),
+        w_ik=r(6, (INDEX_DIM, HIDDEN), 1.0 / math.sqrt(HIDDEN) / math.sqrt(INDEX_DIM)),
+        w_ig=r(7, (INDEX_DIM, HIDDEN), 1.0 / math.sqrt(HIDDEN)),
+        w_iw=r(8, (INDEX_HEADS, HIDDEN), 1.0 / math.sqrt(HIDDEN) / math.sqrt(INDEX_HEADS)),
+        w_uk=r(9, (heads, NOPE_DIM, QK_NOPE), 1.0 / math.sqrt(QK_NOPE) / math.sqrt(LATENT_DIM)),
+        w_uv=r(10, (heads, V_HEAD, NOPE_DIM), 1.0 / math.sqrt(NOPE_DIM)),
+        w_o=r(11, (HIDDEN, heads * V_HEAD), 1.0 / math.sqrt(heads * V_HEAD)),
+    )

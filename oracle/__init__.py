@@ -67,6 +67,8 @@ def lib():
                 i32, i32, i32, P, P, dbl,
                 P, i64, P, P, P, P, i32]
             L.oracle_dsa_queries.restype = None
+            L.oracle_linear.argtypes = [i64, i64, i64, P, i64, P, i64, P, i64, P, i32]
+            L.oracle_linear.restype = None
             L.oracle_has_openmp.argtypes = []
             L.oracle_has_openmp.restype = i32
             _lib = L
@@ -197,3 +199,66 @@ def dsa_queries(q_seq, q_pos, pool_row_off, latent_row_off, kpool, k_pools,
 
 def has_openmp() -> bool:
     return bool(lib().oracle_has_openmp())
+
+
+# ---------------------------------------------------------------- the steps either side
+
+def linear(a, b, with_abs: bool = False, threads: int = 0):
+    """out[i, j] = sum_k a[i, k] * b[j, k] in float64 for bf16 bit arrays a [m, k]
+    and b [n, k] (a linear layer with weights stored [out][in]).  With
+    with_abs, also returns sum_k |a[i, k] b[j, k]|."""
+    a, pa = _c(a, np.uint16)
+    b, pb = _c(b, np.uint16)
+    m, k = a.shape
+    n, kb = b.shape
+    assert kb == k
+    out = np.zeros((m, n), np.float64)
+    ab = np.zeros((m, n), np.float64) if with_abs else None
+    lib().oracle_linear(m, n, k, pa, k, pb, k, out.ctypes.data_as(ctypes.c_void_p), n,
+                        ab.ctypes.data_as(ctypes.c_void_p) if ab is not None else None,
+                        int(threads or (os.cpu_count() or 1)))
+    return (out, ab) if with_abs else out
+
+
+def indexer_project(hidden, q_lora, w_iq, w_ik, w_ig, w_iw, with_abs: bool = False):
+    """The lightning indexer's inputs from the hidden state (linear layers):
+    q_idx = W_iq q_lora [T, 32, 128]; keys = W_ik h; gates = W_ig h; w = W_iw h.
+    Returns float64 arrays (and the |.| sums per output with with_abs)."""
+    T = hidden.shape[0]
+    res = {}
+    for name, (x, W) in {"q_idx": (q_lora, w_iq), "keys": (hidden, w_ik), "gates": (hidden, w_ig),
+                         "w": (hidden, w_iw)}.items():
+        res[name] = linear(x, W, with_abs)
+    if with_abs:
+        out = {k: v[0] for k, v in res.items()}
+        ab = {k: v[1] for k, v in res.items()}
+        out["q_idx"] = out["q_idx"].reshape(T, 32, 128)
+        ab["q_idx"] = ab["q_idx"].reshape(T, 32, 128)
+        return out, ab
+    res["q_idx"] = res["q_idx"].reshape(T, 32, 128)
+    return res
+
+
+def mla_absorb_q(q_nope, w_uk, with_abs: bool = False):
+    """Absorbed query per head: q_lat[t, h, c] = sum_d W_UK[h, c, d] q_nope[t, h, d]
+    (q_nope [T, H, 256], W_UK [H, 512, 256] bf16 bits) -> float64 [T, H, 512]."""
+    T, H, _ = q_nope.shape
+    outs, abss = [], []
+    for h in range(H):
+        r = linear(q_nope[:, h, :], w_uk[h], with_abs)
+        outs.append(r[0] if with_abs else r)
+        if with_abs:
+            abss.append(r[1])
+    out = np.stack(outs, axis=1)
+    return (out, np.stack(abss, axis=1)) if with_abs else out
+
+
+def mla_absorb_out_o(out_lat, w_uv, with_abs: bool = False):
+    """Value up-projection per head: o[t, h, v] = sum_c W_UV[h, v, c] out[t, h, c]
+    (out [T, H, 512], W_UV [H, 256, 512] bf16 bits) -> float64 [T, H, 256]."""
+    return mla_absorb_q(out_lat, w_uv, with_abs)
+
+
+def o_proj(o, w_o, with_abs: bool = False):
+    """hidden_out[t] = W_O o[t] (o [T, H * 256] bf16 bits, W_O [4096, H * 256])."""
+    return linear(o.reshape(o.shape[0], -1), w_o, with_abs)

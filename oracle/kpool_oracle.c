@@ -298,6 +298,38 @@ void oracle_dsa_queries(int nq, const int32_t *q_seq, const int32_t *q_pos,
     }
 }
 
+/* ---- the steps either side: dense products ---------------------------
+ * out[i][j] = sum_k a[i][k] * b[j][k] in double (bf16 inputs widened
+ * exactly), the plain definition of a linear layer y = W x with W stored
+ * [out][in].  Used for the indexer projections from the hidden state
+ * (q_idx, keys, gates, w), the absorbed query q_lat[h] = W_UK[h]^T q_nope[h]
+ * and the output side (W_UV per head, then o_proj).  When abs_out is given,
+ * it receives sum_k |a[i][k] * b[j][k]| (for error bounds of the GPU's fp32
+ * accumulation). */
+void oracle_linear(int64_t m, int64_t n, int64_t k, const uint16_t *a, int64_t lda, const uint16_t *b,
+                   int64_t ldb, double *out, int64_t ldo, double *abs_out, int threads) {
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1) num_threads(threads > 0 ? threads : 1)
+#endif
+    for (int64_t i = 0; i < m; ++i) {
+        double *arow = (double *)malloc(sizeof(double) * (size_t)k);
+        for (int64_t kk = 0; kk < k; ++kk) arow[kk] = oracle_bf16_to_double(a[i * lda + kk]);
+        for (int64_t j = 0; j < n; ++j) {
+            double acc = 0.0, aacc = 0.0;
+            const uint16_t *brow = b + j * ldb;
+            for (int64_t kk = 0; kk < k; ++kk) {
+                const double pr = arow[kk] * oracle_bf16_to_double(brow[kk]);
+                acc += pr;
+                aacc += fabs(pr);
+            }
+            out[i * ldo + j] = acc;
+            if (abs_out) abs_out[i * ldo + j] = aacc;
+        }
+        free(arow);
+    }
+    (void)threads;
+}
+
 /* Reports whether the library was built with OpenMP (threads it can use). */
 int oracle_has_openmp(void) {
 #ifdef _OPENMP
