@@ -17,7 +17,7 @@ thread_local std::string g_last_error;
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 kp_status check_config(const kp_config &c) {
-    if (c.kpool != kKpool) return KP_ERR_UNSUPPORTED;
+    if (c.kpool != 4 && c.kpool != 16) return KP_ERR_UNSUPPORTED;
     if (c.topk_tokens <= 0 || c.topk_tokens % c.kpool != 0) return KP_ERR_INVALID_ARG;
     if (c.topk_tokens / c.kpool > KP_MAX_TOPK_POOLS) return KP_ERR_UNSUPPORTED;
     if (c.compress_mode != KP_COMPRESS_LEARNED && c.compress_mode != KP_COMPRESS_MEAN)
@@ -41,10 +41,11 @@ kp_status check_queries(const kp_queries &q) {
 bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
 
 // Layout checks: latent / pooled say which cache the call reads or writes.
-// Paged mode: page_tokens a power of two in 16 .. 65536, the latent cache a
-// whole number of at least one page, the pooled cache as many pages of
-// page_tokens / kpool rows, and valid page ids that fit a TMA row coordinate.
-kp_status check_seqs(const kp_seqs &s, bool latent, bool pooled, bool need_seq_len = true) {
+// Paged mode: page_tokens a power of two in 16 .. 65536 holding at least 4
+// pools, the latent cache a whole number of at least one page, the pooled
+// cache as many pages of page_tokens / kpool rows, and valid page ids that
+// fit a TMA row coordinate.
+kp_status check_seqs(const kp_seqs &s, int kpool, bool latent, bool pooled, bool need_seq_len = true) {
     if (s.num_seqs < 1 || s.num_seqs > 65535 || (need_seq_len && !s.seq_len)) return KP_ERR_INVALID_ARG;
     if (s.latent_rows <= 0 && (latent || s.block_table)) return KP_ERR_INVALID_ARG;
     if (latent && s.latent_rows >= (int64_t(1) << 40)) return KP_ERR_INVALID_ARG;
@@ -53,11 +54,12 @@ kp_status check_seqs(const kp_seqs &s, bool latent, bool pooled, bool need_seq_l
         if ((latent && !s.latent_row_off) || (pooled && !s.pool_row_off)) return KP_ERR_INVALID_ARG;
         return KP_OK;
     }
-    if (!is_pow2(s.page_tokens) || s.page_tokens < 16 || s.page_tokens > 65536 || s.blocks_per_seq < 1)
+    if (!is_pow2(s.page_tokens) || s.page_tokens < 16 || s.page_tokens > 65536 || s.blocks_per_seq < 1 ||
+        s.page_tokens < 4 * kpool)
         return KP_ERR_INVALID_ARG;
     const int64_t pages = s.latent_rows / s.page_tokens;
     if (pages < 1 || pages > INT32_MAX) return KP_ERR_INVALID_ARG;
-    if (pooled && s.pool_rows < pages * (s.page_tokens / kKpool)) return KP_ERR_INVALID_ARG;
+    if (pooled && s.pool_rows < pages * (s.page_tokens / kpool)) return KP_ERR_INVALID_ARG;
     return KP_OK;
 }
 
@@ -86,8 +88,9 @@ ForwardLayout forward_layout(const kp_forward_args &a, int sm_count) {
 }
 }  // namespace
 
-CacheMap cache_map(const kp_seqs &s) {
+CacheMap cache_map(const kp_seqs &s, int kpool) {
     CacheMap m;
+    m.pool_shift = kpool_shift(kpool);
     m.latent_row_off = s.latent_row_off;
     m.pool_row_off = s.pool_row_off;
     m.block_table = s.block_table;
@@ -186,7 +189,7 @@ kp_status validate_compress(const kp_compress_args *a) {
     if (a->max_new_per_seq == 0 || a->max_new_per_seq > a->num_new) return KP_ERR_INVALID_ARG;
     if (!a->prev_len || !a->new_off || !a->keys || !a->tail_keys || !a->pooled) return KP_ERR_INVALID_ARG;
     if (a->seqs.num_seqs != a->num_seqs) return KP_ERR_INVALID_ARG;
-    const kp_status sst = check_seqs(a->seqs, false, true, false);
+    const kp_status sst = check_seqs(a->seqs, a->cfg.kpool, false, true, false);
     if (sst != KP_OK) return sst;
     if (a->cfg.compress_mode == KP_COMPRESS_LEARNED && (!a->gates || !a->ape || !a->tail_gates))
         return KP_ERR_INVALID_ARG;
@@ -202,7 +205,7 @@ kp_status validate_score(const kp_score_args *a) {
     kp_status st = check_config(a->cfg);
     if (st != KP_OK) return st;
     if ((st = check_queries(a->q)) != KP_OK) return st;
-    if ((st = check_seqs(a->seqs, false, true)) != KP_OK) return st;
+    if ((st = check_seqs(a->seqs, a->cfg.kpool, false, true)) != KP_OK) return st;
     if (a->q.num_queries == 0) return KP_OK;
     if (!a->q_idx || !a->w || !a->pooled || !a->scores) return KP_ERR_INVALID_ARG;
     if (!aligned(a->q_idx, 16) || !aligned(a->pooled, 16) || !aligned(a->w, 4) || !aligned(a->scores, 4))
@@ -237,7 +240,7 @@ kp_status validate_attend(const kp_attend_args *a) {
     kp_status st = check_config(a->cfg);
     if (st != KP_OK) return st;
     if ((st = check_queries(a->q)) != KP_OK) return st;
-    if ((st = check_seqs(a->seqs, true, false)) != KP_OK) return st;
+    if ((st = check_seqs(a->seqs, a->cfg.kpool, true, false)) != KP_OK) return st;
     if (a->q.num_queries == 0) return KP_OK;
     if (!a->q_lat || !a->latent || !a->pool_idx || !a->n_sel || !a->out) return KP_ERR_INVALID_ARG;
     if (!aligned(a->q_lat, 16) || !aligned(a->latent, 16) || !aligned(a->out, 4)) return KP_ERR_INVALID_ARG;
@@ -294,7 +297,7 @@ kp_status kp_dsa_forward(const kp_forward_args *a, kp_stream_t stream) {
     kp_status st = check_config(a->cfg);
     if (st != KP_OK) return st;
     if ((st = check_queries(a->q)) != KP_OK) return st;
-    if ((st = check_seqs(a->seqs, true, true)) != KP_OK) return st;
+    if ((st = check_seqs(a->seqs, a->cfg.kpool, true, true)) != KP_OK) return st;
     if (!a->out) return KP_ERR_INVALID_ARG;
     const int sms = device_sm_count();
     if (sms <= 0) {

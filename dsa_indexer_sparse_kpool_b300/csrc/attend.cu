@@ -75,7 +75,6 @@ constexpr int kAtQBlockBytes = kMlaHeads * 128;           // [64 heads][64 bf16]
 constexpr int kAtQBytes = 8 * kAtQBlockBytes;             // 64 KB
 constexpr int kAtPBytes = kAtTok * kMlaHeads * 2;         // 8 KB per buffer (two buffers)
 constexpr int kAtMaxSplits = 8;
-constexpr int kAtMaxTail = kKpool - 1;
 constexpr int kAtSoftWarps = 8;
 constexpr int kAtSoftThreads = 32 * kAtSoftWarps;
 constexpr int kAtMmaWarp = 8;
@@ -83,9 +82,6 @@ constexpr int kAtProdWarp0 = 9;
 constexpr int kAtProdWarps = 4;                           // TMA gather warps
 constexpr int kAtThreads = 416;
 static_assert(kAtThreads == 32 * (kAtSoftWarps + 1 + kAtProdWarps), "softmax, MMA and gather warps");
-constexpr int kAtPoolsPerTile = kAtTok / kKpool;          // 16 pools of 4 rows
-constexpr int kAtBoxBytes = kKpool * 128;                 // one pool's rows of one 64-column block
-static_assert(kAtPoolsPerTile <= 16, "a gather lane per (pool, block) of a 128-column chunk");
 static_assert(kAtTok % 16 == 0 && kAtTok <= 64, "a tile is whole K-steps of P.V and fits the M = 64 product");
 static_assert(kAtBlockBytes % 1024 == 0, "blocks start on a swizzle atom");
 constexpr int kAtTmemCols = 512;
@@ -112,19 +108,33 @@ constexpr int kNumBars = 4 * kAtSlots * 2 + 9;
 constexpr int kMiscTmem = kMiscBars + kNumBars * 8;
 constexpr int kMiscAbort = kMiscTmem + 4;
 constexpr int kMiscCore = (kMiscAbort + 12 + 15) / 16 * 16;
-// The merge's small buffers, offsets from their base.
-constexpr int kAuxTail = 0;                               // [3][512] bf16 tail rows
-constexpr int kAuxZTail = kAuxTail + kAtMaxTail * kNopeDim * 2;   // [64][4] f32 tail logits
-constexpr int kAuxW = kAuxZTail + 64 * 4 * 4;             // [64][16] f32 merge weights
-constexpr int kAuxLPart = kAuxW + 64 * 16 * 4;            // [4][64] f32 row sums per lane quadrant
-constexpr int kAuxBytes = kAuxLPart + 4 * 64 * 4;
 constexpr int kMrgOBytes = kMlaHeads * kNopeDim * 4;      // [64 heads][512] f32 dump of this CTA's O^T
 static_assert(kMrgOBytes <= kAtSlots * kAtTileBytes, "the O^T dump must fit in the tile slots");
-constexpr bool kAuxInTiles = kMrgOBytes + kAuxBytes <= kAtSlots * kAtTileBytes;
-constexpr int kOffAux = kAuxInTiles ? kOffTile + kMrgOBytes : kOffMisc + kMiscCore;
-constexpr int kMiscBytes = kMiscCore + (kAuxInTiles ? 0 : kAuxBytes);
-constexpr int kAtSmemBytes = kOffMisc + kMiscBytes + 1024;  // + alignment slack
-static_assert(kAtSmemBytes <= 232448, "attention shared memory over the per-CTA limit");
+
+// What depends on the pool size KP (tokens per pool, 4 or 16): a pool is KP
+// consecutive latent rows, gathered as one TMA box of KP rows per 64-column
+// block; the tail holds up to KP - 1 rows.  After the tile loop the tail rows
+// sit in the P buffers' place, and the merge's small buffers after the
+// barriers: tail logits [64][KP], merge weights [64][kWStride] (splits 0..7,
+// tail tokens 8.., 1/L at kWInv) and row-sum partials [4][64].
+template <int KP>
+struct AtPool {
+    static constexpr int kMaxTail = KP - 1;
+    static constexpr int kPoolsPerTile = kAtTok / KP;     // 16 pools of 4 rows, or 4 of 16
+    static constexpr int kBoxBytes = KP * 128;           // one pool's rows of one 64-column block
+    static constexpr int kWInv = 8 + kMaxTail;
+    static constexpr int kWStride = (kWInv + 1 + 15) / 16 * 16;
+    static constexpr int kWF4 = (kWInv + 1 + 3) / 4;     // float4 loads that cover a weight row
+    static constexpr int kZTail = 0;
+    static constexpr int kW = kZTail + kMlaHeads * KP * 4;
+    static constexpr int kLPart = kW + kMlaHeads * kWStride * 4;
+    static constexpr int kAuxBytes = kLPart + 4 * kMlaHeads * 4;
+    static constexpr int kOffAux = kOffMisc + kMiscCore;
+    static constexpr int kSmemBytes = kOffMisc + kMiscCore + kAuxBytes + 1024;  // + alignment slack
+    static_assert(kPoolsPerTile * 2 <= 32, "a gather lane per (pool, block) of a 128-column chunk");
+    static_assert(kMaxTail * kNopeDim * 2 <= 2 * kAtPBytes, "the tail rows fit in the P buffers");
+    static_assert(kSmemBytes <= 232448, "attention shared memory over the per-CTA limit");
+};
 
 // mbarrier indices
 constexpr int kBarFull = 0;                        // [slot][4] chunk gathered (one arrival + TMA bytes)
@@ -201,6 +211,7 @@ __device__ __forceinline__ uint32_t sw128_off(int row, int col) {
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
+template <int KP>
 __global__ void __launch_bounds__(kAtThreads, 1)
     sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_lat,
                          AttendParams P) {
@@ -214,11 +225,15 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     float *mused_s = reinterpret_cast<float *>(misc + kMiscMUsed);
     float *fac_s = reinterpret_cast<float *>(misc + kMiscFac);
     float *lsum_s = reinterpret_cast<float *>(misc + kMiscLSum);
-    uint8_t *aux = smem + kOffAux;  // merge buffers: valid only after the tile loop
-    float *lpart_s = reinterpret_cast<float *>(aux + kAuxLPart);
-    uint16_t *tail_s = reinterpret_cast<uint16_t *>(aux + kAuxTail);
-    float *ztail_s = reinterpret_cast<float *>(aux + kAuxZTail);
-    float *wm_s = reinterpret_cast<float *>(aux + kAuxW);
+    using Pool = AtPool<KP>;
+    constexpr int kAtMaxTail = Pool::kMaxTail;
+    constexpr int kAtPoolsPerTile = Pool::kPoolsPerTile;
+    constexpr int kWS = Pool::kWStride, kWInv = Pool::kWInv;
+    uint8_t *aux = smem + Pool::kOffAux;  // merge buffers: valid only after the tile loop
+    float *lpart_s = reinterpret_cast<float *>(aux + Pool::kLPart);
+    uint16_t *tail_s = reinterpret_cast<uint16_t *>(smem + kOffP);   // the P buffers' place
+    float *ztail_s = reinterpret_cast<float *>(aux + Pool::kZTail);
+    float *wm_s = reinterpret_cast<float *>(aux + Pool::kW);
     const uint32_t bar0 = sbase + kOffMisc + kMiscBars;
     auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
     uint32_t *tmem_s = reinterpret_cast<uint32_t *>(misc + kMiscTmem);
@@ -269,8 +284,8 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     if (qvalid && !paged && (base_row < 0 || base_row + t >= P.cmap.latent_rows)) qvalid = false;
     if (qvalid && paged && (t >> P.cmap.page_shift) >= P.cmap.blocks_per_seq) qvalid = false;
     if (!qvalid && tid == 0) set_status(P.status, KP_ERR_DEVICE_BOUNDS);
-    const int nf = qvalid ? (t + 1) / kKpool : 0;
-    const int n_tail = (qvalid && P.tail) ? (t + 1) - nf * kKpool : 0;
+    const int nf = qvalid ? (t + 1) / KP : 0;
+    const int n_tail = (qvalid && P.tail) ? (t + 1) - nf * KP : 0;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -292,7 +307,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
             ns = max(0, min(ns, ns_max));
         }
     }
-    const int n_pool_tok = ns * kKpool;
+    const int n_pool_tok = ns * KP;
     const int n_tiles = (n_pool_tok + kAtTok - 1) / kAtTok;
     const int tb = n_tiles * split / S, te = n_tiles * (split + 1) / S;
     const int nt = te - tb;
@@ -400,8 +415,8 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         // global read sits between a freed slot and its refill.
         const int w = warp - kAtProdWarp0;
         const int my_chunk = lane >> 3, j = 4 * (lane & 7) + w;
-        const int my_pool = j & 15, blk = 2 * my_chunk + (j >> 4);
-        const bool active = my_pool < kAtPoolsPerTile;
+        const int my_pool = j % kAtPoolsPerTile, blk = 2 * my_chunk + j / kAtPoolsPerTile;
+        const bool active = j < 2 * kAtPoolsPerTile;
         const int pool0 = tb * kAtPoolsPerTile;
         const int npools = min(nt * kAtPoolsPerTile, ns - pool0);
         const int32_t *plist = P.pool_idx + static_cast<int64_t>(q) * P.K + pool0 + my_pool;
@@ -412,25 +427,25 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         auto fetch_pg = [&](int p) -> int {
             if (!paged) return 0;
             if (p < 0 || p >= nf) return -2;
-            const int blk = (p * kKpool) >> P.cmap.page_shift;
+            const int blk = (p * KP) >> P.cmap.page_shift;
             if (blk >= P.cmap.blocks_per_seq) return -2;
             return P.cmap.block_table[static_cast<int64_t>(b) * P.cmap.blocks_per_seq + blk];
         };
         // First row of this lane's pool in tile t, or a coordinate wholly above
         // row 0 (zero fill) for a pool past the end of the list or out of range.
         auto row_at = [&](int t, int p, int pg) -> int {
-            if (!want(t)) return -kKpool;
+            if (!want(t)) return -KP;
             bool good = p >= 0 && p < nf;
             int64_t r = 0;
-            if (good && !paged) r = base_row + static_cast<int64_t>(p) * kKpool;
+            if (good && !paged) r = base_row + static_cast<int64_t>(p) * KP;
             if (good && paged) {
                 good = pg >= 0 && pg < P.cmap.num_pages;
                 r = (static_cast<int64_t>(pg) << P.cmap.page_shift) +
-                    ((p * kKpool) & ((1 << P.cmap.page_shift) - 1));
+                    ((p * KP) & ((1 << P.cmap.page_shift) - 1));
             }
             if (!good) {
                 set_status(P.status, KP_ERR_DEVICE_BOUNDS);
-                return -kKpool;
+                return -KP;
             }
             return static_cast<int>(r);
         };
@@ -453,7 +468,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
                 const int y = row_at(jj, pf_p[u], pf_pg[u]);
                 pf_pg[u ^ 1] = fetch_pg(pf_p[u ^ 1]);   // page of tile jj + 1's pool
                 pf_p[u] = fetch_p(jj + kAtSlots);       // pool of tile jj + 2
-                const uint32_t dst = sTile + u * kAtTileBytes + blk * kAtBlockBytes + my_pool * kAtBoxBytes;
+                const uint32_t dst = sTile + u * kAtTileBytes + blk * kAtBlockBytes + my_pool * Pool::kBoxBytes;
 #pragma unroll
                 for (int cc = 0; cc < kAtChunks; ++cc) {
                     if (jj >= kAtSlots) {  // P.V of the slot's previous tile has read this chunk
@@ -640,8 +655,8 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         const int t2 = tid - kAtSoftThreads;
         for (int k = t2; k < n_tail * 64; k += kTailThreads) {
             const int j = k >> 6, piece = k & 63;
-            const int64_t row = paged ? P.cmap.latent_row(b, nf * kKpool + j)
-                                      : base_row + static_cast<int64_t>(nf) * kKpool + j;
+            const int64_t row = paged ? P.cmap.latent_row(b, nf * KP + j)
+                                      : base_row + static_cast<int64_t>(nf) * KP + j;
             uint4 v = make_uint4(0u, 0u, 0u, 0u);
             if (row >= 0) v = *reinterpret_cast<const uint4 *>(P.latent + row * kLatentDim + piece * 8);
             else if (piece == 0) set_status(P.status, KP_ERR_DEVICE_BOUNDS);
@@ -666,7 +681,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
                 }
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-                if (lane == 0) ztail_s[h * 4 + j] = acc * P.scale_log2;
+                if (lane == 0) ztail_s[h * KP + j] = acc * P.scale_log2;
             }
         }
     }
@@ -691,9 +706,9 @@ __global__ void __launch_bounds__(kAtThreads, 1)
             float M = -INFINITY;
 #pragma unroll
             for (int s2 = 0; s2 < kAtMaxSplits; ++s2) M = fmaxf(M, ms[s2]);
-            for (int j = 0; j < n_tail; ++j) M = fmaxf(M, ztail_s[h * 4 + j]);
+            for (int j = 0; j < n_tail; ++j) M = fmaxf(M, ztail_s[h * KP + j]);
             float L = 0.f;
-            float *w = wm_s + tid * 16;
+            float *w = wm_s + tid * kWS;
 #pragma unroll
             for (int s2 = 0; s2 < kAtMaxSplits; ++s2) {
                 const float ws = ms[s2] > -INFINITY ? fast_exp2(ms[s2] - M) : 0.f;
@@ -701,11 +716,11 @@ __global__ void __launch_bounds__(kAtThreads, 1)
                 if (ws > 0.f) L += ws * ls[s2];
             }
             for (int j = 0; j < kAtMaxTail; ++j) {
-                const float wt = j < n_tail ? fast_exp2(ztail_s[h * 4 + j] - M) : 0.f;
+                const float wt = j < n_tail ? fast_exp2(ztail_s[h * KP + j] - M) : 0.f;
                 w[8 + j] = wt;
                 L += wt;
             }
-            w[12] = L > 0.f ? 1.f / L : 0.f;
+            w[kWInv] = L > 0.f ? 1.f / L : 0.f;
             if (P.lse)
                 P.lse[static_cast<int64_t>(q) * kMlaHeads + h] =
                     L > 0.f ? (M + fast_log2(L)) * 0.69314718055994530942f : -INFINITY;
@@ -721,13 +736,13 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         for (int idx0 = tid; idx0 < n_items; idx0 += kMrgItems * kAtThreads) {
             // weights of the items' heads into registers first (local reads), then
             // every remote load of the group, then the arithmetic
-            float4 wv[kMrgItems][4];
+            float4 wv[kMrgItems][Pool::kWF4];
 #pragma unroll
             for (int it = 0; it < kMrgItems; ++it) {
                 const int idx = min(idx0 + it * kAtThreads, n_items - 1);
-                const float4 *w4 = reinterpret_cast<const float4 *>(wm_s + (idx / (kNopeDim / 4)) * 16);
+                const float4 *w4 = reinterpret_cast<const float4 *>(wm_s + (idx / (kNopeDim / 4)) * kWS);
 #pragma unroll
-                for (int k = 0; k < 4; ++k) wv[it][k] = w4[k];
+                for (int k = 0; k < Pool::kWF4; ++k) wv[it][k] = w4[k];
             }
             float4 v[kMrgItems][kAtMaxSplits];
 #pragma unroll
@@ -748,9 +763,14 @@ __global__ void __launch_bounds__(kAtThreads, 1)
                 const int idx = idx0 + it * kAtThreads;
                 if (idx >= n_items) break;
                 const int hl = idx / (kNopeDim / 4), d = 4 * (idx % (kNopeDim / 4));
-                const float ws[13] = {wv[it][0].x, wv[it][0].y, wv[it][0].z, wv[it][0].w,
-                                      wv[it][1].x, wv[it][1].y, wv[it][1].z, wv[it][1].w,
-                                      wv[it][2].x, wv[it][2].y, wv[it][2].z, wv[it][2].w, wv[it][3].x};
+                float ws[4 * Pool::kWF4];
+#pragma unroll
+                for (int k = 0; k < Pool::kWF4; ++k) {
+                    ws[4 * k] = wv[it][k].x;
+                    ws[4 * k + 1] = wv[it][k].y;
+                    ws[4 * k + 2] = wv[it][k].z;
+                    ws[4 * k + 3] = wv[it][k].w;
+                }
                 float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
                 for (int s2 = 0; s2 < kAtMaxSplits; ++s2) {
@@ -772,7 +792,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
                     a.z = fmaf(wt, bf16_lo(cv.y), a.z);
                     a.w = fmaf(wt, bf16_hi(cv.y), a.w);
                 }
-                const float il = ws[12];
+                const float il = ws[kWInv];
                 *reinterpret_cast<uint2 *>(P.out + (static_cast<int64_t>(q) * kMlaHeads + h0 + hl) * kNopeDim + d) =
                     make_uint2(pack_bf16x2(a.x * il, a.y * il), pack_bf16x2(a.z * il, a.w * il));
             }
@@ -797,20 +817,41 @@ __global__ void __launch_bounds__(kAtThreads, 1)
 }
 
 // Largest cluster size whose clusters, one CTA per SM, all fit at once
-// (cached per device; host threads that race here compute the same value, and
-// the cache entries are atomics, so the race is benign).
-std::atomic<int> g_active_clusters[64][kAtMaxSplits + 1];
-std::atomic<int> g_smem_configured[64];
+// (cached per device and pool size; host threads that race here compute the
+// same value, and the cache entries are atomics, so the race is benign).
+std::atomic<int> g_active_clusters[2][64][kAtMaxSplits + 1];
+std::atomic<int> g_smem_configured[2][64];
 
+template <int KP>
+constexpr int pool_slot() { return KP == 4 ? 0 : 1; }
+
+template <int KP>
+bool attend_smem_configured() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    if (g_smem_configured[pool_slot<KP>()][dev].load(std::memory_order_relaxed)) return true;
+    cudaError_t e = cudaFuncSetAttribute(sparse_mla_tc_kernel<KP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         AtPool<KP>::kSmemBytes);
+    if (e != cudaSuccess) {
+        record_cuda_error("cudaFuncSetAttribute(sparse_mla_tc_kernel)", e);
+        return false;
+    }
+    g_smem_configured[pool_slot<KP>()][dev].store(1, std::memory_order_relaxed);
+    return true;
+}
+
+template <int KP>
 int max_active_clusters(int cluster) {
+    if (!attend_smem_configured<KP>()) return 0;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    const int cached = g_active_clusters[dev][cluster].load(std::memory_order_relaxed);
+    std::atomic<int> &slot = g_active_clusters[pool_slot<KP>()][dev][cluster];
+    const int cached = slot.load(std::memory_order_relaxed);
     if (cached != 0) return cached;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(cluster * 64);
     cfg.blockDim = dim3(kAtThreads);
-    cfg.dynamicSmemBytes = kAtSmemBytes;
+    cfg.dynamicSmemBytes = AtPool<KP>::kSmemBytes;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = cluster;
@@ -819,26 +860,55 @@ int max_active_clusters(int cluster) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, sparse_mla_tc_kernel, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, sparse_mla_tc_kernel<KP>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         n = 0;
     }
-    g_active_clusters[dev][cluster].store(n > 0 ? n : -1, std::memory_order_relaxed);
+    slot.store(n > 0 ? n : -1, std::memory_order_relaxed);
     return n;
 }
 
-bool attend_smem_configured() {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
-    if (g_smem_configured[dev].load(std::memory_order_relaxed)) return true;
-    cudaError_t e = cudaFuncSetAttribute(sparse_mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kAtSmemBytes);
-    if (e != cudaSuccess) {
-        record_cuda_error("cudaFuncSetAttribute(sparse_mla_tc_kernel)", e);
-        return false;
-    }
-    g_smem_configured[dev].store(1, std::memory_order_relaxed);
-    return true;
+template <int KP>
+kp_status launch_attend_kp(const kp_attend_args &a, cudaStream_t s) {
+    const int nq = a.q.num_queries;
+    const int sms = device_sm_count();
+    if (sms <= 0) return KP_ERR_CUDA;
+    if (!attend_smem_configured<KP>()) return KP_ERR_CUDA;
+    int splits = attend_splits(a.cfg, nq, sms);
+    while (splits > 1 && max_active_clusters<KP>(splits) < nq) splits /= 2;
+
+    // The gather addresses latent rows by a signed 32-bit TMA coordinate
+    // (validated: latent_rows <= INT32_MAX).
+    CUtensorMap tm_q, tm_lat;
+    if (!make_tmap_bf16_sw128(&tm_q, a.q_lat, kLatentDim, static_cast<uint64_t>(nq) * kMlaHeads,
+                              kLatentDim * 2, 64, kMlaHeads))
+        return KP_ERR_CUDA;
+    if (!make_tmap_bf16_sw128(&tm_lat, a.latent, kLatentDim, static_cast<uint64_t>(a.seqs.latent_rows),
+                              kLatentDim * 2, 64, KP))
+        return KP_ERR_CUDA;
+    AttendParams P;
+    P.latent = a.latent;
+    P.cmap = cache_map(a.seqs, a.cfg.kpool);
+    P.q_seq = a.q.q_seq;
+    P.q_pos = a.q.q_pos;
+    P.seq_len = a.seqs.seq_len;
+    P.num_seqs = a.seqs.num_seqs;
+    P.pool_idx = a.pool_idx;
+    P.n_sel = a.n_sel;
+    P.K = a.cfg.topk_tokens / a.cfg.kpool;
+    P.tail = a.cfg.always_select_tail ? 1 : 0;
+    P.scale_log2 = a.cfg.sm_scale * 1.44269504088896340736f;
+    P.out = a.out;
+    P.lse = a.lse;
+    P.splits = splits;
+    P.status = a.d_status;
+    P.wait_ns = wait_limit_ns(a.cfg.wait_limit_us);
+    P.stall = (a.cfg.debug_flags & KP_DEBUG_STALL_FIRST_WAIT) ? 1 : 0;
+
+    return launch_kernel("sparse_mla_tc_kernel", sparse_mla_tc_kernel<KP>,
+                         LaunchCfg(dim3(static_cast<unsigned>(nq) * splits), dim3(kAtThreads), AtPool<KP>::kSmemBytes,
+                                   s, splits),
+                         tm_q, tm_lat, P);
 }
 
 }  // namespace
@@ -862,45 +932,8 @@ size_t attend_ws_bytes(const kp_config &cfg, int32_t num_queries, int splits) {
 }
 
 kp_status launch_attend(const kp_attend_args &a, cudaStream_t s) {
-    const int nq = a.q.num_queries;
-    if (nq == 0) return KP_OK;
-    const int sms = device_sm_count();
-    if (sms <= 0) return KP_ERR_CUDA;
-    if (!attend_smem_configured()) return KP_ERR_CUDA;
-    int splits = attend_splits(a.cfg, nq, sms);
-    while (splits > 1 && max_active_clusters(splits) < nq) splits /= 2;
-
-    // The gather addresses latent rows by a signed 32-bit TMA coordinate
-    // (validated: latent_rows <= INT32_MAX).
-    CUtensorMap tm_q, tm_lat;
-    if (!make_tmap_bf16_sw128(&tm_q, a.q_lat, kLatentDim, static_cast<uint64_t>(nq) * kMlaHeads,
-                              kLatentDim * 2, 64, kMlaHeads))
-        return KP_ERR_CUDA;
-    if (!make_tmap_bf16_sw128(&tm_lat, a.latent, kLatentDim, static_cast<uint64_t>(a.seqs.latent_rows),
-                              kLatentDim * 2, 64, kKpool))
-        return KP_ERR_CUDA;
-    AttendParams P;
-    P.latent = a.latent;
-    P.cmap = cache_map(a.seqs);
-    P.q_seq = a.q.q_seq;
-    P.q_pos = a.q.q_pos;
-    P.seq_len = a.seqs.seq_len;
-    P.num_seqs = a.seqs.num_seqs;
-    P.pool_idx = a.pool_idx;
-    P.n_sel = a.n_sel;
-    P.K = a.cfg.topk_tokens / a.cfg.kpool;
-    P.tail = a.cfg.always_select_tail ? 1 : 0;
-    P.scale_log2 = a.cfg.sm_scale * 1.44269504088896340736f;
-    P.out = a.out;
-    P.lse = a.lse;
-    P.splits = splits;
-    P.status = a.d_status;
-    P.wait_ns = wait_limit_ns(a.cfg.wait_limit_us);
-    P.stall = (a.cfg.debug_flags & KP_DEBUG_STALL_FIRST_WAIT) ? 1 : 0;
-
-    return launch_kernel("sparse_mla_tc_kernel", sparse_mla_tc_kernel,
-                         LaunchCfg(dim3(static_cast<unsigned>(nq) * splits), dim3(kAtThreads), kAtSmemBytes, s, splits),
-                         tm_q, tm_lat, P);
+    if (a.q.num_queries == 0) return KP_OK;
+    return a.cfg.kpool == 16 ? launch_attend_kp<16>(a, s) : launch_attend_kp<4>(a, s);
 }
 
 }  // namespace kp

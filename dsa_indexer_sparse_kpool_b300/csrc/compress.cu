@@ -47,19 +47,20 @@ __device__ __forceinline__ Row4 load_bf16x4(const uint16_t *p) {
     return r;
 }
 
+template <int KP>
 __global__ void __launch_bounds__(kCompressWarps * 32)
     kpool_compress_kernel(int32_t mode, const int32_t *__restrict__ prev_len,
                           const int32_t *__restrict__ new_off, const uint16_t *__restrict__ keys,
                           const uint16_t *__restrict__ gates, const uint16_t *__restrict__ ape,
                           uint16_t *__restrict__ tail_keys, uint16_t *__restrict__ tail_gates,
                           uint16_t *__restrict__ pooled, CacheMap cmap, int32_t *status, ScorePlanArgs plan) {
-    constexpr int R = kKpool - 1;  // ring slots per sequence
+    constexpr int R = KP - 1;  // ring slots per sequence
     __shared__ int scratch[33];
     pdl_wait_then_release();
     if (plan.plan && blockIdx.y == gridDim.y - 1) {  // the extra row of CTAs: the scorer's plan
         if (blockIdx.x == 0)
-            build_score_plan(plan.nq, plan.num_seqs, plan.q_seq, plan.q_pos, plan.seq_len, plan.max_tiles,
-                             plan.plan, plan.status, scratch);
+            build_score_plan(plan.nq, plan.num_seqs, plan.q_seq, plan.q_pos, plan.seq_len, plan.kshift,
+                             plan.max_tiles, plan.plan, plan.status, scratch);
         return;
     }
     const int b = blockIdx.y;
@@ -70,21 +71,21 @@ __global__ void __launch_bounds__(kCompressWarps * 32)
     const int n_new = new_off[b + 1] - n0;
     if (n_new <= 0 || prev < 0) return;
     const int len = prev + n_new;
-    const int p_first = prev / kKpool;             // first pool touched
-    const int n_complete = len / kKpool - p_first;  // pools completed by this step
+    const int p_first = prev / KP;             // first pool touched
+    const int n_complete = len / KP - p_first;  // pools completed by this step
     const int n_items = n_complete > 0 ? n_complete : 1;
     if (item >= n_items) return;
     const int d0 = lane * 4;
 
     if (item < n_complete) {
         const int p = p_first + item;
-        Row4 k[kKpool], g[kKpool];
+        Row4 k[KP], g[KP];
 #pragma unroll
-        for (int i = 0; i < kKpool; ++i) {
-            const int pos = p * kKpool + i;
+        for (int i = 0; i < KP; ++i) {
+            const int pos = p * KP + i;
             const uint16_t *ksrc, *gsrc;
             if (pos < prev) {  // only possible for item 0: row held in the ring
-                const size_t off = (static_cast<size_t>(b) * R + (pos % kKpool)) * kIndexDim + d0;
+                const size_t off = (static_cast<size_t>(b) * R + (pos % KP)) * kIndexDim + d0;
                 ksrc = tail_keys + off;
                 gsrc = tail_gates + off;
             } else {
@@ -98,7 +99,7 @@ __global__ void __launch_bounds__(kCompressWarps * 32)
         float out[4];
         if (mode == KP_COMPRESS_LEARNED) {
 #pragma unroll
-            for (int i = 0; i < kKpool; ++i) {
+            for (int i = 0; i < KP; ++i) {
                 Row4 a = load_bf16x4(ape + i * kIndexDim + d0);
 #pragma unroll
                 for (int j = 0; j < 4; ++j) g[i].v[j] += a.v[j];
@@ -107,10 +108,10 @@ __global__ void __launch_bounds__(kCompressWarps * 32)
             for (int j = 0; j < 4; ++j) {
                 float m = g[0].v[j];
 #pragma unroll
-                for (int i = 1; i < kKpool; ++i) m = fmaxf(m, g[i].v[j]);
+                for (int i = 1; i < KP; ++i) m = fmaxf(m, g[i].v[j]);
                 float den = 0.f, num = 0.f;
 #pragma unroll
-                for (int i = 0; i < kKpool; ++i) {
+                for (int i = 0; i < KP; ++i) {
                     const float e = expf(g[i].v[j] - m);
                     den += e;
                     num += e * k[i].v[j];
@@ -122,8 +123,8 @@ __global__ void __launch_bounds__(kCompressWarps * 32)
             for (int j = 0; j < 4; ++j) {
                 float s = 0.f;
 #pragma unroll
-                for (int i = 0; i < kKpool; ++i) s += k[i].v[j];
-                out[j] = s * (1.0f / kKpool);
+                for (int i = 0; i < KP; ++i) s += k[i].v[j];
+                out[j] = s * (1.0f / KP);
             }
         }
         const int64_t row = cmap.pool_row(b, p);
@@ -141,10 +142,10 @@ __global__ void __launch_bounds__(kCompressWarps * 32)
         // Rows of the pool left incomplete go to the ring (slot = position % kpool).
         // This warp already holds the old ring rows it needed in registers.
         __syncwarp();
-        const int tail_start = (len / kKpool) * kKpool;
+        const int tail_start = (len / KP) * KP;
         for (int pos = max(prev, tail_start); pos < len; ++pos) {
             const size_t src = static_cast<size_t>(n0 + pos - prev) * kIndexDim + d0;
-            const size_t dst = (static_cast<size_t>(b) * R + (pos % kKpool)) * kIndexDim + d0;
+            const size_t dst = (static_cast<size_t>(b) * R + (pos % KP)) * kIndexDim + d0;
             *reinterpret_cast<uint2 *>(tail_keys + dst) = *reinterpret_cast<const uint2 *>(keys + src);
             if (mode == KP_COMPRESS_LEARNED)
                 *reinterpret_cast<uint2 *>(tail_gates + dst) =
@@ -157,13 +158,15 @@ __global__ void __launch_bounds__(kCompressWarps * 32)
 
 kp_status launch_compress(const kp_compress_args &a, cudaStream_t s, const ScorePlanArgs *plan) {
     if (a.num_new == 0) return KP_OK;
-    const int max_items = (a.max_new_per_seq + kKpool - 1) / kKpool + 1;
+    const int kp = a.cfg.kpool;
+    const int max_items = (a.max_new_per_seq + kp - 1) / kp + 1;
     ScorePlanArgs pa{};
     if (plan) pa = *plan;
     dim3 grid((max_items + kCompressWarps - 1) / kCompressWarps, a.num_seqs + (pa.plan ? 1 : 0));
-    return launch_kernel("kpool_compress_kernel", kpool_compress_kernel,
+    return launch_kernel("kpool_compress_kernel", kp == 16 ? kpool_compress_kernel<16> : kpool_compress_kernel<4>,
                          LaunchCfg(grid, dim3(kCompressWarps * 32), 0, s), a.cfg.compress_mode, a.prev_len,
-                         a.new_off, a.keys, a.gates, a.ape, a.tail_keys, a.tail_gates, a.pooled, cache_map(a.seqs),
+                         a.new_off, a.keys, a.gates, a.ape, a.tail_keys, a.tail_gates, a.pooled,
+                         cache_map(a.seqs, kp),
                          a.d_status, pa);
 }
 

@@ -21,7 +21,6 @@ constexpr int kIndexDim = KP_INDEX_DIM;
 constexpr int kMlaHeads = KP_MLA_HEADS;
 constexpr int kLatentDim = KP_LATENT_DIM;
 constexpr int kNopeDim = KP_NOPE_DIM;
-constexpr int kKpool = KP_KPOOL;
 
 // A single wait longer than this (1 s) means something is broken.  Callers
 // can set a shorter limit per call (kp_config.wait_limit_us); the waits that
@@ -54,13 +53,14 @@ __device__ __forceinline__ void pdl_wait_then_release() {
 
 // Where a sequence's latent rows and pooled keys live: per-sequence row
 // offsets (contiguous mode) or a block table of pages (paged mode; a page of
-// 2^page_shift token positions holds as many latent rows and 2^page_shift / 4
-// pooled rows, at the same physical page id in both caches).
+// 2^page_shift token positions holds as many latent rows and 2^page_shift /
+// kpool pooled rows, at the same physical page id in both caches).
 struct CacheMap {
     const int64_t *latent_row_off;
     const int64_t *pool_row_off;
     const int32_t *block_table;  // nullptr: contiguous mode
     int page_shift;              // log2(tokens per page)
+    int pool_shift;              // log2(tokens per pool)
     int blocks_per_seq;
     int num_pages;               // valid page ids: 0 .. num_pages - 1
     int64_t latent_rows;
@@ -90,12 +90,14 @@ struct CacheMap {
             return (p >= 0 && r >= 0 && r < pool_rows) ? r : -1;
         }
         if (p < 0) return -1;
-        const int ps = page_shift - 2;  // log2(pools per page); kpool = 4
+        const int ps = page_shift - pool_shift;  // log2(pools per page)
         const int pg = page(b, p >> ps);
         return pg < 0 ? -1 : (static_cast<int64_t>(pg) << ps) + (p & ((1 << ps) - 1));
     }
 };
-static_assert(KP_KPOOL == 4, "pooled rows per page are tokens per page / 4");
+
+// log2 of a supported pool size (4 or 16).
+__host__ __device__ constexpr int kpool_shift(int kpool) { return kpool == 16 ? 4 : 2; }
 
 // First error wins; later ones are dropped.
 __device__ __forceinline__ void set_status(int32_t *st, int code) {

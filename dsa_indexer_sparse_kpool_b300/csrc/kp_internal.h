@@ -13,8 +13,8 @@
 
 namespace kp {
 
-// Device-side view of a kp_seqs layout (validated).
-CacheMap cache_map(const kp_seqs &s);
+// Device-side view of a kp_seqs layout (validated) for pools of `kpool` tokens.
+CacheMap cache_map(const kp_seqs &s, int kpool);
 
 // Records the text of a failed CUDA call for kp_last_error() (per host thread).
 void record_cuda_error(const char *where, cudaError_t err);
@@ -84,6 +84,7 @@ struct ScorePlanArgs {
     const int32_t *q_seq;
     const int32_t *q_pos;
     const int32_t *seq_len;
+    int kshift;        // log2(tokens per pool)
     int max_tiles;
     int32_t *plan;     // nullptr: no plan to build
     int32_t *status;

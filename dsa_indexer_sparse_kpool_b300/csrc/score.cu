@@ -56,12 +56,12 @@ constexpr int kScSmemBytes = kScStages * kScAStageBytes + kScBBytes + kScNumBars
 __global__ void __launch_bounds__(1024) score_plan_kernel(int nq, int num_seqs,
                                                           const int32_t *__restrict__ q_seq,
                                                           const int32_t *__restrict__ q_pos,
-                                                          const int32_t *__restrict__ seq_len,
+                                                          const int32_t *__restrict__ seq_len, int kshift,
                                                           int max_tiles, int32_t *plan_base,
                                                           int32_t *status) {
     __shared__ int scratch[33];
     pdl_wait_then_release();
-    build_score_plan(nq, num_seqs, q_seq, q_pos, seq_len, max_tiles, plan_base, status, scratch);
+    build_score_plan(nq, num_seqs, q_seq, q_pos, seq_len, kshift, max_tiles, plan_base, status, scratch);
 }
 
 struct ScoreParams {
@@ -74,6 +74,7 @@ struct ScoreParams {
     const int32_t *prev_len;   // tokens of each sequence before this step (nullptr: no early loads)
     const int32_t *q_pos;
     const int32_t *seq_len;
+    int kshift;                // log2(tokens per pool)
     const float *w;
     CacheMap cmap;             // where each sequence's pooled keys live
     int seg;                   // pooled rows per TMA box: 128, or a page's pools when pages are shorter
@@ -207,7 +208,7 @@ __global__ void __launch_bounds__(kScThreads, 1)
     if (P.local_plan) {
         if (stage_q) __syncthreads();
         build_score_plan(P.nq, P.num_seqs, stage_q ? qseq_s : P.q_seq, stage_q ? qpos_s : P.q_pos, P.seq_len,
-                         P.max_tiles, unit0_s, P.status, plan_scratch);
+                         P.kshift, P.max_tiles, unit0_s, P.status, plan_scratch);
         plan_base = unit0_s;
     } else {
         pdl_wait_then_release();
@@ -272,8 +273,8 @@ __global__ void __launch_bounds__(kScThreads, 1)
                 const int q0 = plan.q0[g], nq = plan.nq[g];
                 bseq = plan.seq[g];
                 if (!paged) row_base = P.cmap.pool_row_off[bseq];
-                old_pools = P.prev_len ? P.prev_len[bseq] / kKpool : 0;
-                if (paged) need = __reduce_max_sync(full, lane < nq ? (P.q_pos[q0 + lane] + 1) / kKpool : 0);
+                old_pools = P.prev_len ? P.prev_len[bseq] >> P.kshift : 0;
+                if (paged) need = __reduce_max_sync(full, lane < nq ? (P.q_pos[q0 + lane] + 1) >> P.kshift : 0);
                 if (lane == 0) {
                     mbar_expect_tx(bfull_bar, nq * 2 * kScQBoxBytes);
                     for (int qi = 0; qi < nq; ++qi)
@@ -412,7 +413,7 @@ __global__ void __launch_bounds__(kScThreads, 1)
                 nq = plan.nq[gc.g];
                 for (int k = et; k < nq * kIndexHeads; k += kScEpiThreads)
                     w_s[k] = P.w[static_cast<int64_t>(q0) * kIndexHeads + k];
-                if (et < nq) nf_s[et] = (P.q_pos[q0 + et] + 1) / kKpool;
+                if (et < nq) nf_s[et] = (P.q_pos[q0 + et] + 1) >> P.kshift;
                 epi_bar_all(true);
                 first = false;
             }
@@ -463,6 +464,7 @@ ScorePlanArgs score_plan_args(const kp_score_args &a) {
     p.q_seq = a.q.q_seq;
     p.q_pos = a.q.q_pos;
     p.seq_len = a.seqs.seq_len;
+    p.kshift = kpool_shift(a.cfg.kpool);
     p.max_tiles = (a.q.max_pools + kScM - 1) / kScM;
     p.plan = static_cast<int32_t *>(a.workspace);
     p.status = a.d_status;
@@ -483,12 +485,14 @@ kp_status launch_score(const kp_score_args &a, cudaStream_t s, bool plan_ready, 
     if (!plan_ready && !local_plan) {
         const kp_status st = launch_kernel("score_plan_kernel", score_plan_kernel,
                                            LaunchCfg(dim3(1), dim3(1024), 0, s), nq, a.seqs.num_seqs, a.q.q_seq,
-                                           a.q.q_pos, a.seqs.seq_len, max_tiles, plan, a.d_status);
+                                           a.q.q_pos, a.seqs.seq_len, kpool_shift(a.cfg.kpool), max_tiles, plan,
+                                           a.d_status);
         if (st != KP_OK) return st;
     }
     if (max_tiles == 0) return KP_OK;
 
-    const int seg = a.seqs.block_table && a.seqs.page_tokens / kKpool < kScM ? a.seqs.page_tokens / kKpool : kScM;
+    const int pool_page = a.seqs.block_table ? a.seqs.page_tokens / a.cfg.kpool : kScM;  // pools per page
+    const int seg = pool_page < kScM ? pool_page : kScM;
     CUtensorMap tm_pool, tm_q;
     if (!make_tmap_bf16_sw128(&tm_pool, a.pooled, kIndexDim, static_cast<uint64_t>(a.seqs.pool_rows),
                               kIndexDim * 2, 64, static_cast<uint32_t>(seg)) ||
@@ -511,8 +515,9 @@ kp_status launch_score(const kp_score_args &a, cudaStream_t s, bool plan_ready, 
     P.prev_len = local_plan ? prev_len : nullptr;
     P.q_pos = a.q.q_pos;
     P.seq_len = a.seqs.seq_len;
+    P.kshift = kpool_shift(a.cfg.kpool);
     P.w = a.w;
-    P.cmap = cache_map(a.seqs);
+    P.cmap = cache_map(a.seqs, a.cfg.kpool);
     P.seg = seg;
     P.scores = a.scores;
     P.stride = a.score_stride;

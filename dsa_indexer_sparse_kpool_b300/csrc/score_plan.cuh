@@ -23,14 +23,15 @@ struct PlanView {
 };
 
 // Groups runs of up to 8 adjacent queries of the same sequence and counts the
-// 128-pool tiles each group needs (the largest n_full among its queries).  A
+// 128-pool tiles each group needs (the largest n_full = (t + 1) >> kshift
+// among its queries, 2^kshift tokens per pool).  A
 // group whose sequence is out of range, or with a query at or past its
 // sequence's length, gets no tiles and sets KP_ERR_DEVICE_BOUNDS.
 // Every thread of the calling CTA must call it (blockDim.x a multiple of 32);
 // `scratch` holds >= 33 ints of shared memory.
 __device__ __forceinline__ void build_score_plan(int nq, int num_seqs, const int32_t *__restrict__ q_seq,
                                                  const int32_t *__restrict__ q_pos,
-                                                 const int32_t *__restrict__ seq_len, int max_tiles,
+                                                 const int32_t *__restrict__ seq_len, int kshift, int max_tiles,
                                                  int32_t *plan_base, int32_t *status, int *scratch) {
     PlanView plan(plan_base, nq);
     int carry_run = -1, carry_groups = 0;
@@ -65,7 +66,7 @@ __device__ __forceinline__ void build_score_plan(int nq, int num_seqs, const int
         for (int q = q0; q < q1; ++q) {
             const int t = q_pos[q];
             pos_ok = pos_ok && t < len;
-            mx = max(mx, (t + 1) / kKpool);
+            mx = max(mx, (t + 1) >> kshift);
         }
         int tiles = (mx + kScM - 1) / kScM;
         if (!seq_ok || !pos_ok) {

@@ -131,7 +131,7 @@ struct TopkShared {
 template <int kTkThreads>
 __global__ void __launch_bounds__(kTkThreads, 1)
     topk_select_kernel(const float *__restrict__ scores, int64_t stride,
-                       const int32_t *__restrict__ q_pos, int K, int32_t *__restrict__ pool_idx,
+                       const int32_t *__restrict__ q_pos, int kshift, int K, int32_t *__restrict__ pool_idx,
                        int32_t *__restrict__ n_sel, int chunk_cap, int32_t *status) {
     constexpr int kTkWarps = kTkThreads / 32;
     extern __shared__ uint32_t keys[];
@@ -148,7 +148,7 @@ __global__ void __launch_bounds__(kTkThreads, 1)
     // Inputs and shared-memory set-up first: the scores come from the previous
     // kernel, so only their reads wait for the grid dependency.
     const int t = q_pos[q];
-    const int n = t >= 0 ? (t + 1) / kKpool : 0;
+    const int n = t >= 0 ? (t + 1) >> kshift : 0;
     int32_t *out = pool_idx + static_cast<int64_t>(q) * K;
     if (tid == 0) {
         sh.kmin = 0xffffffffu;
@@ -489,7 +489,8 @@ kp_status launch_topk(const kp_topk_args &a, cudaStream_t s) {
     return launch_kernel("topk_select_kernel", kern,
                          LaunchCfg(dim3(static_cast<unsigned>(nq) * C), dim3(wide ? kTkMaxThreads : kTkMinThreads),
                                    smem, s, C),
-                         a.scores, a.score_stride, a.q.q_pos, K, a.pool_idx, a.n_sel, chunk_cap, a.d_status);
+                         a.scores, a.score_stride, a.q.q_pos, kpool_shift(a.cfg.kpool), K, a.pool_idx, a.n_sel,
+                         chunk_cap, a.d_status);
 }
 
 }  // namespace kp

@@ -52,8 +52,10 @@ def test_null_args_rejected(L):
 
 def test_unsupported_kpool_and_bad_budget(L):
     a = kp.kp_score_args()
-    a.cfg = _cfg(kpool=16)
+    a.cfg = _cfg(kpool=8)                    # pools of 4 (the checkpoint) and 16 (NeMo's default) only
     assert L.kp_indexer_score(ctypes.byref(a), None) == 2
+    a.cfg = _cfg(kpool=16, topk_tokens=2048)
+    assert L.kp_indexer_score(ctypes.byref(a), None) == 1   # past the config check; no layout given
     a.cfg = _cfg(topk_tokens=6)
     assert L.kp_indexer_score(ctypes.byref(a), None) == 1
     a.cfg = _cfg(topk_tokens=4 * 2048)
