@@ -42,8 +42,14 @@ DESCR = {
     "long": "long-context decode: 1 seq, ctx 1,048,575, 4 queries, top-k 2048",
 }
 STAGES = ("kpool_compress", "indexer_score", "topk_select", "sparse_mla_attend")
-KERNEL_FILES = {"kpool_compress": "compress.cu", "indexer_score": "score.cu", "topk_select": "topk.cu",
-                "sparse_mla_attend": "attend.cu"}
+FUSED_STAGES = ("kpool_compress", "indexer_score_select", "sparse_mla_attend")
+KERNEL_FILES = {   # each stage's kernel source and the headers it includes
+    "kpool_compress": ("compress.cu", "score_plan.cuh", "kp_common.cuh"),
+    "indexer_score": ("score.cu", "score_plan.cuh", "kp_common.cuh"),
+    "topk_select": ("topk.cu", "topk_select.cuh", "kp_common.cuh"),
+    "indexer_score_select": ("score_select.cu", "topk_select.cuh", "score_plan.cuh", "kp_common.cuh"),
+    "sparse_mla_attend": ("attend.cu", "kp_common.cuh"),
+}
 
 
 def parse():
@@ -55,6 +61,8 @@ def parse():
     ap.add_argument("--workload", default="decode", choices=["decode", "ragged", "prefill", "long"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the CPU-baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--select", default="auto", choices=["auto", "staged", "fused"],
+                    help="how the step scores and selects (fused: one kernel, scores kept on chip)")
     ap.add_argument("--paged", type=int, default=0, metavar="TOKENS",
                     help="page the caches in pages of TOKENS positions (block table, shuffled pages)")
     return ap.parse_args()
@@ -121,6 +129,15 @@ def measured_peaks():
     return 6400.0, 1800.0, 1400.0, "fallback"
 
 
+def kernel_source_hash(stage: str) -> str:
+    """Hash of the stage's kernel source and its headers: a traffic figure
+    is used only while the sources it was captured on are unchanged."""
+    h = hashlib.sha256()
+    for f in KERNEL_FILES[stage]:
+        h.update(open(os.path.join(ROOT, "dsa_indexer_sparse_kpool_b300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
 def kernel_traffic(stage: str, workload_name: str):
     """ncu DRAM bytes per launch of this stage's kernel on this workload
     (profiles/ncu_traffic.txt), if that capture was taken on the current kernel
@@ -128,8 +145,7 @@ def kernel_traffic(stage: str, workload_name: str):
     p = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
     if not os.path.exists(p):
         return None
-    src = os.path.join(ROOT, "dsa_indexer_sparse_kpool_b300", "csrc", KERNEL_FILES[stage])
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    sha = kernel_source_hash(stage)
     for line in open(p):
         f = line.split()
         if len(f) >= 5 and not line.startswith("#") and f[0] == stage and f[2] == workload_name and f[4] == sha:
@@ -330,7 +346,9 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
 
     wl = workload(args.workload, rank)
-    cfg = Config(topk_tokens=wl.spec.topk_tokens, sm_scale=wl.spec.sm_scale)
+    from dsa_indexer_sparse_kpool_b300 import SELECT_AUTO, SELECT_STAGED, SELECT_FUSED
+    mode = {"auto": SELECT_AUTO, "staged": SELECT_STAGED, "fused": SELECT_FUSED}[args.select]
+    cfg = Config(topk_tokens=wl.spec.topk_tokens, sm_scale=wl.spec.sm_scale, select_mode=mode)
     sess = build_session(cfg, wl.lens.tolist(), wl.prev_len.tolist(), wl.tok_off.tolist(), wl.pool_off.tolist(),
                          wl.pool_rows, wl.latent, wl.keys, wl.gates, wl.ape, device=dev,
                          page_tokens=args.paged or None)
@@ -351,7 +369,9 @@ def main():
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=stream):
             step.run()
-        calls, _ = step.stage_calls()
+        fused = step.fused()
+        stages = FUSED_STAGES if fused else STAGES
+        calls, _ = step.stage_calls(fused=fused)
         for c in calls:
             c()
         stage_graphs = []
@@ -388,7 +408,7 @@ def main():
 
         # ---- per-stage breakdown (one graph per stage, events between)
         ks = max(1, min(args.steps, 500))
-        sev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(ks)]
+        sev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)] for _ in range(ks)]
         for i in range(ks):
             flush_l2()
             sev[i][0].record(stream)
@@ -396,8 +416,8 @@ def main():
                 g.replay()
                 sev[i][j + 1].record(stream)
         barrier()
-        stage_ms = {STAGES[j]: float(np.mean([sev[i][j].elapsed_time(sev[i][j + 1]) for i in range(ks)]))
-                    for j in range(4)}
+        stage_ms = {stages[j]: float(np.mean([sev[i][j].elapsed_time(sev[i][j + 1]) for i in range(ks)]))
+                    for j in range(len(stages))}
 
         # ---- end to end: pinned host inputs -> step -> host outputs, every step.
         # The step's inputs and outputs are packed into one device buffer each
@@ -445,6 +465,9 @@ def main():
     if rank == 0:
         alg, n_tok = algorithmic_bytes(wl)
         flops = algorithmic_flops(wl)
+        if fused:   # one kernel does the scoring's work and the selection's
+            alg["indexer_score_select"] = alg["indexer_score"] + alg["topk_select"]
+            flops["indexer_score_select"] = flops["indexer_score"] + flops["topk_select"]
         hbm, bf16, bf16_sus, src = measured_peaks()
         # Every stage against its bound: tensor when its flops take longer at
         # the bf16 peak than its bytes at the HBM peak, else HBM; stages with
@@ -452,7 +475,7 @@ def main():
         # The per-stage graphs run ks launches back to back, under a second: the
         # burst bf16 peak applies.
         stage_roof = {}
-        for st in STAGES:
+        for st in stages:
             t = stage_ms[st] * 1e-3
             tpeak = bf16 if t * ks < 1.0 else bf16_sus
             tr = kernel_traffic(st, args.workload)
@@ -471,9 +494,9 @@ def main():
             else:
                 stage_roof[st] = {"bound": "latency", "achieved": None, "peak": None, "unit": None, "frac": None,
                                   "traffic": tr, "algorithmic_bytes": 0, "avg_launch_ms": stage_ms[st]}
-        dominant = max(STAGES, key=lambda st: stage_ms[st])
+        dominant = max(stages, key=lambda st: stage_ms[st])
         roof = dict(stage_roof[dominant], kernel=dominant)
-        step_bytes = sum(alg.values())
+        step_bytes = sum(alg[st] for st in stages)
         cpu = None
         if not args.no_cpu_baseline:
             threads = os.cpu_count() or 1
@@ -493,6 +516,8 @@ def main():
                        "ctx": int(wl.lens.max()), "topk_tokens": wl.spec.topk_tokens,
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                        "caches": f"paged, {args.paged}-token pages (block table)" if args.paged else "contiguous",
+                       "select": ("fused: scores and top-k in one kernel, no score matrix" if fused else
+                                  "staged: score matrix in the workspace, then top-k"),
                        "l2": "flushed between timed steps (256 MB read)", "timing": "CUDA-graph replay, events"},
             "roofline": roof,
             "stage_roofline": stage_roof,

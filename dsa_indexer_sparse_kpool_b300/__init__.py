@@ -23,6 +23,8 @@ INDEX_HEADS, INDEX_DIM, MLA_HEADS, LATENT_DIM, NOPE_DIM, KPOOL = 32, 128, 64, 57
 MAX_TOPK_POOLS, MAX_SCORE_POOLS, NOALLOC_MAX_QUERIES = 1024, 262144, 8192
 COMPRESS_LEARNED, COMPRESS_MEAN = 0, 1
 DEBUG_STALL_FIRST_WAIT = 1
+SELECT_AUTO, SELECT_STAGED, SELECT_FUSED = 0, 1, 2
+FUSED_MAX_POOLS = 16384
 
 STATUS = {0: "KP_OK", 1: "KP_ERR_INVALID_ARG", 2: "KP_ERR_UNSUPPORTED", 3: "KP_ERR_CUDA",
           4: "KP_ERR_DEVICE_TIMEOUT", 5: "KP_ERR_DEVICE_BOUNDS", 6: "KP_ERR_WORKSPACE"}
@@ -33,7 +35,7 @@ _i32, _i64, _f32, _vp, _sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, cty
 class kp_config(ctypes.Structure):
     _fields_ = [("kpool", _i32), ("topk_tokens", _i32), ("compress_mode", _i32),
                 ("always_select_tail", _i32), ("sm_scale", _f32), ("wait_limit_us", _i32),
-                ("debug_flags", _i32)]
+                ("debug_flags", _i32), ("select_mode", _i32)]
 
 
 class kp_seqs(ctypes.Structure):
@@ -62,6 +64,12 @@ class kp_score_args(ctypes.Structure):
 class kp_topk_args(ctypes.Structure):
     _fields_ = [("cfg", kp_config), ("q", kp_queries), ("scores", _vp), ("score_stride", _i64),
                 ("pool_idx", _vp), ("n_sel", _vp), ("d_status", _vp)]
+
+
+class kp_score_select_args(ctypes.Structure):
+    _fields_ = [("cfg", kp_config), ("seqs", kp_seqs), ("q", kp_queries), ("q_idx", _vp), ("w", _vp),
+                ("pooled", _vp), ("pool_idx", _vp), ("n_sel", _vp), ("workspace", _vp),
+                ("workspace_bytes", _sz), ("d_status", _vp)]
 
 
 class kp_attend_args(ctypes.Structure):
@@ -102,7 +110,8 @@ class kp_mla_absorb_out_args(ctypes.Structure):
                 ("hidden_out", _vp), ("wait_limit_us", _i32), ("d_status", _vp)]
 
 
-EXPORTS = ("kp_kpool_compress", "kp_indexer_score", "kp_topk_select", "kp_sparse_mla_attend",
+EXPORTS = ("kp_kpool_compress", "kp_indexer_score", "kp_topk_select", "kp_indexer_score_select",
+           "kp_sparse_mla_attend",
            "kp_dsa_forward", "kp_indexer_score_noalloc", "kp_score_workspace_size", "kp_attend_workspace_size",
            "kp_workspace_size", "kp_gemm_bf16", "kp_indexer_project", "kp_mla_absorb_q", "kp_mla_absorb_out",
            "kp_status_string", "kp_last_error", "kp_read_device_status", "kp_version")
@@ -121,6 +130,7 @@ def lib() -> ctypes.CDLL:
         for name, argt in (("kp_kpool_compress", kp_compress_args), ("kp_indexer_score", kp_score_args),
                            ("kp_indexer_score_noalloc", kp_score_args),
                            ("kp_topk_select", kp_topk_args), ("kp_sparse_mla_attend", kp_attend_args),
+                           ("kp_indexer_score_select", kp_score_select_args),
                            ("kp_dsa_forward", kp_forward_args), ("kp_gemm_bf16", kp_gemm_args),
                            ("kp_indexer_project", kp_indexer_project_args),
                            ("kp_mla_absorb_q", kp_mla_absorb_q_args),
@@ -184,10 +194,12 @@ class Config:
     sm_scale: float = 1.0 / 16.0
     wait_limit_us: int = 0          # 0: each device-side wait gives up after 1 s
     debug_flags: int = 0            # DEBUG_* bits (failure-path tests only)
+    select_mode: int = SELECT_AUTO  # how kp_dsa_forward scores and selects (SELECT_*)
 
     def c(self) -> kp_config:
         return kp_config(self.kpool, self.topk_tokens, self.compress_mode, int(self.always_select_tail),
-                         float(self.sm_scale), int(self.wait_limit_us), int(self.debug_flags))
+                         float(self.sm_scale), int(self.wait_limit_us), int(self.debug_flags),
+                         int(self.select_mode))
 
     @property
     def k_pools(self) -> int:
@@ -266,6 +278,15 @@ def kp_indexer_score_noalloc(cfg: Config, seqs: Seqs, queries: Queries, q_idx, w
 def kp_topk_select(cfg: Config, queries: Queries, scores, pool_idx, n_sel, d_status=None, stream=None) -> None:
     a = kp_topk_args(cfg.c(), queries.c(), _p(scores), scores.shape[1], _p(pool_idx), _p(n_sel), _p(d_status))
     _check(lib().kp_topk_select(ctypes.byref(a), _stream(stream)), "kp_topk_select")
+
+
+def kp_indexer_score_select(cfg: Config, seqs: Seqs, queries: Queries, q_idx, w, pooled, pool_idx, n_sel,
+                            workspace, d_status=None, stream=None) -> None:
+    """kp_indexer_score then kp_topk_select in one kernel, the scores kept on
+    chip (queries.max_pools <= FUSED_MAX_POOLS)."""
+    a = kp_score_select_args(cfg.c(), seqs.c(), queries.c(), _p(q_idx), _p(w), _p(pooled), _p(pool_idx),
+                             _p(n_sel), _p(workspace), workspace.numel() * workspace.element_size(), _p(d_status))
+    _check(lib().kp_indexer_score_select(ctypes.byref(a), _stream(stream)), "kp_indexer_score_select")
 
 
 def kp_sparse_mla_attend(cfg: Config, seqs: Seqs, queries: Queries, q_lat, latent, pool_idx, n_sel, out, lse,

@@ -26,6 +26,8 @@ kp_status check_config(const kp_config &c) {
     if (!std::isfinite(c.sm_scale)) return KP_ERR_INVALID_ARG;
     if (c.wait_limit_us < 0) return KP_ERR_INVALID_ARG;
     if ((c.debug_flags & ~KP_DEBUG_STALL_FIRST_WAIT) != 0) return KP_ERR_INVALID_ARG;
+    if (c.select_mode != KP_SELECT_AUTO && c.select_mode != KP_SELECT_STAGED && c.select_mode != KP_SELECT_FUSED)
+        return KP_ERR_INVALID_ARG;
     return KP_OK;
 }
 
@@ -69,6 +71,11 @@ int64_t score_stride_for(int32_t max_pools) {
 }
 
 // Forward workspace layout: [scores][pool_idx][n_sel][step scratch].
+// Whether the step scores and selects in one kernel (no score matrix).
+bool forward_fused(const kp_forward_args &a) {
+    return a.cfg.select_mode == KP_SELECT_FUSED && a.q.num_queries > 0 && score_select_fits(a.cfg, a.q);
+}
+
 struct ForwardLayout {
     size_t scores, pool_idx, n_sel, scratch, total;
 };
@@ -77,7 +84,8 @@ ForwardLayout forward_layout(const kp_forward_args &a, int sm_count) {
     const size_t nq = static_cast<size_t>(a.q.num_queries > 0 ? a.q.num_queries : 0);
     const size_t K = static_cast<size_t>(a.cfg.topk_tokens / (a.cfg.kpool > 0 ? a.cfg.kpool : 1));
     L.scores = 0;
-    L.pool_idx = L.scores + align_up(nq * score_stride_for(a.q.max_pools) * 4, 256);
+    const size_t score_bytes = forward_fused(a) ? 0 : nq * score_stride_for(a.q.max_pools) * 4;
+    L.pool_idx = L.scores + align_up(score_bytes, 256);
     L.n_sel = L.pool_idx + align_up(nq * K * 4, 256);
     L.scratch = L.n_sel + align_up(nq * 4, 256);
     const size_t plan = score_plan_bytes(static_cast<int32_t>(nq));
@@ -274,6 +282,39 @@ kp_status kp_topk_select(const kp_topk_args *a, kp_stream_t stream) {
     return launch_topk(*a, reinterpret_cast<cudaStream_t>(stream));
 }
 
+kp_status kp_indexer_score_select(const kp_score_select_args *a, kp_stream_t stream) {
+    if (!a) return KP_ERR_INVALID_ARG;
+    kp_status st = check_config(a->cfg);
+    if (st != KP_OK) return st;
+    if ((st = check_queries(a->q)) != KP_OK) return st;
+    if ((st = check_seqs(a->seqs, a->cfg.kpool, false, true)) != KP_OK) return st;
+    if (a->q.num_queries == 0) return KP_OK;
+    if (!score_select_fits(a->cfg, a->q)) return KP_ERR_UNSUPPORTED;
+    if (!a->q_idx || !a->w || !a->pooled || !a->pool_idx || !a->n_sel) return KP_ERR_INVALID_ARG;
+    if (!aligned(a->q_idx, 16) || !aligned(a->pooled, 16) || !aligned(a->w, 4)) return KP_ERR_INVALID_ARG;
+    if (!a->workspace || a->workspace_bytes < score_plan_bytes(a->q.num_queries) || !aligned(a->workspace, 256))
+        return KP_ERR_WORKSPACE;
+    kp_score_args sc;
+    std::memset(&sc, 0, sizeof sc);
+    sc.cfg = a->cfg;
+    sc.seqs = a->seqs;
+    sc.q = a->q;
+    sc.q_idx = a->q_idx;
+    sc.w = a->w;
+    sc.pooled = a->pooled;
+    sc.workspace = a->workspace;
+    sc.workspace_bytes = a->workspace_bytes;
+    sc.d_status = a->d_status;
+    kp_topk_args tk;
+    std::memset(&tk, 0, sizeof tk);
+    tk.cfg = a->cfg;
+    tk.q = a->q;
+    tk.pool_idx = a->pool_idx;
+    tk.n_sel = a->n_sel;
+    tk.d_status = a->d_status;
+    return launch_score_select(sc, tk, reinterpret_cast<cudaStream_t>(stream), false, nullptr);
+}
+
 size_t kp_attend_workspace_size(const kp_config *cfg, int32_t num_queries) {
     if (!cfg) return 256;
     return attend_ws_need(*cfg, num_queries);
@@ -370,6 +411,24 @@ kp_status kp_dsa_forward(const kp_forward_args *a, kp_stream_t stream) {
     if ((st = validate_attend(&at)) != KP_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const bool queries = a->q.num_queries > 0;
+    if (forward_fused(*a)) {
+        // Scores and top-k in one kernel, the scores kept on chip.  Its plan
+        // (groups of up to 4 queries) is built in that kernel when small
+        // enough, else by an extra grid row of the compression launch, else
+        // by the plan kernel.
+        if (c.num_new > 0 && score_select_plan_is_local(a->q.num_queries)) {
+            if ((st = launch_compress(c, s)) != KP_OK) return st;
+            if ((st = launch_score_select(sc, tk, s, false, c.prev_len)) != KP_OK) return st;
+        } else if (c.num_new > 0 && c.num_seqs < 65535) {
+            const ScorePlanArgs pa = score_select_plan_args(sc);
+            if ((st = launch_compress(c, s, &pa)) != KP_OK) return st;
+            if ((st = launch_score_select(sc, tk, s, true, nullptr)) != KP_OK) return st;
+        } else {
+            if (c.num_new > 0 && (st = launch_compress(c, s)) != KP_OK) return st;
+            if ((st = launch_score_select(sc, tk, s, false, nullptr)) != KP_OK) return st;
+        }
+        return launch_attend(at, s);
+    }
     // The scorer's plan: built by the scorer itself in shared memory when it
     // fits (then the scorer also starts on the older pooled keys during the
     // compression); otherwise by an extra CTA of the compression launch (one
@@ -530,7 +589,7 @@ kp_status kp_read_device_status(const int32_t *d_status, kp_stream_t stream) {
     return static_cast<kp_status>(v);
 }
 
-int kp_version(void) { return 20000; }
+int kp_version(void) { return 20100; }
 
 }  // extern "C"
 

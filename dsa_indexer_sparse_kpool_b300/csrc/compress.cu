@@ -60,7 +60,7 @@ __global__ void __launch_bounds__(kCompressWarps * 32)
     if (plan.plan && blockIdx.y == gridDim.y - 1) {  // the extra row of CTAs: the scorer's plan
         if (blockIdx.x == 0)
             build_score_plan(plan.nq, plan.num_seqs, plan.q_seq, plan.q_pos, plan.seq_len, plan.kshift,
-                             plan.max_tiles, plan.plan, plan.status, scratch);
+                             plan.max_tiles, plan.plan, plan.status, scratch, plan.max_q);
         return;
     }
     const int b = blockIdx.y;

@@ -85,6 +85,7 @@ struct ScorePlanArgs {
     const int32_t *q_pos;
     const int32_t *seq_len;
     int kshift;        // log2(tokens per pool)
+    int max_q;         // queries per group (8 for the scorer, 4 for the fused score-and-select)
     int max_tiles;
     int32_t *plan;     // nullptr: no plan to build
     int32_t *status;
@@ -100,9 +101,20 @@ ScorePlanArgs score_plan_args(const kp_score_args &a);
 // waiting for it.
 kp_status launch_compress(const kp_compress_args &a, cudaStream_t s, const ScorePlanArgs *plan = nullptr);
 bool score_plan_is_local(int32_t num_queries);
+// The scorer's plan kernel on its own (one CTA).
+kp_status launch_score_plan(const ScorePlanArgs &p, cudaStream_t s);
 kp_status launch_score(const kp_score_args &a, cudaStream_t s, bool plan_ready = false,
                        const int32_t *prev_len = nullptr, bool allow_local_plan = true);
 kp_status launch_topk(const kp_topk_args &a, cudaStream_t s);
+// Fused scoring and top-k (no score matrix in global memory): when
+// score_select_fits(...) holds.  plan_ready: the plan (groups of <= 4 queries)
+// was built by the compression launch (score_select_plan_args); prev_len as
+// for launch_score.
+bool score_select_fits(const kp_config &cfg, const kp_queries &q);
+ScorePlanArgs score_select_plan_args(const kp_score_args &a);
+bool score_select_plan_is_local(int32_t num_queries);
+kp_status launch_score_select(const kp_score_args &sc, const kp_topk_args &tk, cudaStream_t s, bool plan_ready,
+                              const int32_t *prev_len);
 // kp_indexer_score with its plan always in the caller's workspace (validated).
 kp_status score_with_workspace_plan(const kp_score_args *a, cudaStream_t stream);
 kp_status launch_attend(const kp_attend_args &a, cudaStream_t s);

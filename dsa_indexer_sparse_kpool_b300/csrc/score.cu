@@ -58,10 +58,10 @@ __global__ void __launch_bounds__(1024) score_plan_kernel(int nq, int num_seqs,
                                                           const int32_t *__restrict__ q_pos,
                                                           const int32_t *__restrict__ seq_len, int kshift,
                                                           int max_tiles, int32_t *plan_base,
-                                                          int32_t *status) {
+                                                          int32_t *status, int max_q) {
     __shared__ int scratch[33];
     pdl_wait_then_release();
-    build_score_plan(nq, num_seqs, q_seq, q_pos, seq_len, kshift, max_tiles, plan_base, status, scratch);
+    build_score_plan(nq, num_seqs, q_seq, q_pos, seq_len, kshift, max_tiles, plan_base, status, scratch, max_q);
 }
 
 struct ScoreParams {
@@ -465,6 +465,7 @@ ScorePlanArgs score_plan_args(const kp_score_args &a) {
     p.q_pos = a.q.q_pos;
     p.seq_len = a.seqs.seq_len;
     p.kshift = kpool_shift(a.cfg.kpool);
+    p.max_q = kScMaxQ;
     p.max_tiles = (a.q.max_pools + kScM - 1) / kScM;
     p.plan = static_cast<int32_t *>(a.workspace);
     p.status = a.d_status;
@@ -472,6 +473,11 @@ ScorePlanArgs score_plan_args(const kp_score_args &a) {
 }
 
 bool score_plan_is_local(int32_t num_queries) { return num_queries <= kScLocalPlanMaxQ; }
+
+kp_status launch_score_plan(const ScorePlanArgs &p, cudaStream_t s) {
+    return launch_kernel("score_plan_kernel", score_plan_kernel, LaunchCfg(dim3(1), dim3(1024), 0, s), p.nq,
+                         p.num_seqs, p.q_seq, p.q_pos, p.seq_len, p.kshift, p.max_tiles, p.plan, p.status, p.max_q);
+}
 
 kp_status launch_score(const kp_score_args &a, cudaStream_t s, bool plan_ready, const int32_t *prev_len,
                        bool allow_local_plan) {
@@ -486,7 +492,7 @@ kp_status launch_score(const kp_score_args &a, cudaStream_t s, bool plan_ready, 
         const kp_status st = launch_kernel("score_plan_kernel", score_plan_kernel,
                                            LaunchCfg(dim3(1), dim3(1024), 0, s), nq, a.seqs.num_seqs, a.q.q_seq,
                                            a.q.q_pos, a.seqs.seq_len, kpool_shift(a.cfg.kpool), max_tiles, plan,
-                                           a.d_status);
+                                           a.d_status, kScMaxQ);
         if (st != KP_OK) return st;
     }
     if (max_tiles == 0) return KP_OK;

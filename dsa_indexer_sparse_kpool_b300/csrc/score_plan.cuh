@@ -22,7 +22,7 @@ struct PlanView {
         : hdr(base), q0(base + 4), nq(base + 4 + n), seq(base + 4 + 2 * n), unit0(base + 4 + 3 * n) {}
 };
 
-// Groups runs of up to 8 adjacent queries of the same sequence and counts the
+// Groups runs of up to max_q (<= 8) adjacent queries of the same sequence and counts the
 // 128-pool tiles each group needs (the largest n_full = (t + 1) >> kshift
 // among its queries, 2^kshift tokens per pool).  A
 // group whose sequence is out of range, or with a query at or past its
@@ -32,7 +32,8 @@ struct PlanView {
 __device__ __forceinline__ void build_score_plan(int nq, int num_seqs, const int32_t *__restrict__ q_seq,
                                                  const int32_t *__restrict__ q_pos,
                                                  const int32_t *__restrict__ seq_len, int kshift, int max_tiles,
-                                                 int32_t *plan_base, int32_t *status, int *scratch) {
+                                                 int32_t *plan_base, int32_t *status, int *scratch,
+                                                 int max_q = kScMaxQ) {
     PlanView plan(plan_base, nq);
     int carry_run = -1, carry_groups = 0;
     for (int base = 0; base < nq; base += blockDim.x) {
@@ -44,7 +45,7 @@ __device__ __forceinline__ void build_score_plan(int nq, int num_seqs, const int
         int rs = block_inclusive_scan<1>(run_start ? i : -1, scratch, &tot);
         rs = max(rs, carry_run);
         carry_run = max(carry_run, tot);
-        const bool gs = in && ((i - rs) % kScMaxQ == 0);
+        const bool gs = in && ((i - rs) % max_q == 0);
         const int incl = block_inclusive_scan<0>(gs ? 1 : 0, scratch, &tot);
         if (gs) {
             const int gid = carry_groups + incl - 1;

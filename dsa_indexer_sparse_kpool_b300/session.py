@@ -11,14 +11,17 @@ from typing import Optional, Sequence
 
 import torch
 
-from . import (Config, Queries, Seqs, forward_args, kp_dsa_forward, kp_indexer_score, kp_kpool_compress,
-               kp_score_workspace_size, kp_attend_workspace_size, kp_sparse_mla_attend, kp_topk_select,
-               kp_workspace_size, score_stride, INDEX_DIM, LATENT_DIM, MLA_HEADS, NOPE_DIM)
+from . import (Config, Queries, Seqs, forward_args, kp_dsa_forward, kp_indexer_score, kp_indexer_score_select,
+               kp_kpool_compress, kp_score_workspace_size, kp_attend_workspace_size, kp_sparse_mla_attend,
+               kp_topk_select, kp_workspace_size, score_stride, FUSED_MAX_POOLS, SELECT_FUSED, INDEX_DIM,
+               LATENT_DIM, MLA_HEADS, NOPE_DIM)
 
 
 # Queries up to which the library's scorer builds its work plan in shared
-# memory (4096 plan words: a 4-word header, four words per query, one more).
+# memory (4096 plan words: a 4-word header, four words per query, one more),
+# and the same for the fused score-and-select kernel (2048 plan words).
 SCORE_LOCAL_PLAN_MAX_QUERIES = (4096 - 5) // 4
+SCORE_SELECT_LOCAL_PLAN_MAX_QUERIES = (2048 - 5) // 4
 
 
 def _dev_i32(x, device):
@@ -195,22 +198,32 @@ class Step:
         self.args = self._args(self.workspace)
         return in_buf, out_buf
 
+    def fused(self) -> bool:
+        """Whether ``run`` scores and selects in one kernel (SELECT_FUSED and
+        rows short enough for it)."""
+        return (self.sess.cfg.select_mode == SELECT_FUSED and self.queries.q_seq.numel() > 0
+                and self.queries.max_pools <= FUSED_MAX_POOLS)
+
     def launches_per_step(self) -> int:
-        """Kernels one ``run`` launches: compress, score, top-k and attention;
-        no queries stops after compress.  The scorer builds its own work plan
-        up to SCORE_LOCAL_PLAN_MAX_QUERIES queries; above that the plan rides in
-        an extra grid row of the compression launch when there are new tokens,
-        else it is one more kernel."""
+        """Kernels one ``run`` launches: compress, score, top-k and attention
+        (score and top-k are one kernel when fused); no queries stops after
+        compress.  The scorer builds its own work plan up to a query count
+        (SCORE_LOCAL_PLAN_MAX_QUERIES, or SCORE_SELECT_LOCAL_PLAN_MAX_QUERIES
+        fused); above that the plan rides in an extra grid row of the
+        compression launch when there are new tokens, else it is one more
+        kernel."""
         nq = self.queries.q_seq.numel()
         new = int(self.new_off[-1].item()) > 0
         if nq == 0:
             return 1 if new else 0
-        plan_free = nq <= SCORE_LOCAL_PLAN_MAX_QUERIES or (new and self.seqs.seq_len.numel() < 65535)
-        return (1 if new else 0) + (1 if plan_free else 2) + 2
+        local = SCORE_SELECT_LOCAL_PLAN_MAX_QUERIES if self.fused() else SCORE_LOCAL_PLAN_MAX_QUERIES
+        plan_free = nq <= local or (new and self.seqs.seq_len.numel() < 65535)
+        return (1 if new else 0) + (1 if plan_free else 2) + (1 if self.fused() else 2)
 
-    def stage_calls(self):
-        """The four stage calls on persistent buffers (capturable one by one):
-        [compress, score, topk, attend]; returns (calls, scores tensor)."""
+    def stage_calls(self, fused: bool = False):
+        """The stage calls on persistent buffers (capturable one by one):
+        [compress, score, topk, attend], or with fused [compress,
+        score_select, attend]; returns (calls, scores tensor)."""
         s, cfg = self.sess, self.sess.cfg
         NQ = self.queries.q_seq.numel()
         if not hasattr(self, "_stage_bufs"):
@@ -220,14 +233,23 @@ class Step:
                 torch.empty(kp_score_workspace_size(NQ), dtype=torch.uint8, device=s.device),
                 torch.empty(max(256, kp_attend_workspace_size(cfg, NQ)), dtype=torch.uint8, device=s.device))
         scores, ws, aws = self._stage_bufs
+        compress = lambda: kp_kpool_compress(cfg, self.seqs, self.prev_len, self.new_off, self.keys,  # noqa: E731
+                                             self.gates, s.ape, s.tail_keys, s.tail_gates, s.pooled, self.max_new,
+                                             d_status=s.status)
+        attend = lambda: kp_sparse_mla_attend(cfg, self.seqs, self.queries, self.q_lat, s.latent,  # noqa: E731
+                                              self.pool_idx, self.n_sel, self.out, self.lse, aws,
+                                              d_status=s.status)
+        if fused:
+            select = lambda: kp_indexer_score_select(cfg, self.seqs, self.queries, self.q_idx,  # noqa: E731
+                                                     self.w, s.pooled, self.pool_idx, self.n_sel, ws,
+                                                     d_status=s.status)
+            return [compress, select, attend], scores
         calls = [
-            lambda: kp_kpool_compress(cfg, self.seqs, self.prev_len, self.new_off, self.keys, self.gates, s.ape,
-                                      s.tail_keys, s.tail_gates, s.pooled, self.max_new, d_status=s.status),
+            compress,
             lambda: kp_indexer_score(cfg, self.seqs, self.queries, self.q_idx, self.w, s.pooled, scores, ws,
                                      d_status=s.status),
             lambda: kp_topk_select(cfg, self.queries, scores, self.pool_idx, self.n_sel, d_status=s.status),
-            lambda: kp_sparse_mla_attend(cfg, self.seqs, self.queries, self.q_lat, s.latent, self.pool_idx,
-                                         self.n_sel, self.out, self.lse, aws, d_status=s.status),
+            attend,
         ]
         return calls, scores
 

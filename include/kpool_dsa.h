@@ -3,7 +3,7 @@
  *
  * One DSA layer step of the GLM-5.3-Flash hybrid decoder, in four stages:
  *
- *   1. kp_kpool_compress     pool every run of `kpool` (4) consecutive indexer
+ *   1. kp_kpool_compress     pool every run of `kpool` (4 or 16) consecutive indexer
  *                            keys into one pooled key and append it to the
  *                            pooled indexer cache; keep the rows of the
  *                            still-incomplete pool in a per-sequence tail ring.
@@ -24,6 +24,8 @@
  *                            (MAX docs Glm5NextConfig.index_kpool_always_select_tail,
  *                            mla_use_nope; Glm5Next.build_layers: 576-wide
  *                            latent rows whose last 64 columns are zero).
+ *
+ *   kp_indexer_score_select  2 and 3 in one kernel, the scores kept on chip.
  *
  *   kp_dsa_forward runs 1-4 in order on one stream.
  *
@@ -47,8 +49,9 @@
  *    or cache row); the offending element is skipped, never dereferenced.
  *    The library never clears it: zero it before the calls you want to check.
  *  - Fixed shapes (compile-time): indexer 32 heads x 128 dims; MLA 64 heads
- *    over latent rows of 576 bf16 of which the first 512 are read; kpool 4.
- *    Anything else returns KP_ERR_UNSUPPORTED.
+ *    over latent rows of 576 bf16 of which the first 512 are read; kpool 4
+ *    (the llm-atlas card's index_kpool) or 16 (the NeMo AutoModel
+ *    Glm5NextTextConfig default).  Anything else returns KP_ERR_UNSUPPORTED.
  *
  * Query positions and visibility
  * ------------------------------
@@ -94,10 +97,11 @@ enum {
     KP_MLA_HEADS = 64,     /* attention heads */
     KP_LATENT_DIM = 576,   /* latent cache row width (bf16) */
     KP_NOPE_DIM = 512,     /* latent columns read (kv_lora_rank); 512..575 are zero */
-    KP_KPOOL = 4,          /* tokens per pool */
+    KP_KPOOL = 4,          /* tokens per pool (16 is supported too) */
     KP_MAX_TOPK_POOLS = 1024,    /* largest supported topk_tokens / kpool */
     KP_MAX_SCORE_POOLS = 262144, /* largest supported pools per query (1,048,576 tokens) */
-    KP_NOALLOC_MAX_QUERIES = 8192 /* largest num_queries of kp_indexer_score_noalloc */
+    KP_NOALLOC_MAX_QUERIES = 8192, /* largest num_queries of kp_indexer_score_noalloc */
+    KP_FUSED_MAX_POOLS = 16384    /* largest max_pools of kp_indexer_score_select */
 };
 
 enum { KP_COMPRESS_LEARNED = 0, KP_COMPRESS_MEAN = 1 };
@@ -112,9 +116,23 @@ enum {
     KP_DEBUG_STALL_FIRST_WAIT = 1
 };
 
+/* select_mode values: how kp_dsa_forward scores and selects. */
+enum {
+    /* The faster path for the call's shape on B300.  At present that is the
+     * staged kernels (kp_indexer_score then kp_topk_select) on every shape. */
+    KP_SELECT_AUTO = 0,
+    /* kp_indexer_score then kp_topk_select: the fp32 score matrix
+     * [NQ][max_pools rounded up to 128] lives in the workspace. */
+    KP_SELECT_STAGED = 1,
+    /* kp_indexer_score_select: scores kept on chip, no score matrix in the
+     * workspace, when max_pools <= KP_FUSED_MAX_POOLS (else staged).  Same
+     * results, bit for bit. */
+    KP_SELECT_FUSED = 2
+};
+
 /* Method and execution options. */
 typedef struct kp_config {
-    int32_t kpool;              /* tokens per pool; must be 4 */
+    int32_t kpool;              /* tokens per pool: 4, or 16 */
     int32_t topk_tokens;        /* token budget of the top-k (index_topk, 2048); a
                                    positive multiple of kpool, <= 4 * KP_MAX_TOPK_POOLS */
     int32_t compress_mode;      /* KP_COMPRESS_LEARNED (gate + ape softmax) or _MEAN */
@@ -124,6 +142,7 @@ typedef struct kp_config {
                                    1 s.  A wait that runs out sets KP_ERR_DEVICE_TIMEOUT
                                    in d_status and the kernel returns early */
     int32_t debug_flags;        /* KP_DEBUG_* bits; 0 in normal use */
+    int32_t select_mode;        /* KP_SELECT_*: how kp_dsa_forward runs stages 2-3 */
 } kp_config;
 
 /* Per-sequence cache layout, in one of two modes.
@@ -240,6 +259,31 @@ typedef struct kp_topk_args {
     int32_t *d_status;
 } kp_topk_args;
 
+/* ---- 2+3 in one kernel ---- */
+/* The pool_idx and n_sel of kp_indexer_score followed by kp_topk_select, bit
+ * for bit, with every score kept in on-chip memory: no score matrix is
+ * written (the llama.cpp PR "add GLM-5.3-Flash (GLM5-Next) support", review
+ * comments: re-materialised pooled intermediates are what slow the graph).
+ * A group of up to 4 adjacent queries of one sequence is scored by a cluster
+ * of C CTAs (C * 2048 >= max_pools), each CTA holding its 2048-pool slice's
+ * scores in shared memory; one CTA per query then gathers the row and selects.
+ * max_pools above KP_FUSED_MAX_POOLS returns KP_ERR_UNSUPPORTED (use the
+ * staged calls).  A query whose visible pools exceed max_pools is cut at
+ * the cluster's capacity and reported as KP_ERR_DEVICE_BOUNDS. */
+typedef struct kp_score_select_args {
+    kp_config cfg;
+    kp_seqs seqs;                 /* as kp_score_args */
+    kp_queries q;
+    const uint16_t *q_idx;        /* [NQ][32][128] bf16 */
+    const float *w;               /* [NQ][32] fp32 */
+    const uint16_t *pooled;       /* [pool_rows][128] bf16 */
+    int32_t *pool_idx;            /* [NQ][K] out, as kp_topk_args */
+    int32_t *n_sel;               /* [NQ] out */
+    void *workspace;              /* >= kp_score_workspace_size(NQ) bytes, 256-aligned */
+    size_t workspace_bytes;
+    int32_t *d_status;
+} kp_score_select_args;
+
 /* ---- 4. sparse MLA over the selected pools + tail ---- */
 /* Token set of query q: rows kpool*p .. kpool*p + kpool-1 of every selected
  * pool p, then the tail positions (when always_select_tail).  For head h:
@@ -298,6 +342,7 @@ typedef struct kp_forward_args {
 KP_API kp_status kp_kpool_compress(const kp_compress_args *args, kp_stream_t stream);
 KP_API kp_status kp_indexer_score(const kp_score_args *args, kp_stream_t stream);
 KP_API kp_status kp_topk_select(const kp_topk_args *args, kp_stream_t stream);
+KP_API kp_status kp_indexer_score_select(const kp_score_select_args *args, kp_stream_t stream);
 KP_API kp_status kp_sparse_mla_attend(const kp_attend_args *args, kp_stream_t stream);
 KP_API kp_status kp_dsa_forward(const kp_forward_args *args, kp_stream_t stream);
 

@@ -19,11 +19,14 @@ from __future__ import annotations
 
 import math
 
+import dataclasses
+
 import numpy as np
 import torch
 
 import kpool_inputs as KI
 import oracle
+import dsa_indexer_sparse_kpool_b300 as kp
 from dsa_indexer_sparse_kpool_b300 import Config, COMPRESS_LEARNED
 from dsa_indexer_sparse_kpool_b300.session import build_session, build_step
 
@@ -236,30 +239,38 @@ def full_check(wl, queries=None, cfg=None, stages=True, check_all_pooled=True, p
     return sess, step, report
 
 
-def fused_check(wl, queries=None, cfg=None, check_all_pooled=True, page_tokens=None):
-    """The path the bench times: kp_dsa_forward on fresh state, against the
-    four stage calls on other fresh state (bit for bit: pooled cache, tail
-    rings, selection, outputs) and against the oracle on the sampled queries
-    (scores from the staged run, selection and attention from the fused one)."""
+def fused_check(wl, queries=None, cfg=None, check_all_pooled=True, page_tokens=None,
+                modes=(kp.SELECT_AUTO, kp.SELECT_FUSED)):
+    """The path the bench times: kp_dsa_forward on fresh state, in each of the
+    given select modes, against the four stage calls on other fresh state (bit
+    for bit: pooled cache, tail rings, selection, outputs) and against the
+    oracle on the sampled queries (scores from the staged run, selection and
+    attention from the forward)."""
     cfg = cfg or cfg_of(wl)
-    sess_f, step_f = make_gpu(wl, cfg, page_tokens=page_tokens)
-    step_f.run()
     sess_s, step_s = make_gpu(wl, cfg, page_tokens=page_tokens)
     scores = step_s.run_stages()
     torch.cuda.synchronize()
-    assert int(sess_f.status.item()) == 0, f"fused: device status {int(sess_f.status.item())}"
     assert int(sess_s.status.item()) == 0, f"staged: device status {int(sess_s.status.item())}"
-    assert torch.equal(sess_f.pooled, sess_s.pooled), "pooled caches differ"
-    assert torch.equal(sess_f.tail_keys, sess_s.tail_keys) and torch.equal(sess_f.tail_gates, sess_s.tail_gates)
-    assert torch.equal(step_f.n_sel, step_s.n_sel), "n_sel differs"
-    assert torch.equal(step_f.pool_idx, step_s.pool_idx), "selection differs"
-    assert torch.equal(step_f.out, step_s.out), "outputs differ"
-    assert torch.equal(step_f.lse, step_s.lse), "lse differs"
-    queries = list(range(wl.NQ) if queries is None else queries)
-    seqs_needed = sorted({int(wl.q_seq[q]) for q in queries}) if not check_all_pooled else None
-    check_pooled(sess_f, wl, seqs_needed, cfg.compress_mode)
-    report = _oracle_checks(sess_f, wl, queries, cfg, host(scores).numpy(), host(step_f.pool_idx).numpy(),
-                            host(step_f.n_sel).numpy(), host(step_f.out.float()).numpy(),
-                            host(step_f.lse).numpy())
-    assert report["checked"] == len(queries)
-    return sess_f, step_f, report
+    out = None
+    for mode in modes:
+        cfg_m = dataclasses.replace(cfg, select_mode=mode)
+        sess_f, step_f = make_gpu(wl, cfg_m, page_tokens=page_tokens)
+        step_f.run()
+        torch.cuda.synchronize()
+        tag = f"select_mode {mode}"
+        assert int(sess_f.status.item()) == 0, f"{tag}: device status {int(sess_f.status.item())}"
+        assert torch.equal(sess_f.pooled, sess_s.pooled), f"{tag}: pooled caches differ"
+        assert torch.equal(sess_f.tail_keys, sess_s.tail_keys) and torch.equal(sess_f.tail_gates, sess_s.tail_gates)
+        assert torch.equal(step_f.n_sel, step_s.n_sel), f"{tag}: n_sel differs"
+        assert torch.equal(step_f.pool_idx, step_s.pool_idx), f"{tag}: selection differs"
+        assert torch.equal(step_f.out, step_s.out), f"{tag}: outputs differ"
+        assert torch.equal(step_f.lse, step_s.lse), f"{tag}: lse differs"
+        queries = list(range(wl.NQ) if queries is None else queries)
+        seqs_needed = sorted({int(wl.q_seq[q]) for q in queries}) if not check_all_pooled else None
+        check_pooled(sess_f, wl, seqs_needed, cfg.compress_mode)
+        report = _oracle_checks(sess_f, wl, queries, cfg, host(scores).numpy(), host(step_f.pool_idx).numpy(),
+                                host(step_f.n_sel).numpy(), host(step_f.out.float()).numpy(),
+                                host(step_f.lse).numpy())
+        assert report["checked"] == len(queries)
+        out = (sess_f, step_f, report)
+    return out

@@ -30,7 +30,7 @@ def test_exports_every_declared_entry_point(L):
     for n in names:
         assert hasattr(L, n), n
     assert set(kp.EXPORTS) == set(names)
-    assert L.kp_version() == 20000
+    assert L.kp_version() == 20100
 
 
 def test_status_strings(L):
@@ -45,8 +45,8 @@ def _cfg(**kw):
 
 
 def test_null_args_rejected(L):
-    for name in ("kp_kpool_compress", "kp_indexer_score", "kp_topk_select", "kp_sparse_mla_attend",
-                 "kp_dsa_forward"):
+    for name in ("kp_kpool_compress", "kp_indexer_score", "kp_topk_select", "kp_indexer_score_select",
+                 "kp_sparse_mla_attend", "kp_dsa_forward"):
         assert getattr(L, name)(None, None) == 1
 
 
@@ -66,6 +66,8 @@ def test_unsupported_kpool_and_bad_budget(L):
     t.cfg = _cfg(wait_limit_us=-1)
     assert L.kp_topk_select(ctypes.byref(t), None) == 1
     t.cfg = _cfg(debug_flags=2)
+    assert L.kp_topk_select(ctypes.byref(t), None) == 1
+    t.cfg = _cfg(select_mode=3)
     assert L.kp_topk_select(ctypes.byref(t), None) == 1
 
 
@@ -120,3 +122,36 @@ def test_noalloc_score_rejects_too_many_queries_before_any_launch(L):
     assert L.kp_indexer_score_noalloc(ctypes.byref(a), None) == 2
     assert "KP_NOALLOC_MAX_QUERIES" in L.kp_last_error().decode()
     assert L.kp_indexer_score_noalloc(None, None) == 1
+
+
+def test_fused_score_select_checks_before_any_launch(L):
+    a = kp.kp_score_select_args()
+    a.cfg = _cfg()
+    a.seqs = kp.kp_seqs(1, 0x1000, 0x1000, 0x1000, 100, 100)
+    a.q = kp.kp_queries(4, 0x1000, 0x1000, kp.FUSED_MAX_POOLS + 1)   # longer rows: the staged calls
+    a.q_idx = a.w = a.pooled = a.pool_idx = a.n_sel = 0x10000
+    a.workspace = 0x10000
+    a.workspace_bytes = 1 << 20
+    assert L.kp_indexer_score_select(ctypes.byref(a), None) == 2
+    a.q = kp.kp_queries(4, 0x1000, 0x1000, kp.FUSED_MAX_POOLS)
+    a.workspace_bytes = 8
+    assert L.kp_indexer_score_select(ctypes.byref(a), None) == 6
+    a.workspace_bytes = 1 << 20
+    a.n_sel = None
+    assert L.kp_indexer_score_select(ctypes.byref(a), None) == 1
+    a.q = kp.kp_queries(0, None, None, 0)                          # nothing to do
+    assert L.kp_indexer_score_select(ctypes.byref(a), None) == 0
+
+
+def test_fused_mode_workspace_holds_no_score_matrix(L):
+    args = kp.kp_forward_args()
+    args.q = kp.kp_queries(32, 0, 0, 8192)
+    args.cfg = kp.Config(select_mode=kp.SELECT_STAGED).c()
+    staged = L.kp_workspace_size(ctypes.byref(args))
+    args.cfg = kp.Config(select_mode=kp.SELECT_FUSED).c()
+    fused = L.kp_workspace_size(ctypes.byref(args))
+    assert staged - fused >= 32 * 8192 * 4
+    args.q = kp.kp_queries(32, 0, 0, kp.FUSED_MAX_POOLS + 128)    # too long for the fused kernel: staged
+    fused_long = L.kp_workspace_size(ctypes.byref(args))
+    args.cfg = kp.Config(select_mode=kp.SELECT_STAGED).c()
+    assert fused_long == L.kp_workspace_size(ctypes.byref(args))

@@ -23,14 +23,16 @@ def small_spec(lens, n_q, topk_tokens=256, seed=11, **kw):
 def test_tiny_all_stages_and_fused():
     wl = KI.make(KI.named("tiny"))
     sess, step, rep = PL.full_check(wl)
-    # the fused call on fresh state gives the same bits as the staged calls
-    sess2, step2 = PL.make_gpu(wl)
-    step2.run()
-    torch.cuda.synchronize()
-    assert torch.equal(step2.pool_idx, step.pool_idx) and torch.equal(step2.n_sel, step.n_sel)
-    assert torch.equal(step2.out, step.out)
-    assert torch.equal(step2.lse, step.lse)
-    assert int(sess2.status.item()) == 0
+    # the whole-step call on fresh state, in either select mode, gives the same
+    # bits as the staged calls
+    for mode in (kp.SELECT_AUTO, kp.SELECT_FUSED):
+        sess2, step2 = PL.make_gpu(wl, PL.cfg_of(wl, select_mode=mode))
+        step2.run()
+        torch.cuda.synchronize()
+        assert torch.equal(step2.pool_idx, step.pool_idx) and torch.equal(step2.n_sel, step.n_sel)
+        assert torch.equal(step2.out, step.out)
+        assert torch.equal(step2.lse, step.lse)
+        assert int(sess2.status.item()) == 0
 
 
 def test_tiny_end_to_end_against_oracle_pipeline():
@@ -162,6 +164,8 @@ def test_exact_ties_in_scores():
     sess, step, rep = PL.full_check(wl)
     sel0 = step.pool_idx[0].cpu().numpy()
     assert np.array_equal(sel0, np.arange(64)), "equal scores must select the lowest pool indices"
+    # the same ties through the step with the scores kept on chip
+    PL.fused_check(wl, modes=(kp.SELECT_FUSED,))
 
 
 @pytest.mark.parametrize("lens,n_q", [
