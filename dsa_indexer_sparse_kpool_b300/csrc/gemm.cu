@@ -267,9 +267,22 @@ kp_status launch_gemm(const kp_gemm_args &g, cudaStream_t s) {
     if (g.m == 0 || g.n == 0) return KP_OK;
     const int sms = device_sm_count();
     if (sms <= 0) return KP_ERR_CUDA;
-    // Columns per tile: the whole batch's N when it fits, else 256; a multiple of 32.
-    int bn = ((g.n + 31) / 32) * 32;
-    if (bn > kGmMaxN) bn = kGmMaxN;
+    // Columns per tile (a multiple of 32, <= 256): the width whose waves of
+    // units cost least, a unit's cost taken as (64 + bn) -- its MMA and B
+    // bytes grow with bn, its A tile and fixed costs do not.  Large products
+    // keep 256; a product of few rows (decode) takes narrow tiles so that
+    // every SM streams a share of the weights instead of a few SMs all of it.
+    const int64_t m_tiles = (g.m + kGmM - 1) / kGmM;
+    int bn = 32;
+    int64_t best = -1;
+    for (int cand = kGmMaxN; cand >= 32; cand /= 2) {
+        const int64_t units = static_cast<int64_t>(g.batch) * m_tiles * ((g.n + cand - 1) / cand);
+        const int64_t cost = (units + sms - 1) / sms * (64 + cand);
+        if (best < 0 || cost < best) {
+            best = cost;
+            bn = cand;
+        }
+    }
     CUtensorMap tm_a, tm_b;
     const uint64_t a_cols = static_cast<uint64_t>(g.a_batch_off) * (g.batch - 1) + g.k;
     const uint64_t b_rows = static_cast<uint64_t>(g.b_batch_off) * (g.batch - 1) + g.n;

@@ -42,7 +42,8 @@ def rnd(shape, gen, std=1.0):
     (200, 128, 4096, 1, False),    # keys / gates shape, two row tiles with a ragged one
     (37, 512, 256, 64, False),     # per-head batch, the absorbed-query layout
     (129, 288, 192, 3, False),     # a column tile cut short, three batches
-    (33, 4096, 16384, 1, False),   # the o_proj shape
+    (33, 4096, 16384, 1, False),   # the o_proj shape (32-column tiles: few rows)
+    (50, 6400, 128, 1, False),     # 64-column tiles
 ])
 def test_gemm_against_oracle(m, n, k, batch, f32):
     gen = torch.Generator().manual_seed(m * 7 + n)
