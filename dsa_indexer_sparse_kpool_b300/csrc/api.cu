@@ -530,7 +530,12 @@ kp_status kp_indexer_project(const kp_indexer_project_args *a, kp_stream_t strea
                   KP_INDEX_DIM, 0, KP_DTYPE_BF16, a->wait_limit_us, a->d_status),
         gemm_args(T, KP_INDEX_HEADS, KP_HIDDEN, 1, a->hidden, KP_HIDDEN, 0, a->w_iw, KP_HIDDEN, 0, a->w,
                   KP_INDEX_HEADS, 0, KP_DTYPE_F32, a->wait_limit_us, a->d_status)};
-    return run_gemms(gs, 4, reinterpret_cast<cudaStream_t>(stream));
+    for (const kp_gemm_args &g : gs) {
+        const kp_status st = validate_gemm(&g);
+        if (st != KP_OK) return st;
+    }
+    // four independent products: one launch, side by side
+    return launch_gemm_group(gs, 4, reinterpret_cast<cudaStream_t>(stream));
 }
 
 kp_status kp_mla_absorb_q(const kp_mla_absorb_q_args *a, kp_stream_t stream) {

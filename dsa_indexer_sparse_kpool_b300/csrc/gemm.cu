@@ -13,14 +13,20 @@
 // (B holds every batch's [N][K] weight one after another) and a column block
 // of C.  Output bf16 (round to nearest even) or fp32.
 //
-// B300 design: persistent CTAs, one per SM, over (batch, 128-row tile,
-// BN-column tile) units.  Warp 0 streams 64-wide K slices of A (128 x 64) and
-// B (BN x 64) by TMA with 128-byte swizzle into a 4-stage ring; warp 1 issues
-// tcgen05.mma (M 128, N = BN <= 256, K 16) into one of two TMEM accumulators,
-// so the epilogue of one unit overlaps the MMAs of the next; warps 2-9 read
-// the accumulator back with tcgen05.ld (two warps per TMEM lane quadrant,
-// splitting the 32-column chunks) and store converted rows.
+// B300 design: persistent CTAs, one per SM, over (problem, batch, 128-row
+// tile, BN-column tile) units; up to four independent problems share one
+// launch, so small products run side by side instead of one after another.
+// Warp 0 streams 64-wide K slices of A (128 x 64) and B (BN x 64) by TMA with
+// 128-byte swizzle into a ring of 192 KB: four stages at BN 256, up to nine
+// when every problem's tiles are narrow, so a CTA that streams weights alone
+// keeps more bytes in flight.  Warp 1 issues tcgen05.mma (M 128, N = BN <=
+// 256, K 16) into one of two TMEM accumulators, so the epilogue of one unit
+// overlaps the MMAs of the next; warps 2-9 read the accumulator back with
+// tcgen05.ld (two warps per TMEM lane quadrant, splitting the 32-column
+// chunks) and store converted rows.
 #include <cuda.h>
+
+#include <cstring>
 
 #include "kp_common.cuh"
 #include "kp_internal.h"
@@ -32,24 +38,38 @@ namespace {
 constexpr int kGmM = 128;                       // rows per tile (MMA M)
 constexpr int kGmMaxN = 256;                    // columns per tile (MMA N max)
 constexpr int kGmK = 64;                        // K per stage: one 128-byte swizzle row of bf16
-constexpr int kGmStages = 4;
 constexpr int kGmABytes = kGmM * 128;           // 16 KB
-constexpr int kGmBBytes = kGmMaxN * 128;        // 32 KB
-constexpr int kGmStageBytes = kGmABytes + kGmBBytes;
+constexpr int kGmRingBytes = 4 * (kGmABytes + kGmMaxN * 128);   // 192 KB: four stages at BN 256
+constexpr int kGmMaxStages = 12;
+constexpr int kGmMaxProblems = 4;
 constexpr int kGmEpiThreads = 256;
 constexpr int kGmThreads = 64 + kGmEpiThreads;
-constexpr int kGmNumBars = 2 * kGmStages + 4 + 1;
-constexpr int kGmSmemBytes = kGmStages * kGmStageBytes + kGmNumBars * 8 + 1024;
+constexpr int kGmNumBars = 2 * kGmMaxStages + 4 + 1;
+constexpr int kGmSmemBytes = kGmRingBytes + kGmNumBars * 8 + 1024;
 
-struct GemmParams {
+// One product of a launch.  Its units are unit0 .. unit0 + batch * m_tiles *
+// n_tiles - 1, in the order batch, column tile, row tile (row tiles of one
+// column tile run on neighbouring CTAs and share the B tile in L2).
+struct GemmProblem {
     int m, n, k, batch;
     int bn;                      // columns per tile (multiple of 32, <= 256)
-    int m_tiles, n_tiles;
+    int m_tiles, n_tiles, unit0;
     int64_t a_batch_off;         // A columns between batches
     int64_t b_batch_off;         // B rows between batches
     void *c;
     int64_t ldc, c_batch_off;    // C row pitch and columns between batches (elements)
     int c_f32;                   // 1: fp32 output, 0: bf16
+};
+
+struct GemmMaps {
+    CUtensorMap a[kGmMaxProblems], b[kGmMaxProblems];
+};
+
+struct GemmParams {
+    GemmProblem pr[kGmMaxProblems];
+    int n_problems, units;
+    int stages;                  // ring stages (<= kGmMaxStages)
+    uint32_t stage_bytes;        // A tile + the widest B tile, a multiple of 1024
     unsigned long long wait_ns;
     int32_t *status;
 };
@@ -68,7 +88,7 @@ __device__ __forceinline__ bool gm_epi_bar_all(bool v) {
 }
 
 // Stores columns col0 .. col0 + 31 (clipped to n) of one row of batch b.
-__device__ __forceinline__ void store_row_chunk(const GemmParams &P, int b, int row, int col0,
+__device__ __forceinline__ void store_row_chunk(const GemmProblem &P, int b, int row, int col0,
                                                 const uint32_t (&r)[32]) {
     const int64_t off = static_cast<int64_t>(row) * P.ldc + b * P.c_batch_off + col0;
     const int ncol = min(32, P.n - col0);
@@ -103,24 +123,24 @@ __device__ __forceinline__ void store_row_chunk(const GemmParams &P, int b, int 
 }
 
 __global__ void __launch_bounds__(kGmThreads, 1)
-    gemm_bf16_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                     GemmParams P) {
+    gemm_bf16_kernel(const __grid_constant__ GemmMaps M, const __grid_constant__ GemmParams P) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint32_t tmem_base_s;
     __shared__ int abort_s;
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
     const uint32_t s0 = smem_u32(smem);
-    const uint32_t bar0 = s0 + kGmStages * kGmStageBytes;
+    const uint32_t bar0 = s0 + kGmRingBytes;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
-    auto empty_bar = [&](int s) { return bar0 + 8u * (kGmStages + s); };
-    auto accf_bar = [&](int a) { return bar0 + 8u * (2 * kGmStages + a); };
-    auto acce_bar = [&](int a) { return bar0 + 8u * (2 * kGmStages + 2 + a); };
-    const uint32_t drain_bar = bar0 + 8u * (2 * kGmStages + 4);
+    auto empty_bar = [&](int s) { return bar0 + 8u * (kGmMaxStages + s); };
+    auto accf_bar = [&](int a) { return bar0 + 8u * (2 * kGmMaxStages + a); };
+    auto acce_bar = [&](int a) { return bar0 + 8u * (2 * kGmMaxStages + 2 + a); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * kGmMaxStages + 4);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int stages = P.stages;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kGmStages; ++s) {
+        for (int s = 0; s < kGmMaxStages; ++s) {
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
         }
@@ -131,8 +151,10 @@ __global__ void __launch_bounds__(kGmThreads, 1)
         mbar_init(drain_bar, 1);
         fence_mbar_init();
         abort_s = 0;
-        tma_prefetch_desc(&tm_a);
-        tma_prefetch_desc(&tm_b);
+        for (int p = 0; p < P.n_problems; ++p) {
+            tma_prefetch_desc(&M.a[p]);
+            tma_prefetch_desc(&M.b[p]);
+        }
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(&tmem_base_s), 512);
@@ -144,62 +166,69 @@ __global__ void __launch_bounds__(kGmThreads, 1)
     pdl_wait_then_release();
     const uint32_t tmem = tmem_base_s;
     volatile int *abort_flag = &abort_s;
-    const int units = P.batch * P.m_tiles * P.n_tiles;
-    const int k_steps = P.k / kGmK;
-    // unit u: batch, then column tile, then row tile (row tiles of one column
-    // tile run on neighbouring CTAs and share the B tile in L2)
-    auto decode = [&](int u, int &b, int &mt, int &nt) {
-        mt = u % P.m_tiles;
-        const int r = u / P.m_tiles;
-        nt = r % P.n_tiles;
-        b = r / P.n_tiles;
+    // unit u -> problem p, batch b, row tile mt, column tile nt
+    auto decode = [&](int u, int &p, int &b, int &mt, int &nt) {
+        p = 0;
+        while (p + 1 < P.n_problems && u >= P.pr[p + 1].unit0) ++p;
+        const GemmProblem &g = P.pr[p];
+        const int v = u - g.unit0;
+        mt = v % g.m_tiles;
+        const int r = v / g.m_tiles;
+        nt = r % g.n_tiles;
+        b = r / g.n_tiles;
     };
 
     if (warp == 0) {
         if (lane == 0) {
-            int stage = 0, a_phase[kGmStages];
+            int stage = 0, a_phase[kGmMaxStages];
             uint32_t phase = 0;
-            for (int i = 0; i < kGmStages; ++i) a_phase[i] = -1;
+            for (int i = 0; i < kGmMaxStages; ++i) a_phase[i] = -1;
             bool ok = true;
-            const uint32_t bytes = kGmABytes + static_cast<uint32_t>(P.bn) * 128u;
-            for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
-                int b, mt, nt;
-                decode(u, b, mt, nt);
+            for (int u = blockIdx.x; ok && u < P.units; u += gridDim.x) {
+                int p, b, mt, nt;
+                decode(u, p, b, mt, nt);
+                const GemmProblem &g = P.pr[p];
+                const uint32_t bytes = kGmABytes + static_cast<uint32_t>(g.bn) * 128u;
                 const int ya = mt * kGmM;
-                const int yb = static_cast<int>(b * P.b_batch_off) + nt * P.bn;
+                const int yb = static_cast<int>(b * g.b_batch_off) + nt * g.bn;
+                const int k_steps = g.k / kGmK;
                 for (int ks = 0; ks < k_steps; ++ks) {
                     if (!mbar_wait(empty_bar(stage), phase ^ 1, abort_flag, P.status, P.wait_ns)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t dst = s0 + stage * kGmStageBytes;
+                    const uint32_t dst = s0 + static_cast<uint32_t>(stage) * P.stage_bytes;
                     mbar_expect_tx(full_bar(stage), bytes);
-                    tma_load_2d(dst, &tm_a, full_bar(stage), static_cast<int>(b * P.a_batch_off) + ks * kGmK, ya);
-                    tma_load_2d(dst + kGmABytes, &tm_b, full_bar(stage), ks * kGmK, yb);
+                    tma_load_2d(dst, &M.a[p], full_bar(stage), static_cast<int>(b * g.a_batch_off) + ks * kGmK, ya);
+                    tma_load_2d(dst + kGmABytes, &M.b[p], full_bar(stage), ks * kGmK, yb);
                     a_phase[stage] = static_cast<int>(phase);
-                    if (++stage == kGmStages) {
+                    if (++stage == stages) {
                         stage = 0;
                         phase ^= 1;
                     }
                 }
             }
             if (!ok)  // gave up: every load issued lands before the CTA goes away
-                for (int i = 0; i < kGmStages; ++i)
+                for (int i = 0; i < kGmMaxStages; ++i)
                     if (a_phase[i] >= 0) mbar_wait(full_bar(i), static_cast<uint32_t>(a_phase[i]), nullptr, P.status);
         }
     } else if (warp == 1) {
         if (lane == 0) {
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
-            const uint32_t idesc = idesc_bf16_f32(kGmM, P.bn);
             bool ok = true;
-            for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+            for (int u = blockIdx.x; ok && u < P.units; u += gridDim.x) {
+                int p, b, mt, nt;
+                decode(u, p, b, mt, nt);
+                const GemmProblem &g = P.pr[p];
+                const uint32_t idesc = idesc_bf16_f32(kGmM, g.bn);
+                const int k_steps = g.k / kGmK;
                 if (!(ok = mbar_wait(acce_bar(acc), acc_phase ^ 1, abort_flag, P.status, P.wait_ns))) break;
                 const uint32_t d_tmem = tmem + acc * kGmMaxN;
                 for (int ks = 0; ks < k_steps; ++ks) {
                     if (!(ok = mbar_wait(full_bar(stage), phase, abort_flag, P.status, P.wait_ns))) break;
                     tc_fence_after();
-                    const uint32_t a_base = s0 + stage * kGmStageBytes;
+                    const uint32_t a_base = s0 + static_cast<uint32_t>(stage) * P.stage_bytes;
 #pragma unroll
                     for (int kk = 0; kk < kGmK / 16; ++kk) {
                         const uint64_t ad = desc_kmajor_sw128(a_base + kk * 32);
@@ -207,7 +236,7 @@ __global__ void __launch_bounds__(kGmThreads, 1)
                         tc_mma_bf16(d_tmem, ad, bd, idesc, (ks | kk) ? 1u : 0u);
                     }
                     tc_commit(empty_bar(stage));
-                    if (++stage == kGmStages) {
+                    if (++stage == stages) {
                         stage = 0;
                         phase ^= 1;
                     }
@@ -230,19 +259,20 @@ __global__ void __launch_bounds__(kGmThreads, 1)
         const int quad = warp & 3, et = threadIdx.x - 64, half = et >> 7;
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int u = blockIdx.x; u < units; u += gridDim.x) {
-            int b, mt, nt;
-            decode(u, b, mt, nt);
+        for (int u = blockIdx.x; u < P.units; u += gridDim.x) {
+            int p, b, mt, nt;
+            decode(u, p, b, mt, nt);
+            const GemmProblem &g = P.pr[p];
             if (!gm_epi_bar_all(mbar_wait(accf_bar(acc), acc_phase, abort_flag, P.status, P.wait_ns))) break;
             tc_fence_after();
             const int row = mt * kGmM + quad * 32 + lane;
             const uint32_t tbase = tmem + acc * kGmMaxN + (static_cast<uint32_t>(quad * 32) << 16);
-            for (int ch = half; ch < P.bn / 32; ch += 2) {
+            for (int ch = half; ch < g.bn / 32; ch += 2) {
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(tbase + ch * 32, r);
                 tmem_ld_wait();
-                const int col0 = nt * P.bn + ch * 32;  // column inside the batch
-                if (row < P.m && col0 < P.n) store_row_chunk(P, b, row, col0, r);
+                const int col0 = nt * g.bn + ch * 32;  // column inside the batch
+                if (row < g.m && col0 < g.n) store_row_chunk(g, b, row, col0, r);
             }
             tc_fence_before();
             mbar_arrive(acce_bar(acc));
@@ -263,59 +293,84 @@ __global__ void __launch_bounds__(kGmThreads, 1)
 
 }  // namespace
 
-kp_status launch_gemm(const kp_gemm_args &g, cudaStream_t s) {
-    if (g.m == 0 || g.n == 0) return KP_OK;
+kp_status launch_gemm_group(const kp_gemm_args *gs, int count, cudaStream_t s) {
+    if (count < 1 || count > kGmMaxProblems) return KP_ERR_INVALID_ARG;
     const int sms = device_sm_count();
     if (sms <= 0) return KP_ERR_CUDA;
-    // Columns per tile (a multiple of 32, <= 256): the width whose waves of
-    // units cost least, a unit's cost taken as (64 + bn) -- its MMA and B
-    // bytes grow with bn, its A tile and fixed costs do not.  Large products
-    // keep 256; a product of few rows (decode) takes narrow tiles so that
-    // every SM streams a share of the weights instead of a few SMs all of it.
-    const int64_t m_tiles = (g.m + kGmM - 1) / kGmM;
-    int bn = 32;
-    int64_t best = -1;
-    for (int cand = kGmMaxN; cand >= 32; cand /= 2) {
-        const int64_t units = static_cast<int64_t>(g.batch) * m_tiles * ((g.n + cand - 1) / cand);
-        const int64_t cost = (units + sms - 1) / sms * (64 + cand);
-        if (best < 0 || cost < best) {
-            best = cost;
-            bn = cand;
+    GemmMaps maps;
+    GemmParams P;
+    std::memset(&maps, 0, sizeof maps);
+    std::memset(&P, 0, sizeof P);
+    int64_t units = 0;
+    uint32_t widest = 0;
+    for (int i = 0; i < count; ++i) {
+        const kp_gemm_args &g = gs[i];
+        if (g.m == 0 || g.n == 0) continue;
+        // Columns per tile (a multiple of 32, <= 256): the width whose waves of
+        // units cost least, a unit's cost taken as (64 + bn) -- its MMA and B
+        // bytes grow with bn, its A tile and fixed costs do not.  Large products
+        // keep 256; a product of few rows (decode) takes narrow tiles so that
+        // every SM streams a share of the weights instead of a few SMs all of it.
+        const int64_t m_tiles = (g.m + kGmM - 1) / kGmM;
+        int bn = 32;
+        int64_t best = -1;
+        for (int cand = kGmMaxN; cand >= 32; cand /= 2) {
+            const int64_t u = static_cast<int64_t>(g.batch) * m_tiles * ((g.n + cand - 1) / cand);
+            const int64_t cost = (u + sms - 1) / sms * (64 + cand);
+            if (best < 0 || cost < best) {
+                best = cost;
+                bn = cand;
+            }
+        }
+        const int p = P.n_problems++;
+        const uint64_t a_cols = static_cast<uint64_t>(g.a_batch_off) * (g.batch - 1) + g.k;
+        const uint64_t b_rows = static_cast<uint64_t>(g.b_batch_off) * (g.batch - 1) + g.n;
+        if (!make_tmap_bf16_sw128(&maps.a[p], g.a, a_cols, static_cast<uint64_t>(g.m),
+                                  static_cast<uint64_t>(g.lda) * 2, kGmK, kGmM) ||
+            !make_tmap_bf16_sw128(&maps.b[p], g.b, static_cast<uint64_t>(g.k), b_rows,
+                                  static_cast<uint64_t>(g.ldb) * 2, kGmK, static_cast<uint32_t>(bn)))
+            return KP_ERR_CUDA;
+        GemmProblem &q = P.pr[p];
+        q.m = g.m;
+        q.n = g.n;
+        q.k = g.k;
+        q.batch = g.batch;
+        q.bn = bn;
+        q.m_tiles = static_cast<int>(m_tiles);
+        q.n_tiles = (g.n + bn - 1) / bn;
+        q.unit0 = static_cast<int>(units);
+        q.a_batch_off = g.a_batch_off;
+        q.b_batch_off = g.b_batch_off;
+        q.c = g.c;
+        q.ldc = g.ldc;
+        q.c_batch_off = g.c_batch_off;
+        q.c_f32 = g.c_dtype == KP_DTYPE_F32 ? 1 : 0;
+        units += static_cast<int64_t>(g.batch) * q.m_tiles * q.n_tiles;
+        const uint32_t stage = static_cast<uint32_t>(kGmABytes) + static_cast<uint32_t>(bn) * 128u;
+        if (stage > widest) widest = stage;
+        // the first problem's limits stand for the launch (every problem of a
+        // call carries the same wait limit and status word)
+        if (p == 0) {
+            P.wait_ns = wait_limit_ns(g.wait_limit_us);
+            P.status = g.d_status;
         }
     }
-    CUtensorMap tm_a, tm_b;
-    const uint64_t a_cols = static_cast<uint64_t>(g.a_batch_off) * (g.batch - 1) + g.k;
-    const uint64_t b_rows = static_cast<uint64_t>(g.b_batch_off) * (g.batch - 1) + g.n;
-    if (!make_tmap_bf16_sw128(&tm_a, g.a, a_cols, static_cast<uint64_t>(g.m), static_cast<uint64_t>(g.lda) * 2,
-                              kGmK, kGmM) ||
-        !make_tmap_bf16_sw128(&tm_b, g.b, static_cast<uint64_t>(g.k), b_rows, static_cast<uint64_t>(g.ldb) * 2, kGmK,
-                              static_cast<uint32_t>(bn)))
-        return KP_ERR_CUDA;
+    if (P.n_problems == 0) return KP_OK;
+    if (units > INT32_MAX) return KP_ERR_UNSUPPORTED;
+    P.units = static_cast<int>(units);
+    P.stage_bytes = widest;   // 16 KB + a multiple of 4 KB: every stage starts 1024-aligned
+    P.stages = static_cast<int>(kGmRingBytes / widest);
+    if (P.stages > kGmMaxStages) P.stages = kGmMaxStages;
     cudaError_t e = cudaFuncSetAttribute(gemm_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGmSmemBytes);
     if (e != cudaSuccess) {
         record_cuda_error("cudaFuncSetAttribute(gemm_bf16_kernel)", e);
         return KP_ERR_CUDA;
     }
-    GemmParams P;
-    P.m = g.m;
-    P.n = g.n;
-    P.k = g.k;
-    P.batch = g.batch;
-    P.bn = bn;
-    P.m_tiles = (g.m + kGmM - 1) / kGmM;
-    P.n_tiles = (g.n + bn - 1) / bn;
-    P.a_batch_off = g.a_batch_off;
-    P.b_batch_off = g.b_batch_off;
-    P.c = g.c;
-    P.ldc = g.ldc;
-    P.c_batch_off = g.c_batch_off;
-    P.c_f32 = g.c_dtype == KP_DTYPE_F32 ? 1 : 0;
-    P.wait_ns = wait_limit_ns(g.wait_limit_us);
-    P.status = g.d_status;
-    const int64_t units = static_cast<int64_t>(g.batch) * P.m_tiles * P.n_tiles;
     const int grid = static_cast<int>(units < sms ? units : sms);
     return launch_kernel("gemm_bf16_kernel", gemm_bf16_kernel, LaunchCfg(dim3(grid), dim3(kGmThreads), kGmSmemBytes, s),
-                         tm_a, tm_b, P);
+                         maps, P);
 }
+
+kp_status launch_gemm(const kp_gemm_args &g, cudaStream_t s) { return launch_gemm_group(&g, 1, s); }
 
 }  // namespace kp

@@ -119,6 +119,9 @@ kp_status launch_score_select(const kp_score_args &sc, const kp_topk_args &tk, c
 kp_status score_with_workspace_plan(const kp_score_args *a, cudaStream_t stream);
 kp_status launch_attend(const kp_attend_args &a, cudaStream_t s);
 kp_status launch_gemm(const kp_gemm_args &g, cudaStream_t s);
+// Up to four independent products (validated, none reading another's output)
+// in one launch.
+kp_status launch_gemm_group(const kp_gemm_args *gs, int count, cudaStream_t s);
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 

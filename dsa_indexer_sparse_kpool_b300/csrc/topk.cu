@@ -48,11 +48,10 @@ __global__ void __launch_bounds__(kTkThreads, 1)
     topk_select_kernel(const float *__restrict__ scores, int64_t stride,
                        const int32_t *__restrict__ q_pos, int kshift, int K, int32_t *__restrict__ pool_idx,
                        int32_t *__restrict__ n_sel, int chunk_cap, int32_t *status) {
-    constexpr int kTkWarps = kTkThreads / 32;
     extern __shared__ __align__(16) uint32_t keys[];
     __shared__ __align__(16) TopkShared sh;
 
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x;
     const uint32_t rank = cluster_ctarank(), C = cluster_size();
     const int q = blockIdx.x / C;
     // A one-CTA row needs only block barriers.
