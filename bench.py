@@ -148,7 +148,8 @@ def kernel_traffic(stage: str, workload_name: str):
     sha = kernel_source_hash(stage)
     for line in open(p):
         f = line.split()
-        if len(f) >= 5 and not line.startswith("#") and f[0] == stage and f[2] == workload_name and f[4] == sha:
+        # stage kernel workload bytes_per_launch ... source_sha
+        if len(f) >= 5 and not line.startswith("#") and f[0] == stage and f[2] == workload_name and f[-1] == sha:
             return int(f[3])
     return None
 
