@@ -149,6 +149,14 @@ def test_fused_over_1022_queries_small():
     PL.fused_check(wl, queries=qs)
 
 
+def test_few_queries_full_budget_widest_split():
+    # 3 queries with the full 2048-token budget: each query's 32 tiles go to a
+    # cluster of 8 CTAs (4 tiles each), whose merge gives every CTA 8 heads;
+    # one query has a 3-token tail.
+    wl = KI.make(small_spec([9000, 12003], [1, 2], 2048, seed=33))
+    PL.fused_check(wl)
+
+
 def test_exact_ties_in_scores():
     # sequence 0: every pool identical -> all 5000 scores equal (the radix
     # levels run down to a single key value shared by every pool); sequence 1:
