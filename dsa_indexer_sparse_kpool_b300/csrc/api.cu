@@ -171,6 +171,30 @@ bool make_tmap_bf16_sw128(CUtensorMap *m, const void *base, uint64_t inner, uint
     return true;
 }
 
+bool make_tmap_bf16_sw128_kblocks(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows,
+                                  uint64_t row_bytes, uint32_t box_rows, uint32_t kblocks) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) {
+        record_error_text("cuTensorMapEncodeTiled is not available");
+        return false;
+    }
+    if (cols % 64 != 0) return false;
+    // (64 columns, rows, column blocks of 64): a box of kblocks blocks lands as
+    // kblocks consecutive [box_rows][128 B] slabs
+    cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(cols / 64)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(row_bytes), 128};
+    cuuint32_t box[3] = {64, box_rows, kblocks};
+    cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        record_error_text("cuTensorMapEncodeTiled (column blocks) failed");
+        return false;
+    }
+    return true;
+}
+
 int device_sm_count() {
     int dev = 0, n = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;

@@ -40,12 +40,15 @@ constexpr int kGmMaxN = 256;                    // columns per tile (MMA N max)
 constexpr int kGmK = 64;                        // K per stage: one 128-byte swizzle row of bf16
 constexpr int kGmABytes = kGmM * 128;           // 16 KB
 constexpr int kGmRingBytes = 4 * (kGmABytes + kGmMaxN * 128);   // 192 KB: four stages at BN 256
-constexpr int kGmMaxStages = 12;
+constexpr int kGmMaxStages = 24;
 constexpr int kGmMaxProblems = 4;
 constexpr int kGmEpiThreads = 256;
 constexpr int kGmThreads = 64 + kGmEpiThreads;
 constexpr int kGmNumBars = 2 * kGmMaxStages + 4 + 1;
-constexpr int kGmSmemBytes = kGmRingBytes + kGmNumBars * 8 + 1024;
+// The MMA reads a 128-row A window from each stage; with fewer A rows loaded
+// the window runs past the stage (rows >= m only feed output rows that are never
+// stored), so the ring is followed by one A tile of slack.
+constexpr int kGmSmemBytes = kGmRingBytes + kGmABytes + kGmNumBars * 8 + 1024;
 
 // One product of a launch.  Its units are unit0 .. unit0 + batch * m_tiles *
 // n_tiles - 1, in the order batch, column tile, row tile (row tiles of one
@@ -69,7 +72,9 @@ struct GemmParams {
     GemmProblem pr[kGmMaxProblems];
     int n_problems, units;
     int stages;                  // ring stages (<= kGmMaxStages)
-    uint32_t stage_bytes;        // A tile + the widest B tile, a multiple of 1024
+    uint32_t a_bytes;            // A rows loaded per K block x 128 (rows a multiple of 8, <= 128)
+    int kb;                      // 64-wide K blocks per stage (one TMA box each for A and B when > 1)
+    uint32_t stage_bytes;        // kb x (a_bytes + the widest B tile), a multiple of 1024
     unsigned long long wait_ns;
     int32_t *status;
 };
@@ -130,7 +135,7 @@ __global__ void __launch_bounds__(kGmThreads, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
     const uint32_t s0 = smem_u32(smem);
-    const uint32_t bar0 = s0 + kGmRingBytes;
+    const uint32_t bar0 = s0 + kGmRingBytes + kGmABytes;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (kGmMaxStages + s); };
     auto accf_bar = [&](int a) { return bar0 + 8u * (2 * kGmMaxStages + a); };
@@ -188,10 +193,12 @@ __global__ void __launch_bounds__(kGmThreads, 1)
                 int p, b, mt, nt;
                 decode(u, p, b, mt, nt);
                 const GemmProblem &g = P.pr[p];
-                const uint32_t bytes = kGmABytes + static_cast<uint32_t>(g.bn) * 128u;
+                const uint32_t b_blk = static_cast<uint32_t>(g.bn) * 128u;
+                const uint32_t bytes = static_cast<uint32_t>(P.kb) * (P.a_bytes + b_blk);
                 const int ya = mt * kGmM;
                 const int yb = static_cast<int>(b * g.b_batch_off) + nt * g.bn;
-                const int k_steps = g.k / kGmK;
+                const int a_blk0 = static_cast<int>(b * g.a_batch_off) / kGmK;   // A's first K block of batch b
+                const int k_steps = g.k / (kGmK * P.kb);
                 for (int ks = 0; ks < k_steps; ++ks) {
                     if (!mbar_wait(empty_bar(stage), phase ^ 1, abort_flag, P.status, P.wait_ns)) {
                         ok = false;
@@ -199,8 +206,13 @@ __global__ void __launch_bounds__(kGmThreads, 1)
                     }
                     const uint32_t dst = s0 + static_cast<uint32_t>(stage) * P.stage_bytes;
                     mbar_expect_tx(full_bar(stage), bytes);
-                    tma_load_2d(dst, &M.a[p], full_bar(stage), static_cast<int>(b * g.a_batch_off) + ks * kGmK, ya);
-                    tma_load_2d(dst + kGmABytes, &M.b[p], full_bar(stage), ks * kGmK, yb);
+                    if (P.kb == 1) {
+                        tma_load_2d(dst, &M.a[p], full_bar(stage), static_cast<int>(b * g.a_batch_off) + ks * kGmK, ya);
+                        tma_load_2d(dst + P.a_bytes, &M.b[p], full_bar(stage), ks * kGmK, yb);
+                    } else {  // kb K blocks per box: [kb][rows][128 B] slabs, A's then B's
+                        tma_load_3d(dst, &M.a[p], full_bar(stage), 0, ya, a_blk0 + ks * P.kb);
+                        tma_load_3d(dst + P.kb * P.a_bytes, &M.b[p], full_bar(stage), 0, yb, ks * P.kb);
+                    }
                     a_phase[stage] = static_cast<int>(phase);
                     if (++stage == stages) {
                         stage = 0;
@@ -222,18 +234,22 @@ __global__ void __launch_bounds__(kGmThreads, 1)
                 decode(u, p, b, mt, nt);
                 const GemmProblem &g = P.pr[p];
                 const uint32_t idesc = idesc_bf16_f32(kGmM, g.bn);
-                const int k_steps = g.k / kGmK;
+                const uint32_t b_blk = static_cast<uint32_t>(g.bn) * 128u;
+                const int k_steps = g.k / (kGmK * P.kb);
                 if (!(ok = mbar_wait(acce_bar(acc), acc_phase ^ 1, abort_flag, P.status, P.wait_ns))) break;
                 const uint32_t d_tmem = tmem + acc * kGmMaxN;
                 for (int ks = 0; ks < k_steps; ++ks) {
                     if (!(ok = mbar_wait(full_bar(stage), phase, abort_flag, P.status, P.wait_ns))) break;
                     tc_fence_after();
                     const uint32_t a_base = s0 + static_cast<uint32_t>(stage) * P.stage_bytes;
+                    const uint32_t b_base = a_base + static_cast<uint32_t>(P.kb) * P.a_bytes;
+                    for (int j = 0; j < P.kb; ++j) {
 #pragma unroll
-                    for (int kk = 0; kk < kGmK / 16; ++kk) {
-                        const uint64_t ad = desc_kmajor_sw128(a_base + kk * 32);
-                        const uint64_t bd = desc_kmajor_sw128(a_base + kGmABytes + kk * 32);
-                        tc_mma_bf16(d_tmem, ad, bd, idesc, (ks | kk) ? 1u : 0u);
+                        for (int kk = 0; kk < kGmK / 16; ++kk) {
+                            const uint64_t ad = desc_kmajor_sw128(a_base + j * P.a_bytes + kk * 32);
+                            const uint64_t bd = desc_kmajor_sw128(b_base + j * b_blk + kk * 32);
+                            tc_mma_bf16(d_tmem, ad, bd, idesc, (ks | j | kk) ? 1u : 0u);
+                        }
                     }
                     tc_commit(empty_bar(stage));
                     if (++stage == stages) {
@@ -303,6 +319,28 @@ kp_status launch_gemm_group(const kp_gemm_args *gs, int count, cudaStream_t s) {
     std::memset(&P, 0, sizeof P);
     int64_t units = 0;
     uint32_t widest = 0;
+    // A rows loaded per stage: a product of at most 128 rows loads only its rows
+    // (rounded up to 8, one swizzle atom), which leaves ring room for more stages.
+    int a_rows = 8;
+    for (int i = 0; i < count; ++i) {
+        const kp_gemm_args &g = gs[i];
+        if (g.m == 0 || g.n == 0) continue;
+        const int r = g.m > kGmM ? kGmM : (g.m + 7) / 8 * 8;
+        if (r > a_rows) a_rows = r;
+    }
+    const uint32_t a_bytes = static_cast<uint32_t>(a_rows) * 128u;
+    // K blocks per stage: with few rows the tiles are small, and the TMA box
+    // count, not the bytes, sets the pace; a box then carries four 64-wide K
+    // blocks (fewer where K or a batch offset does not divide).
+    int kb = 1;
+    if (a_rows < kGmM) {
+        kb = 4;
+        for (int i = 0; i < count; ++i) {
+            const kp_gemm_args &g = gs[i];
+            if (g.m == 0 || g.n == 0) continue;
+            while (kb > 1 && ((g.k / kGmK) % kb != 0 || g.a_batch_off % kGmK != 0)) kb /= 2;
+        }
+    }
     for (int i = 0; i < count; ++i) {
         const kp_gemm_args &g = gs[i];
         if (g.m == 0 || g.n == 0) continue;
@@ -325,11 +363,18 @@ kp_status launch_gemm_group(const kp_gemm_args *gs, int count, cudaStream_t s) {
         const int p = P.n_problems++;
         const uint64_t a_cols = static_cast<uint64_t>(g.a_batch_off) * (g.batch - 1) + g.k;
         const uint64_t b_rows = static_cast<uint64_t>(g.b_batch_off) * (g.batch - 1) + g.n;
-        if (!make_tmap_bf16_sw128(&maps.a[p], g.a, a_cols, static_cast<uint64_t>(g.m),
-                                  static_cast<uint64_t>(g.lda) * 2, kGmK, kGmM) ||
-            !make_tmap_bf16_sw128(&maps.b[p], g.b, static_cast<uint64_t>(g.k), b_rows,
-                                  static_cast<uint64_t>(g.ldb) * 2, kGmK, static_cast<uint32_t>(bn)))
-            return KP_ERR_CUDA;
+        const bool ok =
+            kb == 1 ? make_tmap_bf16_sw128(&maps.a[p], g.a, a_cols, static_cast<uint64_t>(g.m),
+                                           static_cast<uint64_t>(g.lda) * 2, kGmK, static_cast<uint32_t>(a_rows)) &&
+                          make_tmap_bf16_sw128(&maps.b[p], g.b, static_cast<uint64_t>(g.k), b_rows,
+                                               static_cast<uint64_t>(g.ldb) * 2, kGmK, static_cast<uint32_t>(bn))
+                    : make_tmap_bf16_sw128_kblocks(&maps.a[p], g.a, a_cols, static_cast<uint64_t>(g.m),
+                                                   static_cast<uint64_t>(g.lda) * 2, static_cast<uint32_t>(a_rows),
+                                                   static_cast<uint32_t>(kb)) &&
+                          make_tmap_bf16_sw128_kblocks(&maps.b[p], g.b, static_cast<uint64_t>(g.k), b_rows,
+                                                       static_cast<uint64_t>(g.ldb) * 2, static_cast<uint32_t>(bn),
+                                                       static_cast<uint32_t>(kb));
+        if (!ok) return KP_ERR_CUDA;
         GemmProblem &q = P.pr[p];
         q.m = g.m;
         q.n = g.n;
@@ -346,7 +391,7 @@ kp_status launch_gemm_group(const kp_gemm_args *gs, int count, cudaStream_t s) {
         q.c_batch_off = g.c_batch_off;
         q.c_f32 = g.c_dtype == KP_DTYPE_F32 ? 1 : 0;
         units += static_cast<int64_t>(g.batch) * q.m_tiles * q.n_tiles;
-        const uint32_t stage = static_cast<uint32_t>(kGmABytes) + static_cast<uint32_t>(bn) * 128u;
+        const uint32_t stage = static_cast<uint32_t>(kb) * (a_bytes + static_cast<uint32_t>(bn) * 128u);
         if (stage > widest) widest = stage;
         // the first problem's limits stand for the launch (every problem of a
         // call carries the same wait limit and status word)
@@ -358,7 +403,9 @@ kp_status launch_gemm_group(const kp_gemm_args *gs, int count, cudaStream_t s) {
     if (P.n_problems == 0) return KP_OK;
     if (units > INT32_MAX) return KP_ERR_UNSUPPORTED;
     P.units = static_cast<int>(units);
-    P.stage_bytes = widest;   // 16 KB + a multiple of 4 KB: every stage starts 1024-aligned
+    P.a_bytes = a_bytes;
+    P.kb = kb;
+    P.stage_bytes = widest;   // multiples of 1024 (A: 8-row atoms; B: 32-row tiles): stages stay 1024-aligned
     P.stages = static_cast<int>(kGmRingBytes / widest);
     if (P.stages > kGmMaxStages) P.stages = kGmMaxStages;
     cudaError_t e = cudaFuncSetAttribute(gemm_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGmSmemBytes);

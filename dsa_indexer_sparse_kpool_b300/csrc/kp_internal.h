@@ -31,6 +31,10 @@ int device_sm_count();
 // elements (box_inner * 2 <= 128).  False (error recorded) on failure.
 bool make_tmap_bf16_sw128(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows,
                           uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows);
+// The same matrix seen as (64 columns, rows, cols / 64 column blocks), boxes of
+// box_rows rows x kblocks blocks (cols a multiple of 64).
+bool make_tmap_bf16_sw128_kblocks(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows,
+                                  uint64_t row_bytes, uint32_t box_rows, uint32_t kblocks);
 
 // Launch configuration with programmatic stream serialisation (the kernel
 // may start while the previous kernel of the stream drains; it waits in
