@@ -63,6 +63,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--select", default="auto", choices=["auto", "staged", "fused"],
                     help="how the step scores and selects (fused: one kernel, scores kept on chip)")
+    ap.add_argument("--share-mtp", action="store_true",
+                    help="each sequence's later queries attend its first query's selection (shared selection)")
     ap.add_argument("--paged", type=int, default=0, metavar="TOKENS",
                     help="page the caches in pages of TOKENS positions (block table, shuffled pages)")
     return ap.parse_args()
@@ -356,6 +358,17 @@ def main():
     step = build_step(sess, wl.lens.tolist(), wl.prev_len.tolist(), wl.tok_off.tolist(), wl.keys, wl.gates,
                       wl.q_seq, wl.q_pos, wl.q_idx, wl.w, wl.q_lat)
     NQ = wl.NQ
+    if args.share_mtp:   # the MTP verification queries take their sequence's first query's selection
+        first = {}
+        share = []
+        for q in range(NQ):
+            b = int(wl.q_seq[q])
+            if b in first:
+                share.append(first[b])
+            else:
+                first[b] = q
+                share.append(-1)
+        step.set_share(share)
     stream = torch.cuda.Stream(device=dev)
     flush = torch.empty(256 << 18, dtype=torch.float32, device=dev).fill_(1.0)   # 256 MB > 126 MB L2
 
@@ -518,7 +531,9 @@ def main():
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                        "caches": f"paged, {args.paged}-token pages (block table)" if args.paged else "contiguous",
                        "select": ("fused: scores and top-k in one kernel, no score matrix" if fused else
-                                  "staged: score matrix in the workspace, then top-k"),
+                                  "staged: score matrix in the workspace, then top-k")
+                                 + ("; later queries of a sequence share its first query's selection"
+                                    if args.share_mtp else ""),
                        "l2": "flushed between timed steps (256 MB read)", "timing": "CUDA-graph replay, events"},
             "roofline": roof,
             "stage_roofline": stage_roof,

@@ -45,7 +45,7 @@ class kp_seqs(ctypes.Structure):
 
 
 class kp_queries(ctypes.Structure):
-    _fields_ = [("num_queries", _i32), ("q_seq", _vp), ("q_pos", _vp), ("max_pools", _i32)]
+    _fields_ = [("num_queries", _i32), ("q_seq", _vp), ("q_pos", _vp), ("max_pools", _i32), ("share_src", _vp)]
 
 
 class kp_compress_args(ctypes.Structure):
@@ -231,9 +231,11 @@ class Queries:
     q_seq: torch.Tensor     # [NQ] int32
     q_pos: torch.Tensor     # [NQ] int32
     max_pools: int          # upper bound of floor((q_pos + 1) / kpool)
+    share_src: Optional[torch.Tensor] = None   # [NQ] int32: query whose selection each query attends (-1: its own)
 
     def c(self) -> kp_queries:
-        return kp_queries(self.q_seq.numel(), _p(self.q_seq), _p(self.q_pos), int(self.max_pools))
+        return kp_queries(self.q_seq.numel(), _p(self.q_seq), _p(self.q_pos), int(self.max_pools),
+                          _p(self.share_src))
 
 
 def score_stride(max_pools: int) -> int:

@@ -618,7 +618,7 @@ kp_status kp_read_device_status(const int32_t *d_status, kp_stream_t stream) {
     return static_cast<kp_status>(v);
 }
 
-int kp_version(void) { return 20100; }
+int kp_version(void) { return 20200; }
 
 }  // extern "C"
 

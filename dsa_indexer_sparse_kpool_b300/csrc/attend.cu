@@ -157,6 +157,8 @@ struct AttendParams {
     int num_seqs;
     const int32_t *pool_idx;
     const int32_t *n_sel;
+    const int32_t *share_src;    // [nq] shared selection (nullptr: none)
+    int nq;
     int K;
     int tail;
     float scale_log2;
@@ -284,6 +286,22 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     if (qvalid && !paged && (base_row < 0 || base_row + t >= P.cmap.latent_rows)) qvalid = false;
     if (qvalid && paged && (t >> P.cmap.page_shift) >= P.cmap.blocks_per_seq) qvalid = false;
     if (!qvalid && tid == 0) set_status(P.status, KP_ERR_DEVICE_BOUNDS);
+    // The selection row this query attends: its own, or a shared source's (a
+    // query of the same sequence that selects for itself); a bad source leaves
+    // the query its tail alone.
+    int sel_row = q;
+    bool sel_ok = true;
+    if (qvalid && P.share_src) {
+        const int src = P.share_src[q];
+        if (src >= 0) {
+            if (src < P.nq && P.q_seq[src] == b && P.share_src[src] < 0) {
+                sel_row = src;
+            } else {
+                sel_ok = false;
+                if (tid == 0) set_status(P.status, KP_ERR_DEVICE_BOUNDS);
+            }
+        }
+    }
     const int nf = qvalid ? (t + 1) / KP : 0;
     const int n_tail = (qvalid && P.tail) ? (t + 1) - nf * KP : 0;
     tc_fence_before();
@@ -299,8 +317,8 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     // ---- the selection comes from the previous kernel
     pdl_wait_then_release();
     int ns = 0;
-    if (qvalid) {
-        ns = P.n_sel[q];
+    if (qvalid && sel_ok) {
+        ns = P.n_sel[sel_row];
         const int ns_max = min(P.K, nf);
         if (ns < 0 || ns > ns_max) {
             if (tid == 0) set_status(P.status, KP_ERR_DEVICE_BOUNDS);
@@ -419,7 +437,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         const bool active = j < 2 * kAtPoolsPerTile;
         const int pool0 = tb * kAtPoolsPerTile;
         const int npools = min(nt * kAtPoolsPerTile, ns - pool0);
-        const int32_t *plist = P.pool_idx + static_cast<int64_t>(q) * P.K + pool0 + my_pool;
+        const int32_t *plist = P.pool_idx + static_cast<int64_t>(sel_row) * P.K + pool0 + my_pool;
         auto want = [&](int t) -> bool { return active && t * kAtPoolsPerTile + my_pool < npools; };
         auto fetch_p = [&](int t) -> int { return want(t) ? plist[t * kAtPoolsPerTile] : -1; };
         // Raw block-table entry of pool p's page (checked where it is used), -2
@@ -895,6 +913,8 @@ kp_status launch_attend_kp(const kp_attend_args &a, cudaStream_t s) {
     P.num_seqs = a.seqs.num_seqs;
     P.pool_idx = a.pool_idx;
     P.n_sel = a.n_sel;
+    P.share_src = a.q.share_src;
+    P.nq = nq;
     P.K = a.cfg.topk_tokens / a.cfg.kpool;
     P.tail = a.cfg.always_select_tail ? 1 : 0;
     P.scale_log2 = a.cfg.sm_scale * 1.44269504088896340736f;

@@ -72,6 +72,7 @@ struct SsParams {
     const int32_t *q_seq;
     const int32_t *prev_len;   // tokens of each sequence before this step (nullptr: no early loads)
     const int32_t *q_pos;
+    const int32_t *share;      // [nq] shared selection (nullptr: none): shared rows are skipped
     const int32_t *seq_len;
     int kshift;
     const float *w;
@@ -373,8 +374,9 @@ __global__ void __launch_bounds__(kSsThreads, 1)
             const int row_n = (gvalid && rr < nqg) ? min(cap, (P.q_pos[row_q] + 1) >> P.kshift) : 0;
             __syncthreads();
             if (C > 1) cluster_barrier();
-            // read after the barrier: nothing sets the flag during the rounds
-            const bool own = rr < nqg && *abort_flag == 0;
+            // read after the barrier: nothing sets the flag during the rounds; a
+            // shared query's row is left as it was
+            const bool own = rr < nqg && *abort_flag == 0 && !(P.share && P.share[row_q] >= 0);
             if (own) {
                 int32_t *out = P.pool_idx + static_cast<int64_t>(row_q) * P.K;
                 if (row_n > P.K) {
@@ -527,6 +529,7 @@ kp_status launch_score_select(const kp_score_args &sc, const kp_topk_args &tk, c
     P.q_seq = sc.q.q_seq;
     P.prev_len = local_plan ? prev_len : nullptr;
     P.q_pos = sc.q.q_pos;
+    P.share = tk.q.share_src;
     P.seq_len = sc.seqs.seq_len;
     P.kshift = kpool_shift(sc.cfg.kpool);
     P.w = sc.w;

@@ -46,14 +46,18 @@ namespace {
 template <int kTkThreads>
 __global__ void __launch_bounds__(kTkThreads, 1)
     topk_select_kernel(const float *__restrict__ scores, int64_t stride,
-                       const int32_t *__restrict__ q_pos, int kshift, int K, int32_t *__restrict__ pool_idx,
-                       int32_t *__restrict__ n_sel, int chunk_cap, int32_t *status) {
+                       const int32_t *__restrict__ q_pos, const int32_t *__restrict__ share, int kshift, int K,
+                       int32_t *__restrict__ pool_idx, int32_t *__restrict__ n_sel, int chunk_cap, int32_t *status) {
     extern __shared__ __align__(16) uint32_t keys[];
     __shared__ __align__(16) TopkShared sh;
 
     const int tid = threadIdx.x;
     const uint32_t rank = cluster_ctarank(), C = cluster_size();
     const int q = blockIdx.x / C;
+    if (share && share[q] >= 0) {  // a shared query: its row is left as it was (every CTA of its cluster)
+        pdl_wait_then_release();
+        return;
+    }
     // A one-CTA row needs only block barriers.
     auto cbar = [&]() {
         if (C > 1) cluster_barrier();
@@ -160,7 +164,8 @@ kp_status launch_topk(const kp_topk_args &a, cudaStream_t s) {
     return launch_kernel("topk_select_kernel", kern,
                          LaunchCfg(dim3(static_cast<unsigned>(nq) * C), dim3(wide ? kTkMaxThreads : kTkMinThreads),
                                    smem, s, C),
-                         a.scores, a.score_stride, a.q.q_pos, kpool_shift(a.cfg.kpool), K, a.pool_idx, a.n_sel,
+                         a.scores, a.score_stride, a.q.q_pos, a.q.share_src, kpool_shift(a.cfg.kpool), K, a.pool_idx,
+                         a.n_sel,
                          chunk_cap, a.d_status);
 }
 

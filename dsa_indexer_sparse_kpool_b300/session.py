@@ -166,6 +166,13 @@ class Step:
     def run(self, stream=None) -> None:
         kp_dsa_forward(self.args, stream=stream)
 
+    def set_share(self, share_src) -> None:
+        """Shared selection: share_src[q] >= 0 makes query q attend that query's
+        selection instead of selecting its own (None: every query selects)."""
+        t = None if share_src is None else _dev_i32([int(x) for x in share_src], self.sess.device)
+        self.queries = Queries(self.queries.q_seq, self.queries.q_pos, self.queries.max_pools, t)
+        self.args = self._args(self.workspace)
+
     def pack_io(self):
         """Moves the step's per-step inputs (positions, new keys and gates,
         queries) into one device buffer and its outputs (out, lse) into
@@ -176,6 +183,9 @@ class Step:
         d = self.sess.device
         ins = [self.prev_len, self.new_off, self.keys, self.gates, self.queries.q_seq, self.queries.q_pos,
                self.q_idx, self.w, self.q_lat]
+        share = self.queries.share_src
+        if share is not None:
+            ins.append(share)
         outs = [self.out, self.lse]
 
         def carve(ts):
@@ -191,9 +201,9 @@ class Step:
                 views.append(v)
             return buf, views
 
-        in_buf, (self.prev_len, self.new_off, self.keys, self.gates, q_seq, q_pos, self.q_idx, self.w,
-                 self.q_lat) = carve(ins)
-        self.queries = Queries(q_seq, q_pos, self.queries.max_pools)
+        in_buf, views = carve(ins)
+        (self.prev_len, self.new_off, self.keys, self.gates, q_seq, q_pos, self.q_idx, self.w, self.q_lat) = views[:9]
+        self.queries = Queries(q_seq, q_pos, self.queries.max_pools, views[9] if share is not None else None)
         out_buf, (self.out, self.lse) = carve(outs)
         self.args = self._args(self.workspace)
         return in_buf, out_buf

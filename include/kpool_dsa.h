@@ -192,7 +192,20 @@ typedef struct kp_queries {
     const int32_t *q_pos;       /* [NQ] absolute position of each query */
     int32_t max_pools;          /* host: an upper bound of n_full(q_pos) over the queries,
                                    <= KP_MAX_SCORE_POOLS */
+    const int32_t *share_src;   /* [NQ] or NULL: shared selection (below) */
 } kp_queries;
+
+/* Shared selection (MAX docs, Glm5NextConfig.index_share_for_mtp_iteration,
+ * read for the MTP verification query of a step): share_src[q] >= 0 names the
+ * query whose selection query q attends, instead of its own.  The source must
+ * be a query of the same sequence that is not itself shared.  Then:
+ *  - kp_topk_select and kp_indexer_score_select skip query q: pool_idx[q] and
+ *    n_sel[q] are left as they were (kp_indexer_score still scores it);
+ *  - kp_sparse_mla_attend attends the source's pool_idx row and n_sel (pools
+ *    past q's own n_full are skipped and reported) plus q's own tail.
+ * A source out of range, in another sequence or itself shared is reported as
+ * KP_ERR_DEVICE_BOUNDS, and query q then attends its tail alone.
+ * share_src[q] < 0, or share_src NULL: q selects for itself. */
 
 /* ---- 1. pooled-key compression (fused into the indexer-cache write) ---- */
 /* For sequence b the new tokens are positions prev_len[b] .. prev_len[b] +
