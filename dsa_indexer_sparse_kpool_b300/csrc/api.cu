@@ -363,7 +363,7 @@ kp_status kp_dsa_forward(const kp_forward_args *a, kp_stream_t stream) {
     if (st != KP_OK) return st;
     if ((st = check_queries(a->q)) != KP_OK) return st;
     if ((st = check_seqs(a->seqs, a->cfg.kpool, true, true)) != KP_OK) return st;
-    if (!a->out) return KP_ERR_INVALID_ARG;
+    if (a->q.num_queries > 0 && !a->out) return KP_ERR_INVALID_ARG;   // no queries: nothing is written
     const int sms = device_sm_count();
     if (sms <= 0) {
         record_error_text("cannot query the current CUDA device");

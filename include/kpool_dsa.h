@@ -343,7 +343,7 @@ typedef struct kp_forward_args {
     const uint16_t *q_lat;
     const uint16_t *latent;
     /* outputs */
-    uint16_t *out;                /* [NQ][64][512] bf16 */
+    uint16_t *out;                /* [NQ][64][512] bf16 (may be NULL when NQ == 0) */
     float *lse;                   /* [NQ][64] fp32 (may be NULL) */
     int32_t *pool_idx;            /* [NQ][K] (may be NULL: kept in the workspace) */
     int32_t *n_sel;               /* [NQ]    (may be NULL: kept in the workspace) */
