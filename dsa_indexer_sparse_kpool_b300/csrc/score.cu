@@ -47,7 +47,12 @@ constexpr int kScEpiThreads = 256;                       // 8 epilogue warps, tw
 constexpr int kScThreads = 64 + kScEpiThreads;
 constexpr int kScTmemCols = 512;
 constexpr int kScAccCols = 256;
-constexpr int kScNumBars = 2 * kScStages + 4 + 2 + 2;  // + drain, never
+constexpr int kScNumBars = 2 * kScStages + 4 + 4 + 2;  // full, empty, acc x 4, queries full/empty x 2, drain, never
+// The queries' buffer: one 64 KB region for groups of up to 8 queries, or,
+// when no group has more than 4, two 32 KB slots used in turn, so that the next
+// group's queries load while the current group's MMAs still read its own.
+constexpr int kScBSlotBytes = kScBBytes / 2;                  // 32 KB
+constexpr int kScBSlotBlockBytes = kScBSlotBytes / 2;         // [128 rows][64 bf16] = 16 KB
 constexpr int kScPlanStage = 4096;                        // plan words held in shared memory
 constexpr int kScLocalPlanMaxQ = (kScPlanStage - 5) / 4;  // queries whose whole plan fits there
 constexpr int kScSmemBytes = kScStages * kScAStageBytes + kScBBytes + kScNumBars * 8 + kScPlanStage * 4 + 1024;
@@ -154,10 +159,10 @@ __global__ void __launch_bounds__(kScThreads, 1)
     auto empty_bar = [&](int s) { return bar0 + 8u * (kScStages + s); };
     auto accf_bar = [&](int a) { return bar0 + 8u * (2 * kScStages + a); };
     auto acce_bar = [&](int a) { return bar0 + 8u * (2 * kScStages + 2 + a); };
-    const uint32_t bfull_bar = bar0 + 8u * (2 * kScStages + 4);
-    const uint32_t bempty_bar = bar0 + 8u * (2 * kScStages + 5);
-    const uint32_t drain_bar = bar0 + 8u * (2 * kScStages + 6);  // MMAs issued before a give-up are done
-    const uint32_t never_bar = bar0 + 8u * (2 * kScStages + 7);  // nothing arrives (failure-path tests)
+    auto bfull_bar = [&](int s) { return bar0 + 8u * (2 * kScStages + 4 + s); };   // queries slot s landed
+    auto bempty_bar = [&](int s) { return bar0 + 8u * (2 * kScStages + 6 + s); };  // slot s's MMAs done
+    const uint32_t drain_bar = bar0 + 8u * (2 * kScStages + 8);  // MMAs issued before a give-up are done
+    const uint32_t never_bar = bar0 + 8u * (2 * kScStages + 9);  // nothing arrives (failure-path tests)
 
     // Set-up that reads nothing an earlier kernel writes: before the grid
     // dependency resolves.  The query sequences and positions the local plan
@@ -180,8 +185,10 @@ __global__ void __launch_bounds__(kScThreads, 1)
             mbar_init(accf_bar(a), 1);
             mbar_init(acce_bar(a), kScEpiThreads);
         }
-        mbar_init(bfull_bar, 1);
-        mbar_init(bempty_bar, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bfull_bar(b), 1);
+            mbar_init(bempty_bar(b), 1);
+        }
         mbar_init(drain_bar, 1);
         mbar_init(never_bar, 1);
         fence_mbar_init();
@@ -224,6 +231,7 @@ __global__ void __launch_bounds__(kScThreads, 1)
     const PlanView plan(plan_base, P.nq);
     const int ng = plan.hdr[0];
     const long long n_units = plan.hdr[1];
+    const bool b_dbl = plan.hdr[2] <= kScMaxQ / 2;   // every group fits one queries slot
     const int32_t *unit0 = (P.local_plan || P.nq + 1 > kScPlanStage) ? plan.unit0 : unit0_s;
     const int u_begin = static_cast<int>(n_units * blockIdx.x / gridDim.x);
     const int u_end = static_cast<int>(n_units * (blockIdx.x + 1) / gridDim.x);
@@ -248,7 +256,7 @@ __global__ void __launch_bounds__(kScThreads, 1)
         const unsigned full = 0xffffffffu;
         GroupCursor gc;
         gc.init(unit0, find_group(unit0, ng, u_begin));
-        int b_loads = 0, stage = 0;
+        int b_loads0 = 0, b_loads1 = 0, b_slot = 1, stage = 0;   // queries loads per slot, last slot used
         int64_t row_base = 0;
         uint32_t phase = 0;
         int old_pools = 0;  // pools of the group's sequence complete before this step
@@ -261,11 +269,13 @@ __global__ void __launch_bounds__(kScThreads, 1)
         const bool paged = P.cmap.paged();
         const int nseg = kScM / P.seg;
         for (int u = u_begin; u < u_end; ++u) {
-            if (gc.seek(u) || b_loads == 0) {
+            if (gc.seek(u) || b_loads0 + b_loads1 == 0) {
                 const int g = gc.g;
+                const int bs = b_dbl ? (b_slot ^ 1) : 0;
+                const int nb = bs ? b_loads1 : b_loads0;
                 bool w_ok = true;
-                if (lane == 0 && b_loads > 0)
-                    w_ok = mbar_wait(bempty_bar, (b_loads - 1) & 1, abort_flag, P.status, P.wait_ns);
+                if (lane == 0 && nb > 0)   // the slot's previous group's MMAs are done
+                    w_ok = mbar_wait(bempty_bar(bs), (nb - 1) & 1, abort_flag, P.status, P.wait_ns);
                 if (!__shfl_sync(full, w_ok, 0)) {
                     ok = false;
                     break;
@@ -276,13 +286,17 @@ __global__ void __launch_bounds__(kScThreads, 1)
                 old_pools = P.prev_len ? P.prev_len[bseq] >> P.kshift : 0;
                 if (paged) need = __reduce_max_sync(full, lane < nq ? (P.q_pos[q0 + lane] + 1) >> P.kshift : 0);
                 if (lane == 0) {
-                    mbar_expect_tx(bfull_bar, nq * 2 * kScQBoxBytes);
+                    const uint32_t b_base = sB + bs * kScBSlotBytes;
+                    const int kb_bytes = b_dbl ? kScBSlotBlockBytes : kScBBlockBytes;
+                    mbar_expect_tx(bfull_bar(bs), nq * 2 * kScQBoxBytes);
                     for (int qi = 0; qi < nq; ++qi)
                         for (int kb = 0; kb < 2; ++kb)
-                            tma_load_2d(sB + kb * kScBBlockBytes + qi * kScQBoxBytes, &tm_q,
-                                        bfull_bar, kb * 64, (q0 + qi) * kIndexHeads);
+                            tma_load_2d(b_base + kb * kb_bytes + qi * kScQBoxBytes, &tm_q, bfull_bar(bs), kb * 64,
+                                        (q0 + qi) * kIndexHeads);
                 }
-                ++b_loads;
+                if (bs) ++b_loads1;
+                else ++b_loads0;
+                b_slot = bs;
             }
             bool w_ok = true;
             if (lane == 0) w_ok = mbar_wait(empty_bar(stage), phase ^ 1, abort_flag, P.status, P.wait_ns);
@@ -328,7 +342,8 @@ __global__ void __launch_bounds__(kScThreads, 1)
             // Gave up: every load the warp issued lands before the shared memory
             // and the CTA go away (the latest phase of each barrier it armed;
             // bounded by the default limit).
-            if (b_loads > 0) mbar_wait(bfull_bar, (b_loads - 1) & 1, nullptr, P.status);
+            if (b_loads0 > 0) mbar_wait(bfull_bar(0), (b_loads0 - 1) & 1, nullptr, P.status);
+            if (b_loads1 > 0) mbar_wait(bfull_bar(1), (b_loads1 - 1) & 1, nullptr, P.status);
 #pragma unroll
             for (int i = 0; i < kScStages; ++i)
                 if (a_phase[i] >= 0) mbar_wait(full_bar(i), static_cast<uint32_t>(a_phase[i]), nullptr, P.status);
@@ -337,14 +352,22 @@ __global__ void __launch_bounds__(kScThreads, 1)
         if (lane == 0) {
             GroupCursor gc;
             gc.init(unit0, find_group(unit0, ng, u_begin));
-            int b_loads = 0, stage = 0, acc = 0;
-            uint32_t phase = 0, acc_phase = 0, idesc = 0;
+            int b_uses0 = 0, b_uses1 = 0, b_slot = 1, b_cur = -1, stage = 0, acc = 0;
+            uint32_t phase = 0, acc_phase = 0, idesc = 0, b_base = sB;
+            int kb_bytes = kScBBlockBytes;
             bool ok = !P.stall || mbar_wait(never_bar, 0, abort_flag, P.status, P.wait_ns);
             for (int u = u_begin; ok && u < u_end; ++u) {
-                if (gc.seek(u) || b_loads == 0) {
-                    if (b_loads > 0) tc_commit(bempty_bar);
-                    if (!(ok = mbar_wait(bfull_bar, b_loads & 1, abort_flag, P.status, P.wait_ns))) break;
-                    ++b_loads;
+                if (gc.seek(u) || b_cur < 0) {
+                    if (b_cur >= 0) tc_commit(bempty_bar(b_cur));   // the previous group's queries are free
+                    const int bs = b_dbl ? (b_slot ^ 1) : 0;
+                    if (!(ok = mbar_wait(bfull_bar(bs), (bs ? b_uses1 : b_uses0) & 1, abort_flag, P.status,
+                                         P.wait_ns)))
+                        break;
+                    if (bs) ++b_uses1;
+                    else ++b_uses0;
+                    b_slot = b_cur = bs;
+                    b_base = sB + bs * kScBSlotBytes;
+                    kb_bytes = b_dbl ? kScBSlotBlockBytes : kScBBlockBytes;
                     idesc = idesc_bf16_f32(kScM, kIndexHeads * plan.nq[gc.g]);
                 }
                 if (!(ok = mbar_wait(acce_bar(acc), acc_phase ^ 1, abort_flag, P.status, P.wait_ns))) break;
@@ -356,7 +379,7 @@ __global__ void __launch_bounds__(kScThreads, 1)
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint32_t koff = (kk & 3) * 32;  // 16 bf16 = 32 B inside the swizzled row
                     const uint64_t ad = desc_kmajor_sw128(a_base + (kk >> 2) * kScABlockBytes + koff);
-                    const uint64_t bd = desc_kmajor_sw128(sB + (kk >> 2) * kScBBlockBytes + koff);
+                    const uint64_t bd = desc_kmajor_sw128(b_base + (kk >> 2) * kb_bytes + koff);
                     tc_mma_bf16(d_tmem, ad, bd, idesc, kk > 0 ? 1u : 0u);
                 }
                 tc_commit(empty_bar(stage));

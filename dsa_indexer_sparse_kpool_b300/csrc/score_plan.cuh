@@ -13,7 +13,7 @@ constexpr int kScMaxQ = 8;  // queries per group
 
 // Plan layout (int32 words) inside the score workspace.
 struct PlanView {
-    int32_t *hdr;      // [0] groups, [1] units
+    int32_t *hdr;      // [0] groups, [1] units, [2] queries in the largest group
     int32_t *q0;       // [NQ] first query of each group
     int32_t *nq;       // [NQ] queries in each group
     int32_t *seq;      // [NQ] sequence of each group
@@ -56,6 +56,7 @@ __device__ __forceinline__ void build_score_plan(int nq, int num_seqs, const int
     }
     __syncthreads();
     const int ng = carry_groups;
+    int group_max = 0;
     for (int g = threadIdx.x; g < ng; g += blockDim.x) {
         const int q0 = plan.q0[g];
         const int q1 = (g + 1 < ng) ? plan.q0[g + 1] : nq;
@@ -80,8 +81,10 @@ __device__ __forceinline__ void build_score_plan(int nq, int num_seqs, const int
         }
         plan.nq[g] = q1 - q0;
         plan.unit0[g] = tiles;
+        group_max = max(group_max, q1 - q0);
     }
     __syncthreads();
+    (void)block_inclusive_scan<1>(group_max, scratch, &group_max);
     int carry_units = 0;
     for (int base = 0; base < ng; base += blockDim.x) {
         const int g = base + threadIdx.x;
@@ -95,6 +98,7 @@ __device__ __forceinline__ void build_score_plan(int nq, int num_seqs, const int
         plan.unit0[ng] = carry_units;
         plan.hdr[0] = ng;
         plan.hdr[1] = carry_units;
+        plan.hdr[2] = group_max;
     }
 }
 
