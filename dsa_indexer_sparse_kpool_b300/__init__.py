@@ -84,7 +84,7 @@ class kp_forward_args(ctypes.Structure):
                 ("keys", _vp), ("gates", _vp), ("ape", _vp), ("tail_keys", _vp), ("tail_gates", _vp),
                 ("pooled", _vp), ("q_idx", _vp), ("w", _vp), ("q_lat", _vp), ("latent", _vp),
                 ("out", _vp), ("lse", _vp), ("pool_idx", _vp), ("n_sel", _vp),
-                ("workspace", _vp), ("workspace_bytes", _sz), ("d_status", _vp)]
+                ("workspace", _vp), ("workspace_bytes", _sz), ("d_status", _vp), ("q_lat_ready", _vp)]
 
 
 class kp_gemm_args(ctypes.Structure):
@@ -117,6 +117,7 @@ EXPORTS = ("kp_kpool_compress", "kp_indexer_score", "kp_topk_select", "kp_indexe
            "kp_status_string", "kp_last_error", "kp_read_device_status", "kp_version")
 DTYPE_BF16, DTYPE_F32 = 0, 1
 
+ABI_VERSION = 20300   # kp_version() of the library whose structs the classes above mirror
 _lib = None
 
 
@@ -152,6 +153,9 @@ def lib() -> ctypes.CDLL:
         L.kp_read_device_status.restype = ctypes.c_int
         L.kp_version.argtypes = []
         L.kp_version.restype = ctypes.c_int
+        if L.kp_version() != ABI_VERSION:   # the structs above must match the library's
+            raise RuntimeError(f"{LIB_PATH} is version {L.kp_version()}, the binding expects {ABI_VERSION}: "
+                               "rebuild with `python -m dsa_indexer_sparse_kpool_b300.build`")
         _lib = L
     return _lib
 
@@ -301,12 +305,19 @@ def kp_sparse_mla_attend(cfg: Config, seqs: Seqs, queries: Queries, q_lat, laten
 
 def forward_args(cfg: Config, seqs: Seqs, queries: Queries, *, prev_len, new_off, max_new_per_seq, keys, gates,
                  ape, tail_keys, tail_gates, pooled, q_idx, w, q_lat, latent, out, lse=None, pool_idx=None,
-                 n_sel=None, workspace=None, d_status=None) -> kp_forward_args:
+                 n_sel=None, workspace=None, d_status=None, q_lat_ready=None) -> kp_forward_args:
+    """q_lat_ready: None, or a recorded torch.cuda.Event that the attention
+    launch waits for (kp_forward_args.q_lat_ready)."""
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    ev = None
+    if q_lat_ready is not None:
+        ev = q_lat_ready.cuda_event
+        if not ev:
+            raise ValueError("q_lat_ready: the event has not been recorded")
     return kp_forward_args(cfg.c(), seqs.c(), queries.c(), _p(prev_len), _p(new_off), keys.shape[0],
                            int(max_new_per_seq), _p(keys), _p(gates), _p(ape), _p(tail_keys), _p(tail_gates),
                            _p(pooled), _p(q_idx), _p(w), _p(q_lat), _p(latent), _p(out), _p(lse), _p(pool_idx),
-                           _p(n_sel), _p(workspace), ws_bytes, _p(d_status))
+                           _p(n_sel), _p(workspace), ws_bytes, _p(d_status), ev)
 
 
 def kp_workspace_size(args: kp_forward_args) -> int:

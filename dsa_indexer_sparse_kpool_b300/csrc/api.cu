@@ -357,6 +357,19 @@ size_t kp_workspace_size(const kp_forward_args *a) {
     return forward_layout(*a, sms).total;
 }
 
+// The attention is the only stage that reads q_lat: when the caller's copy of
+// q_lat may still be in flight, the stream waits for it here, after the
+// earlier stages were launched.
+static kp_status wait_for_q_lat(const kp_forward_args &a, cudaStream_t s) {
+    if (!a.q_lat_ready) return KP_OK;
+    const cudaError_t e = cudaStreamWaitEvent(s, reinterpret_cast<cudaEvent_t>(a.q_lat_ready), 0);
+    if (e != cudaSuccess) {
+        record_cuda_error("cudaStreamWaitEvent(q_lat_ready)", e);
+        return KP_ERR_CUDA;
+    }
+    return KP_OK;
+}
+
 kp_status kp_dsa_forward(const kp_forward_args *a, kp_stream_t stream) {
     if (!a) return KP_ERR_INVALID_ARG;
     kp_status st = check_config(a->cfg);
@@ -451,6 +464,7 @@ kp_status kp_dsa_forward(const kp_forward_args *a, kp_stream_t stream) {
             if (c.num_new > 0 && (st = launch_compress(c, s)) != KP_OK) return st;
             if ((st = launch_score_select(sc, tk, s, false, nullptr)) != KP_OK) return st;
         }
+        if ((st = wait_for_q_lat(*a, s)) != KP_OK) return st;
         return launch_attend(at, s);
     }
     // The scorer's plan: built by the scorer itself in shared memory when it
@@ -473,6 +487,7 @@ kp_status kp_dsa_forward(const kp_forward_args *a, kp_stream_t stream) {
     }
     if (!queries) return KP_OK;
     if ((st = launch_topk(tk, s)) != KP_OK) return st;
+    if ((st = wait_for_q_lat(*a, s)) != KP_OK) return st;
     return launch_attend(at, s);
 }
 
@@ -618,7 +633,7 @@ kp_status kp_read_device_status(const int32_t *d_status, kp_stream_t stream) {
     return static_cast<kp_status>(v);
 }
 
-int kp_version(void) { return 20200; }
+int kp_version(void) { return 20300; }
 
 }  // extern "C"
 

@@ -154,38 +154,44 @@ class Step:
         ws = kp_workspace_size(args)
         self.workspace = torch.empty(ws, dtype=torch.uint8, device=d)
         self.args = self._args(self.workspace)
+        self._io = None          # (in_buf, out_buf, byte offset of q_lat in in_buf) after pack_io
+        self._late_args = None   # the args with q_lat_ready set (run_host)
 
-    def _args(self, workspace):
+    def _args(self, workspace, q_lat_ready=None):
         s = self.sess
         return forward_args(s.cfg, self.seqs, self.queries, prev_len=self.prev_len, new_off=self.new_off,
                             max_new_per_seq=self.max_new, keys=self.keys, gates=self.gates, ape=s.ape,
                             tail_keys=s.tail_keys, tail_gates=s.tail_gates, pooled=s.pooled, q_idx=self.q_idx,
                             w=self.w, q_lat=self.q_lat, latent=s.latent, out=self.out, lse=self.lse,
-                            pool_idx=self.pool_idx, n_sel=self.n_sel, workspace=workspace, d_status=s.status)
+                            pool_idx=self.pool_idx, n_sel=self.n_sel, workspace=workspace, d_status=s.status,
+                            q_lat_ready=q_lat_ready)
 
     def run(self, stream=None) -> None:
         kp_dsa_forward(self.args, stream=stream)
 
     def set_share(self, share_src) -> None:
         """Shared selection: share_src[q] >= 0 makes query q attend that query's
-        selection instead of selecting its own (None: every query selects)."""
+        selection instead of selecting its own (None: every query selects).
+        Call it before pack_io: the table is one of the step's inputs."""
         t = None if share_src is None else _dev_i32([int(x) for x in share_src], self.sess.device)
         self.queries = Queries(self.queries.q_seq, self.queries.q_pos, self.queries.max_pools, t)
         self.args = self._args(self.workspace)
+        self._io = None
+        self._late_args = None
 
     def pack_io(self):
         """Moves the step's per-step inputs (positions, new keys and gates,
         queries) into one device buffer and its outputs (out, lse) into
         another, keeping their values, and re-points the step at them, so a
         caller moves each direction with one copy.  Returns the two buffers
-        (uint8 device tensors, 256-byte aligned pieces).  A CUDA graph captured
-        before the call still reads the old tensors."""
+        (uint8 device tensors, 256-byte aligned pieces).  q_lat is the last
+        piece of the input buffer, so that it can cross separately
+        (run_host).  A CUDA graph captured before the call still reads the
+        old tensors."""
         d = self.sess.device
-        ins = [self.prev_len, self.new_off, self.keys, self.gates, self.queries.q_seq, self.queries.q_pos,
-               self.q_idx, self.w, self.q_lat]
         share = self.queries.share_src
-        if share is not None:
-            ins.append(share)
+        ins = [self.prev_len, self.new_off, self.keys, self.gates, self.queries.q_seq, self.queries.q_pos,
+               self.q_idx, self.w] + ([share] if share is not None else []) + [self.q_lat]
         outs = [self.out, self.lse]
 
         def carve(ts):
@@ -199,14 +205,60 @@ class Step:
                 v = buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
                 v.copy_(t)
                 views.append(v)
-            return buf, views
+            return buf, views, offs
 
-        in_buf, views = carve(ins)
-        (self.prev_len, self.new_off, self.keys, self.gates, q_seq, q_pos, self.q_idx, self.w, self.q_lat) = views[:9]
-        self.queries = Queries(q_seq, q_pos, self.queries.max_pools, views[9] if share is not None else None)
-        out_buf, (self.out, self.lse) = carve(outs)
+        in_buf, views, offs = carve(ins)
+        (self.prev_len, self.new_off, self.keys, self.gates, q_seq, q_pos, self.q_idx, self.w) = views[:8]
+        self.q_lat = views[-1]
+        self.queries = Queries(q_seq, q_pos, self.queries.max_pools, views[8] if share is not None else None)
+        out_buf, (self.out, self.lse), _ = carve(outs)
         self.args = self._args(self.workspace)
+        self._io = (in_buf, out_buf, offs[-1])
+        self._late_args = None
         return in_buf, out_buf
+
+    def run_host(self, h_in: torch.Tensor, h_out: torch.Tensor) -> None:
+        """One step from pinned host memory, asynchronous on the current
+        stream (capturable in a CUDA graph): the inputs come from ``h_in``
+        (laid out as the buffer pack_io returned) and out / lse go to
+        ``h_out`` (laid out as pack_io's output buffer).
+
+        q_lat, most of the input bytes and read only by the attention, crosses
+        on a second stream while compression, scoring and selection run; the
+        attention launch waits for it (kp_forward_args.q_lat_ready).  The
+        second stream starts only once this stream's earlier work (the
+        previous step's attention included) and the early inputs' copy are
+        done."""
+        if self._io is None:
+            raise RuntimeError("run_host needs pack_io() first")
+        in_buf, out_buf, late = self._io
+        if h_in.numel() != in_buf.numel() or h_out.numel() != out_buf.numel():
+            raise ValueError("run_host: host buffers must match the sizes pack_io returned")
+        main = torch.cuda.current_stream(self.sess.device)
+        if self.queries.q_seq.numel() == 0:          # no attention: nothing to overlap
+            in_buf.copy_(h_in, non_blocking=True)
+            kp_dsa_forward(self.args, stream=main)
+            h_out.copy_(out_buf, non_blocking=True)
+            return
+        if self._late_args is None:
+            self._copy_stream = torch.cuda.Stream(device=self.sess.device)
+            self._fork = torch.cuda.Event()
+            self._q_lat_ready = torch.cuda.Event()
+        side = self._copy_stream
+        # The early inputs first, alone on the bus: the compression and the
+        # scorer wait for them, and two host-to-device copies in flight at once
+        # finished later than the same copies one after the other.
+        in_buf[:late].copy_(h_in[:late], non_blocking=True)
+        self._fork.record(main)
+        side.wait_event(self._fork)
+        with torch.cuda.stream(side):
+            in_buf[late:].copy_(h_in[late:], non_blocking=True)
+        self._q_lat_ready.record(side)
+        if self._late_args is None:              # the event exists once recorded
+            self._late_args = self._args(self.workspace, q_lat_ready=self._q_lat_ready)
+        kp_dsa_forward(self._late_args, stream=main)
+        main.wait_event(self._q_lat_ready)       # rejoins the copy stream on every path
+        h_out.copy_(out_buf, non_blocking=True)
 
     def fused(self) -> bool:
         """Whether ``run`` scores and selects in one kernel (SELECT_FUSED and

@@ -78,8 +78,9 @@
 extern "C" {
 #endif
 
-/* cudaStream_t without including the CUDA headers. */
+/* cudaStream_t and cudaEvent_t without including the CUDA headers. */
 typedef struct CUstream_st *kp_stream_t;
+typedef struct CUevent_st *kp_event_t;
 
 typedef enum kp_status {
     KP_OK = 0,
@@ -350,6 +351,15 @@ typedef struct kp_forward_args {
     void *workspace;              /* >= kp_workspace_size(args) bytes */
     size_t workspace_bytes;
     int32_t *d_status;
+    /* May be NULL.  An event that completes once q_lat holds this step's
+     * queries, e.g. one recorded after an asynchronous host-to-device copy of
+     * q_lat on another stream.  The call makes `stream` wait for it just
+     * before the attention launch (cudaStreamWaitEvent), so compression,
+     * scoring and selection run while q_lat is still in transit: no stage
+     * before the attention reads q_lat.  Record the event before the call.
+     * A failed wait returns KP_ERR_CUDA with the first stages already
+     * launched and out / lse not written. */
+    kp_event_t q_lat_ready;
 } kp_forward_args;
 
 KP_API kp_status kp_kpool_compress(const kp_compress_args *args, kp_stream_t stream);

@@ -30,7 +30,7 @@ def test_exports_every_declared_entry_point(L):
     for n in names:
         assert hasattr(L, n), n
     assert set(kp.EXPORTS) == set(names)
-    assert L.kp_version() == 20200
+    assert L.kp_version() == 20300 == kp.ABI_VERSION
 
 
 def test_status_strings(L):
