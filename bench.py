@@ -558,7 +558,8 @@ def main():
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "path": "Step.run_host from pinned memory: q_lat crosses on a second stream while compress, "
-                            "score and top-k run; out and lse back after the attention"},
+                            "score and top-k run; batches of at least 512 queries then pipeline chunks of 256 "
+                            "(q_lat in, attention, out and lse back)"},
             "gpu_launches": step.launches_per_step() * args.steps,
             "clocks": clocks,
             "device_status": status,

@@ -117,7 +117,7 @@ EXPORTS = ("kp_kpool_compress", "kp_indexer_score", "kp_topk_select", "kp_indexe
            "kp_status_string", "kp_last_error", "kp_read_device_status", "kp_version")
 DTYPE_BF16, DTYPE_F32 = 0, 1
 
-ABI_VERSION = 20300   # kp_version() of the library whose structs the classes above mirror
+ABI_VERSION = 20400   # kp_version() of the library whose structs the classes above mirror
 _lib = None
 
 
@@ -295,12 +295,21 @@ def kp_indexer_score_select(cfg: Config, seqs: Seqs, queries: Queries, q_idx, w,
     _check(lib().kp_indexer_score_select(ctypes.byref(a), _stream(stream)), "kp_indexer_score_select")
 
 
+def attend_args(cfg: Config, seqs: Seqs, queries: Queries, q_lat, latent, pool_idx, n_sel, out, lse,
+                workspace, d_status=None) -> kp_attend_args:
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return kp_attend_args(cfg.c(), seqs.c(), queries.c(), _p(q_lat), _p(latent), _p(pool_idx), _p(n_sel), _p(out),
+                          _p(lse), _p(workspace), ws_bytes, _p(d_status))
+
+
+def kp_sparse_mla_attend_args(args: kp_attend_args, stream=None) -> None:
+    _check(lib().kp_sparse_mla_attend(ctypes.byref(args), _stream(stream)), "kp_sparse_mla_attend")
+
+
 def kp_sparse_mla_attend(cfg: Config, seqs: Seqs, queries: Queries, q_lat, latent, pool_idx, n_sel, out, lse,
                          workspace, d_status=None, stream=None) -> None:
-    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    a = kp_attend_args(cfg.c(), seqs.c(), queries.c(), _p(q_lat), _p(latent), _p(pool_idx), _p(n_sel), _p(out),
-                       _p(lse), _p(workspace), ws_bytes, _p(d_status))
-    _check(lib().kp_sparse_mla_attend(ctypes.byref(a), _stream(stream)), "kp_sparse_mla_attend")
+    kp_sparse_mla_attend_args(attend_args(cfg, seqs, queries, q_lat, latent, pool_idx, n_sel, out, lse, workspace,
+                                          d_status), stream)
 
 
 def forward_args(cfg: Config, seqs: Seqs, queries: Queries, *, prev_len, new_off, max_new_per_seq, keys, gates,

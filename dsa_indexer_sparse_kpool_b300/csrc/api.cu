@@ -376,7 +376,10 @@ kp_status kp_dsa_forward(const kp_forward_args *a, kp_stream_t stream) {
     if (st != KP_OK) return st;
     if ((st = check_queries(a->q)) != KP_OK) return st;
     if ((st = check_seqs(a->seqs, a->cfg.kpool, true, true)) != KP_OK) return st;
-    if (a->q.num_queries > 0 && !a->out) return KP_ERR_INVALID_ARG;   // no queries: nothing is written
+    // No out with queries: the selection only (stages 1-3), into the caller's
+    // pool_idx and n_sel; the attention is left to kp_sparse_mla_attend.
+    const bool select_only = a->q.num_queries > 0 && !a->out;
+    if (select_only && (!a->pool_idx || !a->n_sel)) return KP_ERR_INVALID_ARG;
     const int sms = device_sm_count();
     if (sms <= 0) {
         record_error_text("cannot query the current CUDA device");
@@ -445,7 +448,7 @@ kp_status kp_dsa_forward(const kp_forward_args *a, kp_stream_t stream) {
     if ((st = validate_compress(&c)) != KP_OK) return st;
     if ((st = validate_score(&sc)) != KP_OK) return st;
     if ((st = validate_topk(&tk)) != KP_OK) return st;
-    if ((st = validate_attend(&at)) != KP_OK) return st;
+    if (!select_only && (st = validate_attend(&at)) != KP_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const bool queries = a->q.num_queries > 0;
     if (forward_fused(*a)) {
@@ -464,6 +467,7 @@ kp_status kp_dsa_forward(const kp_forward_args *a, kp_stream_t stream) {
             if (c.num_new > 0 && (st = launch_compress(c, s)) != KP_OK) return st;
             if ((st = launch_score_select(sc, tk, s, false, nullptr)) != KP_OK) return st;
         }
+        if (select_only) return KP_OK;
         if ((st = wait_for_q_lat(*a, s)) != KP_OK) return st;
         return launch_attend(at, s);
     }
@@ -487,6 +491,7 @@ kp_status kp_dsa_forward(const kp_forward_args *a, kp_stream_t stream) {
     }
     if (!queries) return KP_OK;
     if ((st = launch_topk(tk, s)) != KP_OK) return st;
+    if (select_only) return KP_OK;
     if ((st = wait_for_q_lat(*a, s)) != KP_OK) return st;
     return launch_attend(at, s);
 }
@@ -633,7 +638,7 @@ kp_status kp_read_device_status(const int32_t *d_status, kp_stream_t stream) {
     return static_cast<kp_status>(v);
 }
 
-int kp_version(void) { return 20300; }
+int kp_version(void) { return 20400; }
 
 }  // extern "C"
 

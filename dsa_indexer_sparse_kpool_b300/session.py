@@ -11,10 +11,10 @@ from typing import Optional, Sequence
 
 import torch
 
-from . import (Config, Queries, Seqs, forward_args, kp_dsa_forward, kp_indexer_score, kp_indexer_score_select,
-               kp_kpool_compress, kp_score_workspace_size, kp_attend_workspace_size, kp_sparse_mla_attend,
-               kp_topk_select, kp_workspace_size, score_stride, FUSED_MAX_POOLS, SELECT_FUSED, INDEX_DIM,
-               LATENT_DIM, MLA_HEADS, NOPE_DIM)
+from . import (Config, Queries, Seqs, attend_args, forward_args, kp_dsa_forward, kp_indexer_score,
+               kp_indexer_score_select, kp_kpool_compress, kp_score_workspace_size, kp_attend_workspace_size,
+               kp_sparse_mla_attend, kp_sparse_mla_attend_args, kp_topk_select, kp_workspace_size, score_stride,
+               FUSED_MAX_POOLS, SELECT_FUSED, INDEX_DIM, LATENT_DIM, MLA_HEADS, NOPE_DIM)
 
 
 # Queries up to which the library's scorer builds its work plan in shared
@@ -22,6 +22,22 @@ from . import (Config, Queries, Seqs, forward_args, kp_dsa_forward, kp_indexer_s
 # and the same for the fused score-and-select kernel (2048 plan words).
 SCORE_LOCAL_PLAN_MAX_QUERIES = (4096 - 5) // 4
 SCORE_SELECT_LOCAL_PLAN_MAX_QUERIES = (2048 - 5) // 4
+
+# Step.run_host pipelines batches of at least two chunks of this many queries:
+# each chunk's q_lat copy, attention and output copy overlap the neighbouring
+# chunks'.  From 128 queries on, a chunk and the whole batch alike attend
+# with one CTA per query (no split of a query's tokens), so chunking changes
+# no result bit.
+HOST_CHUNK_QUERIES = 256
+HOST_MIN_CHUNK_QUERIES = 128
+
+
+def host_chunks(nq: int, chunk_queries: int):
+    """Query ranges [a, b) of run_host's pipeline: nq // chunk_queries chunks
+    as even as the count allows, so every chunk holds at least chunk_queries
+    queries (one chunk, the whole batch, below two chunks' worth)."""
+    n = max(1, nq // chunk_queries)
+    return [(nq * c // n, nq * (c + 1) // n) for c in range(n)]
 
 
 def _dev_i32(x, device):
@@ -154,8 +170,9 @@ class Step:
         ws = kp_workspace_size(args)
         self.workspace = torch.empty(ws, dtype=torch.uint8, device=d)
         self.args = self._args(self.workspace)
-        self._io = None          # (in_buf, out_buf, byte offset of q_lat in in_buf) after pack_io
+        self._io = None          # (in_buf, out_buf, q_lat's byte offset in in_buf, lse's in out_buf)
         self._late_args = None   # the args with q_lat_ready set (run_host)
+        self._chunked = None     # run_host's pipeline: chunk bounds, argument structs, streams, events
 
     def _args(self, workspace, q_lat_ready=None):
         s = self.sess
@@ -178,6 +195,7 @@ class Step:
         self.args = self._args(self.workspace)
         self._io = None
         self._late_args = None
+        self._chunked = None
 
     def pack_io(self):
         """Moves the step's per-step inputs (positions, new keys and gates,
@@ -211,13 +229,14 @@ class Step:
         (self.prev_len, self.new_off, self.keys, self.gates, q_seq, q_pos, self.q_idx, self.w) = views[:8]
         self.q_lat = views[-1]
         self.queries = Queries(q_seq, q_pos, self.queries.max_pools, views[8] if share is not None else None)
-        out_buf, (self.out, self.lse), _ = carve(outs)
+        out_buf, (self.out, self.lse), out_offs = carve(outs)
         self.args = self._args(self.workspace)
-        self._io = (in_buf, out_buf, offs[-1])
+        self._io = (in_buf, out_buf, offs[-1], out_offs[1])
         self._late_args = None
+        self._chunked = None
         return in_buf, out_buf
 
-    def run_host(self, h_in: torch.Tensor, h_out: torch.Tensor) -> None:
+    def run_host(self, h_in: torch.Tensor, h_out: torch.Tensor, chunk_queries: Optional[int] = None) -> None:
         """One step from pinned host memory, asynchronous on the current
         stream (capturable in a CUDA graph): the inputs come from ``h_in``
         (laid out as the buffer pack_io returned) and out / lse go to
@@ -228,22 +247,38 @@ class Step:
         attention launch waits for it (kp_forward_args.q_lat_ready).  The
         second stream starts only once this stream's earlier work (the
         previous step's attention included) and the early inputs' copy are
-        done."""
+        done.
+
+        Batches of at least 2 * chunk_queries queries (default
+        HOST_CHUNK_QUERIES; not with a shared selection) run as a pipeline
+        instead: the selection for all queries (kp_dsa_forward with out =
+        NULL), then per chunk of queries its q_lat copy, its attention
+        (kp_sparse_mla_attend, in chunk order on this stream) and its out /
+        lse copy back on a third stream, so the copies in both directions
+        overlap the attention of other chunks.  Results are the same bits as
+        the single call's."""
         if self._io is None:
             raise RuntimeError("run_host needs pack_io() first")
-        in_buf, out_buf, late = self._io
+        in_buf, out_buf, late, _ = self._io
         if h_in.numel() != in_buf.numel() or h_out.numel() != out_buf.numel():
             raise ValueError("run_host: host buffers must match the sizes pack_io returned")
         main = torch.cuda.current_stream(self.sess.device)
-        if self.queries.q_seq.numel() == 0:          # no attention: nothing to overlap
+        nq = self.queries.q_seq.numel()
+        if nq == 0:          # no attention: nothing to overlap
             in_buf.copy_(h_in, non_blocking=True)
             kp_dsa_forward(self.args, stream=main)
             h_out.copy_(out_buf, non_blocking=True)
             return
+        cq = HOST_CHUNK_QUERIES if chunk_queries is None else int(chunk_queries)
+        if cq < HOST_MIN_CHUNK_QUERIES:
+            raise ValueError(f"run_host: chunks of at least {HOST_MIN_CHUNK_QUERIES} queries")
         if self._late_args is None:
             self._copy_stream = torch.cuda.Stream(device=self.sess.device)
             self._fork = torch.cuda.Event()
             self._q_lat_ready = torch.cuda.Event()
+        if nq >= 2 * cq and self.queries.share_src is None:
+            self._run_host_chunked(h_in, h_out, host_chunks(nq, cq), main)
+            return
         side = self._copy_stream
         # The early inputs first, alone on the bus: the compression and the
         # scorer wait for them, and two host-to-device copies in flight at once
@@ -259,6 +294,52 @@ class Step:
         kp_dsa_forward(self._late_args, stream=main)
         main.wait_event(self._q_lat_ready)       # rejoins the copy stream on every path
         h_out.copy_(out_buf, non_blocking=True)
+
+    def _run_host_chunked(self, h_in, h_out, bounds, main) -> None:
+        in_buf, out_buf, late, lse_off = self._io
+        nq = self.queries.q_seq.numel()
+        if self._chunked is None or self._chunked["bounds"] != bounds:
+            s = self.sess
+            sel = forward_args(s.cfg, self.seqs, self.queries, prev_len=self.prev_len, new_off=self.new_off,
+                               max_new_per_seq=self.max_new, keys=self.keys, gates=self.gates, ape=s.ape,
+                               tail_keys=s.tail_keys, tail_gates=s.tail_gates, pooled=s.pooled,
+                               q_idx=self.q_idx, w=self.w, q_lat=None, latent=s.latent, out=None, lse=None,
+                               pool_idx=self.pool_idx, n_sel=self.n_sel, workspace=self.workspace,
+                               d_status=s.status)
+            ws = torch.empty(kp_attend_workspace_size(s.cfg, nq), dtype=torch.uint8, device=s.device)
+            att = [attend_args(s.cfg, self.seqs,
+                               Queries(self.queries.q_seq[a:b], self.queries.q_pos[a:b], self.queries.max_pools),
+                               self.q_lat[a:b], s.latent, self.pool_idx[a:b], self.n_sel[a:b], self.out[a:b],
+                               self.lse[a:b], ws, s.status) for a, b in bounds]
+            self._chunked = {"bounds": bounds, "sel": sel, "att": att, "ws": ws,
+                             "d2h": torch.cuda.Stream(device=s.device),
+                             "in": [torch.cuda.Event() for _ in bounds], "out": [torch.cuda.Event() for _ in bounds],
+                             "done": torch.cuda.Event()}
+        st = self._chunked
+        side, d2h = self._copy_stream, st["d2h"]
+        qb = self.q_lat[0].numel() * self.q_lat.element_size()      # q_lat bytes per query
+        ob = self.out[0].numel() * self.out.element_size()          # out bytes per query
+        lb = self.lse[0].numel() * self.lse.element_size()          # lse bytes per query
+        in_buf[:late].copy_(h_in[:late], non_blocking=True)
+        self._fork.record(main)
+        side.wait_event(self._fork)
+        with torch.cuda.stream(side):
+            for (a, b), ev in zip(st["bounds"], st["in"]):
+                in_buf[late + a * qb:late + b * qb].copy_(h_in[late + a * qb:late + b * qb], non_blocking=True)
+                ev.record(side)
+        kp_dsa_forward(st["sel"], stream=main)                     # the selection of every query
+        for (a, b), args, ev_in, ev_out in zip(st["bounds"], st["att"], st["in"], st["out"]):
+            main.wait_event(ev_in)
+            kp_sparse_mla_attend_args(args, stream=main)
+            ev_out.record(main)
+            d2h.wait_event(ev_out)
+            with torch.cuda.stream(d2h):
+                h_out[a * ob:b * ob].copy_(out_buf[a * ob:b * ob], non_blocking=True)
+                h_out[lse_off + a * lb:lse_off + b * lb].copy_(out_buf[lse_off + a * lb:lse_off + b * lb],
+                                                                 non_blocking=True)
+        st["done"].record(d2h)
+        main.wait_event(st["in"][-1])            # rejoins both copy streams
+        main.wait_event(st["done"])
 
     def fused(self) -> bool:
         """Whether ``run`` scores and selects in one kernel (SELECT_FUSED and

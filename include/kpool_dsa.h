@@ -344,7 +344,11 @@ typedef struct kp_forward_args {
     const uint16_t *q_lat;
     const uint16_t *latent;
     /* outputs */
-    uint16_t *out;                /* [NQ][64][512] bf16 (may be NULL when NQ == 0) */
+    uint16_t *out;                /* [NQ][64][512] bf16; NULL with queries: the call stops
+                                     after the selection (stages 1-3), which it writes to
+                                     pool_idx and n_sel (both required then); q_lat is not
+                                     read, and kp_sparse_mla_attend runs the attention
+                                     (for instance over chunks of the queries) */
     float *lse;                   /* [NQ][64] fp32 (may be NULL) */
     int32_t *pool_idx;            /* [NQ][K] (may be NULL: kept in the workspace) */
     int32_t *n_sel;               /* [NQ]    (may be NULL: kept in the workspace) */

@@ -30,7 +30,7 @@ def test_exports_every_declared_entry_point(L):
     for n in names:
         assert hasattr(L, n), n
     assert set(kp.EXPORTS) == set(names)
-    assert L.kp_version() == 20300 == kp.ABI_VERSION
+    assert L.kp_version() == 20400 == kp.ABI_VERSION
 
 
 def test_status_strings(L):
@@ -155,3 +155,20 @@ def test_fused_mode_workspace_holds_no_score_matrix(L):
     fused_long = L.kp_workspace_size(ctypes.byref(args))
     args.cfg = kp.Config(select_mode=kp.SELECT_STAGED).c()
     assert fused_long == L.kp_workspace_size(ctypes.byref(args))
+
+
+def test_forward_select_only_needs_the_selection_buffers(L):
+    # out = NULL with queries: the selection only, into the caller's pool_idx
+    # and n_sel, which must then be given
+    a = kp.kp_forward_args()
+    a.cfg = _cfg()
+    a.seqs = kp.kp_seqs(1, 0x1000, 0x1000, 0x1000, 100, 100)
+    a.q = kp.kp_queries(4, 0x1000, 0x1000, 16)
+    a.prev_len = a.new_off = 0x1000
+    a.q_idx = a.w = a.pooled = a.latent = 0x10000
+    a.workspace = 0x10000
+    a.workspace_bytes = 1 << 30
+    assert L.kp_dsa_forward(ctypes.byref(a), None) == 1
+    a.pool_idx = a.n_sel = 0x10000
+    # past the argument checks: the next step asks for the device (none here)
+    assert L.kp_dsa_forward(ctypes.byref(a), None) == 3

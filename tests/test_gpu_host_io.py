@@ -116,3 +116,44 @@ def test_run_host_needs_pack_io_and_matching_buffers():
     with pytest.raises(ValueError):
         step.run_host(torch.empty(in_buf.numel() + 1, dtype=torch.uint8).pin_memory(),
                       torch.empty(out_buf.numel(), dtype=torch.uint8).pin_memory())
+
+
+@pytest.mark.parametrize("chunk", [256, 128])
+def test_run_host_chunked_pipeline_equals_run(chunk):
+    # 600 queries of one sequence, as in a prefill chunk: two chunks of 300
+    # queries, or four of 150, each with its own q_lat copy, attention and
+    # copy back; eagerly, then replayed from a captured graph
+    wl = KI.make(KI.Spec("hostio", [20000], [600], topk_tokens=2048, seed=85))
+    ref, ref_pooled = _reference(wl, kp.SELECT_AUTO, None)
+    sess, step, in_buf, out_buf, h_in, h_out = _host_step(wl, kp.SELECT_AUTO, None)
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        in_buf.zero_()
+        step.out.zero_()
+        step.run_host(h_in, h_out, chunk_queries=chunk)
+        torch.cuda.synchronize()
+        assert int(sess.status.item()) == 0
+        assert len(step._chunked["bounds"]) == 600 // chunk
+        _same(step, ref, h_out, out_buf)
+        assert np.array_equal(PL.gpu_pooled_of_seq(sess, wl, 0), ref_pooled)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step.run_host(h_in, h_out, chunk_queries=chunk)
+        in_buf.zero_()
+        step.out.zero_()
+        h_out.zero_()
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        assert int(sess.status.item()) == 0
+        _same(step, ref, h_out, out_buf)
+
+
+def test_run_host_rejects_small_chunks():
+    wl = KI.make(KI.Spec("hostio", [3001], [2], topk_tokens=256, seed=86))
+    _, step = PL.make_gpu(wl)
+    in_buf, out_buf = step.pack_io()
+    h_in = torch.empty(in_buf.numel(), dtype=torch.uint8).pin_memory()
+    h_out = torch.empty(out_buf.numel(), dtype=torch.uint8).pin_memory()
+    with pytest.raises(ValueError):
+        step.run_host(h_in, h_out, chunk_queries=64)

@@ -1,10 +1,12 @@
 """Host-side checks of the session helpers (no GPU, no library calls)."""
 import types
 
+import pytest
+
 import torch
 
 from dsa_indexer_sparse_kpool_b300 import Queries
-from dsa_indexer_sparse_kpool_b300.session import SCORE_LOCAL_PLAN_MAX_QUERIES, Step
+from dsa_indexer_sparse_kpool_b300.session import SCORE_LOCAL_PLAN_MAX_QUERIES, Step, host_chunks
 
 
 def _step_stub():
@@ -44,6 +46,25 @@ def test_pack_io_keeps_values_and_packs_into_two_buffers():
     # one copy per direction moves every byte of the step's inputs / outputs
     need_in = sum(old[k].numel() * old[k].element_size() for k in names_in) + 2 * 3 * 4
     assert in_buf.numel() >= need_in and out_buf.numel() >= 3 * 64 * 512 * 2 + 3 * 64 * 4
+    # q_lat is the input buffer's last piece (run_host copies it on its own);
+    # every other input ends before it
+    _, _, late, lse_off = st._io
+    assert st.q_lat.data_ptr() - in_buf.data_ptr() == late
+    for k in ("prev_len", "new_off", "keys", "gates", "q_idx", "w"):
+        t = getattr(st, k)
+        assert t.data_ptr() + t.numel() * t.element_size() <= in_buf.data_ptr() + late, k
+    assert st.out.data_ptr() == out_buf.data_ptr() and st.lse.data_ptr() - out_buf.data_ptr() == lse_off
+
+
+@pytest.mark.parametrize("nq,cq", [(4096, 256), (600, 256), (530, 256), (511, 256), (512, 256), (300, 128),
+                                   (10, 256)])
+def test_host_chunks_cover_the_batch_with_full_chunks(nq, cq):
+    ch = host_chunks(nq, cq)
+    assert ch[0][0] == 0 and ch[-1][1] == nq
+    assert all(a1 == b0 for (_, b0), (a1, _) in zip(ch, ch[1:]))
+    assert len(ch) == max(1, nq // cq)
+    if len(ch) > 1:
+        assert min(b - a for a, b in ch) >= cq
 
 
 def test_local_plan_threshold_matches_the_plan_layout():
