@@ -14,31 +14,36 @@
 //
 // B300 design.  The 64 heads of a query share every latent row (MQA-like),
 // so heads are the natural N of the tensor-core products and the gathered
-// tokens their M:
-//   S^T[tok, h] = C[tok, :512] . Q[h, :512]^T     M = 64 tokens, N = 64, K = 512
-//   O^T[d, h]  += C[tok, d]^T . P[tok, h]          M = 128 latent columns (x4), N = 64, K = 64 tokens
-// 64-token tiles of latent rows (64 KB) are gathered into two shared-memory
-// slots in the 128-byte-swizzle layout, so the next tile streams in while
-// this one is computed; the S product reads a tile K-major, the P.V product
-// reads the same bytes M-major, so each latent row crosses HBM once.  Q takes
-// the other 64 KB, so two slots is all that fits.  Measured on B300, these
-// small-N products cost about 50 cycles per instruction at best (about 75 with
-// operand addresses changing every instruction), whatever M is, so a tile's
-// 48 MMAs take ~1.8 us: the S product's 32 instructions are per tile, not per
-// token, which is why smaller tiles in more slots (48 tokens in three) came
-// out slower.  A
+// tokens their M.  64-token tiles of latent rows (64 KB) are gathered into two
+// shared-memory slots in the 128-byte-swizzle layout, so the next tile streams
+// in while this one is computed; Q takes the other 64 KB, so two slots is all
+// that fits.  Measured on B300, an M = 64 or 128, N = 64 product costs about
+// 50 cycles per instruction at best (about 75 in this kernel), whatever M is,
+// while M = 128 with N = 128 or more runs at the full 4,096 FMA/clk.  So the
+// logits come from one M = 128, N = 128 product per K step that stacks the
+// two halves of the latent columns (L = columns 0-255, H = 256-511):
+//   [C_L; C_H] . [Q_L; Q_H]^T   (A: the tile's 64 rows twice, K-halves L and H;
+//                               B: Q's 64 heads twice; K = 256 in 16 steps)
+//   S^T[tok, h] = D[tok, h] + D[64 + tok, 64 + h]
+// (the off-diagonal blocks are computed and ignored): 16 instructions per tile
+// instead of 32 at N = 64.  The tile and Q keep each 64-column block j at
+// block position 2(j % 4) + j / 4, so blocks j and j + 4 sit next to each other
+// and every such pair is one K-major 128-row operand (8-row groups 1 KB apart).
+//   O^T[d, h] += C[tok, d]^T . P[tok, h]   M = 128 latent columns (x4), N = 64, K = 64 tokens
+// reads the same pairs M-major: chunk c of O^T holds columns 64c + i (lane i <
+// 64) and 256 + 64c + i (lane 64 + i).  Each latent row crosses HBM once.  A
 // selected pool is kpool = 4 consecutive latent rows, so the gather is a plain
 // tiled TMA load per (pool, 64-column block): a 4-row box of 512 bytes that
 // lands at a 512-byte offset of its 1 KB swizzle atom (the swizzle follows the
 // shared-memory address, so a half atom gets the rows 4-7 pattern).  Pools
 // missing from a partial tile load rows at a negative coordinate, which the
-// TMA fills with zeros, so P.V never multiplies stale bytes.  S^T
-// (M = 64: token r in TMEM lane 32*(r/16) + r%16) and O^T (4 x 64 columns)
-// live in TMEM.  The softmax reads S^T with the 16-lane TMEM load, so each
-// thread holds 2 tokens x 8 heads; per-head tile maxima come from three
-// shuffles per head plus a 4-warp exchange; the running max is raised only
-// when a tile's max exceeds it by 2^8 (then O^T and the row sums are
-// rescaled), so the correction pass almost never runs.
+// TMA fills with zeros, so P.V never multiplies stale bytes.  D (two buffers
+// of 128 columns) and O^T (4 x 64 columns) live in TMEM.  A token's two
+// partial logits sit in lane quadrants q and q + 2, read by different warps:
+// each warp pair swaps half of its 32 heads through shared memory, so each
+// thread ends with 1 token x 16 heads.  The running max is raised only when a
+// tile's max exceeds it by 2^8 (then O^T and the row sums are rescaled), so
+// the correction pass almost never runs.
 //
 // A query's token list is split over the CTAs of a thread-block cluster
 // (up to 8).  After its tiles, each CTA dumps its unnormalised O^T, running
@@ -49,8 +54,9 @@
 // fp32 lse.  No global scratch, no second launch.
 //
 // Warp roles (416 threads, one CTA per SM):
-//   warps 0-7  softmax: warp w owns TMEM lane quadrant w % 4 (tokens 16(w%4) ..
-//              +15 in lanes 0-15) and heads 32 * (w / 4) .. +31; then the O^T dump
+//   warps 0-7  softmax: warp w reads TMEM lane quadrant w % 4 (tokens
+//              32 (w % 2) .. +31; column half (w % 4) / 2) and ends with heads
+//              32 (w / 4) + 16 ((w % 4) / 2) .. +15 of its token; then the O^T dump
 //   warp 8     TMEM allocation, Q TMA, MMA issue (one lane)
 //   warps 9-12 gather: all four load each 128-column chunk of a tile in turn,
 //              8 TMA boxes per warp per chunk (TMA issue is serial within a
@@ -86,8 +92,16 @@ static_assert(kAtTok % 16 == 0 && kAtTok <= 64, "a tile is whole K-steps of P.V 
 static_assert(kAtBlockBytes % 1024 == 0, "blocks start on a swizzle atom");
 constexpr int kAtTmemCols = 512;
 constexpr uint32_t kAtOCol = 0;                           // O^T: chunk c at columns 64c .. 64c+63
-constexpr uint32_t kAtSCol = 256;                         // S^T: two buffers of 64 columns
+constexpr uint32_t kAtSCol = 256;                         // D (stacked logits): two buffers of 128 columns
 constexpr float kAtRescaleLog2 = 8.f;                     // raise the running max only past 2^8
+// Softmax exchange during the tile loop, in the merge buffers' place: per warp
+// pair (token half, head half) and direction, [16 heads][32 tokens] f32.
+constexpr int kAtXBytes = 4 * 2 * 16 * 32 * 4;
+static_assert(kAtTok == 64, "the stacked S product and the softmax assume 64-token tiles");
+
+// Shared-memory position of 64-column block j of a tile or of Q: blocks j and
+// j + 4 (the two K-halves of one S step) are adjacent.
+__host__ __device__ constexpr int at_block_pos(int j) { return 2 * (j & 3) + (j >> 2); }
 
 // Shared memory (offsets from a 1024-aligned base).  During the tile loop:
 // Q, the tile slots, the two P buffers and a small block of per-head state and
@@ -130,7 +144,8 @@ struct AtPool {
     static constexpr int kLPart = kW + kMlaHeads * kWStride * 4;
     static constexpr int kAuxBytes = kLPart + 4 * kMlaHeads * 4;
     static constexpr int kOffAux = kOffMisc + kMiscCore;
-    static constexpr int kSmemBytes = kOffMisc + kMiscCore + kAuxBytes + 1024;  // + alignment slack
+    static constexpr int kSmemBytes = kOffMisc + kMiscCore + (kAuxBytes > kAtXBytes ? kAuxBytes : kAtXBytes) +
+                                      1024;  // + alignment slack
     static_assert(kPoolsPerTile * 2 <= 32, "a gather lane per (pool, block) of a 128-column chunk");
     static_assert(kMaxTail * kNopeDim * 2 <= 2 * kAtPBytes, "the tail rows fit in the P buffers");
     static_assert(kSmemBytes <= 232448, "attention shared memory over the per-CTA limit");
@@ -311,7 +326,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     if (tid == 32 * kAtMmaWarp && qvalid) {  // Q: 64 heads x 512 columns, 8 swizzled blocks
         mbar_expect_tx(bar(kBarQ), kAtQBytes);
         for (int blk = 0; blk < 8; ++blk)
-            tma_load_2d(sQ + blk * kAtQBlockBytes, &tm_q, bar(kBarQ), blk * 64, q * kMlaHeads);
+            tma_load_2d(sQ + at_block_pos(blk) * kAtQBlockBytes, &tm_q, bar(kBarQ), blk * 64, q * kMlaHeads);
     }
 
     // ---- the selection comes from the previous kernel
@@ -341,7 +356,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         if (lane == 0) {
             bool ok = !P.stall || mbar_wait(bar(kBarNever), 0, abort_flag, P.status, P.wait_ns);
             ok = ok && (nt == 0 || mbar_wait(bar(kBarQ), 0, abort_flag, P.status, P.wait_ns));
-            const uint32_t idesc_s = idesc_bf16_f32(64, kMlaHeads);                 // M = 64
+            const uint32_t idesc_s = idesc_bf16_f32(128, 2 * kMlaHeads);            // stacked K-halves
             const uint32_t idesc_pv = idesc_bf16_f32(128, kMlaHeads, true, true);   // M = 128 columns
             // Descriptors are built once; a step along K or to another block adds
             // (bytes >> 4) to the start-address field (addresses stay < 256 KB).
@@ -394,12 +409,13 @@ __global__ void __launch_bounds__(kAtThreads, 1)
                         if (!ok) break;
                     }
                     tc_fence_after();
+                    // Chunk c holds blocks c and c + 4 (positions 2c, 2c + 1): the
+                    // tile's rows over both K-halves as A, Q's heads over both as B.
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t blk = 2 * c + (kk >> 2), koff = (kk & 3) * 32;
-                        const uint64_t ad = dt0 + ((slot * kAtTileBytes + blk * kAtBlockBytes + koff) >> 4);
-                        const uint64_t bd = dq0 + ((blk * kAtQBlockBytes + koff) >> 4);
-                        tc_mma_bf16(tmem + kAtSCol + 64 * sbuf, ad, bd, idesc_s, (c | kk) ? 1u : 0u);
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t ad = dt0 + ((slot * kAtTileBytes + c * kAtChunkBytes + kk * 32) >> 4);
+                        const uint64_t bd = dq0 + ((2 * c * kAtQBlockBytes + kk * 32) >> 4);
+                        tc_mma_bf16(tmem + kAtSCol + 128 * sbuf, ad, bd, idesc_s, (c | kk) ? 1u : 0u);
                     }
                 }
                 if (!ok) break;
@@ -424,7 +440,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         // A tile is 4 chunks of 32 TMA boxes (16 pools x 2 64-column blocks).
         // The four warps load every chunk together, chunk by chunk: lanes 8c ..
         // 8c + 7 of warp w issue boxes j = 4 (l % 8) + w of chunk c (pool j % 16,
-        // block 2c + j / 16), so chunk 0 of a tile lands first and the S product
+        // latent column block c + 4 (j / 16)), so chunk 0 of a tile lands first and the S product
         // starts on it while chunks 1-3 are still in flight.  Warp 0 posts each
         // chunk's byte count (boxes of other warps may land before it: the
         // transaction count may go negative, the phase cannot complete without
@@ -433,7 +449,9 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         // global read sits between a freed slot and its refill.
         const int w = warp - kAtProdWarp0;
         const int my_chunk = lane >> 3, j = 4 * (lane & 7) + w;
-        const int my_pool = j % kAtPoolsPerTile, blk = 2 * my_chunk + j / kAtPoolsPerTile;
+        // chunk c = latent column blocks c and c + 4, at block positions 2c and 2c + 1
+        const int my_pool = j % kAtPoolsPerTile, khalf = j / kAtPoolsPerTile;
+        const int blk = my_chunk + 4 * khalf, spos = 2 * my_chunk + khalf;
         const bool active = j < 2 * kAtPoolsPerTile;
         const int pool0 = tb * kAtPoolsPerTile;
         const int npools = min(nt * kAtPoolsPerTile, ns - pool0);
@@ -486,7 +504,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
                 const int y = row_at(jj, pf_p[u], pf_pg[u]);
                 pf_pg[u ^ 1] = fetch_pg(pf_p[u ^ 1]);   // page of tile jj + 1's pool
                 pf_p[u] = fetch_p(jj + kAtSlots);       // pool of tile jj + 2
-                const uint32_t dst = sTile + u * kAtTileBytes + blk * kAtBlockBytes + my_pool * Pool::kBoxBytes;
+                const uint32_t dst = sTile + u * kAtTileBytes + spos * kAtBlockBytes + my_pool * Pool::kBoxBytes;
 #pragma unroll
                 for (int cc = 0; cc < kAtChunks; ++cc) {
                     if (jj >= kAtSlots) {  // P.V of the slot's previous tile has read this chunk
@@ -515,19 +533,28 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         }
     } else {
         // ------------------------------------------------------------ softmax
-        // S^T keeps token 16q + i of the tile in TMEM lane 32q + i (i < 16); the
-        // 16-lane load gives thread l tokens tA = l/4 and tB = l/4 + 8 of its
-        // quadrant and, in each 8-head group g, heads 8g + 2(l%4) and + 1.
+        // D lane i < 64 holds token i's logits over the first column half
+        // (heads in columns 0-63), lane 64 + i the same token's over the second
+        // (heads in columns 64-127).  Warp w reads lane quadrant w % 4, columns
+        // of head half w / 4: quadrants 0-1 (tokens 0-31, 32-63) the first
+        // column half, 2-3 the second.  Warps w and w ^ 2 hold the same tokens:
+        // each sends the other 16 of its 32 heads' partial sums through shared
+        // memory, so each thread ends with its token's logits for 16 heads.
         const int quad = warp & 3, half = warp >> 2;
-        const int hb = half * 32;                    // this warp's first head
-        const int tA = quad * 16 + (lane >> 2), tB = tA + 8;
-        const int cp = 2 * (lane & 3);               // my first head within each 8-head group
+        const int second = quad >> 1;                      // reads the second column half
+        const int tk = 32 * (quad & 1) + lane;             // this thread's token in the tile
+        const int hb = 32 * half + 16 * second;            // this thread's first head
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-        // Per head k = 2g + j (head hb + 8g + cp + j): row-sum partials and the
-        // running max (log2 units; a copy of mused_s).
-        float lp[8], mr[8];
+        const uint32_t scol = kAtSCol + 64 * second + 32 * half;
+        float *xbuf = reinterpret_cast<float *>(smem + Pool::kOffAux);   // the merge buffers' place
+        float *xsend = xbuf + (((quad & 1) * 2 + half) * 2 + second) * 512;        // [16][32] f32
+        const float *xrecv = xbuf + (((quad & 1) * 2 + half) * 2 + (second ^ 1)) * 512;
+        const int pair_bar = 3 + (quad & 1) * 2 + half;    // named barrier of warps w, w ^ 2
+        // Per head k (head hb + k): row-sum partial and running max (log2 units,
+        // a copy of mused_s).
+        float lp[16], mr[16];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
+        for (int k = 0; k < 16; ++k) {
             lp[k] = 0.f;
             mr[k] = -INFINITY;
         }
@@ -537,35 +564,40 @@ __global__ void __launch_bounds__(kAtThreads, 1)
                                mbar_wait(bar(kBarS + (jj & 1)), (jj >> 1) & 1, abort_flag, P.status, P.wait_ns));
             if (!ok) break;
             tc_fence_after();
-            uint32_t r[16];
-            tmem_ld_16x256b_x4(tmem + lane_base + kAtSCol + 64 * (jj & 1) + hb, r);
+            uint32_t r[32];   // heads 32 half + 0..31, this column half's partial sums
+            tmem_ld_32x32b_x32(tmem + lane_base + scol + 128 * (jj & 1), r);
             tmem_ld_wait();
+            // The partner's heads go out (the first-half warp keeps heads 0-15 of
+            // the half, the second-half warp heads 16-31).
+#pragma unroll
+            for (int k = 0; k < 16; ++k) xsend[k * 32 + lane] = __uint_as_float(second ? r[k] : r[16 + k]);
+            named_bar(pair_bar, 64);
             const int n_valid = min(kAtTok, n_pool_tok - (tb + jj) * kAtTok);
-            const bool vA = tA < n_valid, vB = tB < n_valid;
-            float xa[8], xb[8];
+            const bool valid = tk < n_valid;
+            float x[16];
             bool high = false;  // a logit more than 2^8 above the running max
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const int g = k >> 1, j = k & 1;
-                xa[k] = vA ? __uint_as_float(r[4 * g + j]) * P.scale_log2 : -INFINITY;
-                xb[k] = vB ? __uint_as_float(r[4 * g + 2 + j]) * P.scale_log2 : -INFINITY;
-                high |= (xa[k] > mr[k] + kAtRescaleLog2) | (xb[k] > mr[k] + kAtRescaleLog2);
+            for (int k = 0; k < 16; ++k) {
+                const float mine = __uint_as_float(second ? r[16 + k] : r[k]);
+                const float other = xrecv[k * 32 + lane];
+                const float z = second ? other + mine : mine + other;   // first half + second half
+                x[k] = valid ? z * P.scale_log2 : -INFINITY;
+                high |= x[k] > mr[k] + kAtRescaleLog2;
             }
             bool rescale = false;
             if (named_bar_any(1, kAtSoftThreads, high)) {
                 // Slow path (the first tile, and whenever a head's max jumps): exact
                 // per-head tile max, raise the running max, rescale O^T and row sums.
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    float m = fmaxf(xa[k], xb[k]);
-                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
-                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
-                    if (lane < 4) red_s[quad * 64 + hb + 8 * (k >> 1) + cp + (k & 1)] = m;
+                for (int k = 0; k < 16; ++k) {
+                    float m = x[k];
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                    if (lane == 0) red_s[(quad & 1) * 64 + hb + k] = m;
                 }
                 named_bar(1, kAtSoftThreads);
                 if (tid < kMlaHeads) {
-                    const float mt = fmaxf(fmaxf(red_s[tid], red_s[64 + tid]), fmaxf(red_s[128 + tid], red_s[192 + tid]));
+                    const float mt = fmaxf(red_s[tid], red_s[64 + tid]);
                     const float mo = mused_s[tid];
                     if (mt > mo + kAtRescaleLog2) {
                         mused_s[tid] = mt;
@@ -576,39 +608,40 @@ __global__ void __launch_bounds__(kAtThreads, 1)
                 }
                 named_bar(1, kAtSoftThreads);
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const int h = hb + 8 * (k >> 1) + cp + (k & 1);
-                    lp[k] *= fac_s[h];
-                    mr[k] = mused_s[h];
+                for (int k = 0; k < 16; ++k) {
+                    lp[k] *= fac_s[hb + k];
+                    mr[k] = mused_s[hb + k];
                 }
                 rescale = jj > 0;
             }
-            // p = 2^(x - m), row partial sums, bf16 P rows tA and tB (128-byte swizzle).
+            // p = 2^(x - m), row partial sums, and this token's 16 heads of P as
+            // two 16-byte pieces of its 128-byte row (128-byte swizzle).
             {
                 uint8_t *pt = smem + kOffP + (jj & 1) * kAtPBytes;
+                uint32_t pk[8];
 #pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    const float pa0 = fast_exp2(xa[2 * g] - mr[2 * g]);
-                    const float pa1 = fast_exp2(xa[2 * g + 1] - mr[2 * g + 1]);
-                    const float pb0 = fast_exp2(xb[2 * g] - mr[2 * g]);
-                    const float pb1 = fast_exp2(xb[2 * g + 1] - mr[2 * g + 1]);
-                    lp[2 * g] += pa0 + pb0;
-                    lp[2 * g + 1] += pa1 + pb1;
-                    const int chunk = 4 * half + g;
-                    if (quad * 16 < kAtTok) {  // lanes past the tile hold no token
-                        *reinterpret_cast<uint32_t *>(pt + tA * 128 + ((chunk ^ (tA & 7)) << 4) + 2 * cp) = pack_bf16x2(pa0, pa1);
-                        *reinterpret_cast<uint32_t *>(pt + tB * 128 + ((chunk ^ (tB & 7)) << 4) + 2 * cp) = pack_bf16x2(pb0, pb1);
-                    }
+                for (int g = 0; g < 8; ++g) {
+                    const float p0 = fast_exp2(x[2 * g] - mr[2 * g]);
+                    const float p1 = fast_exp2(x[2 * g + 1] - mr[2 * g + 1]);
+                    lp[2 * g] += p0;
+                    lp[2 * g + 1] += p1;
+                    pk[g] = pack_bf16x2(p0, p1);
                 }
+                const int c0 = hb >> 3;
+                *reinterpret_cast<uint4 *>(pt + tk * 128 + ((c0 ^ (tk & 7)) << 4)) =
+                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                *reinterpret_cast<uint4 *>(pt + tk * 128 + (((c0 + 1) ^ (tk & 7)) << 4)) =
+                    make_uint4(pk[4], pk[5], pk[6], pk[7]);
             }
             if (rescale) {
                 // O^T must hold P.V of the previous tile before it is rescaled; P.V of
-                // this tile waits for our arrival below.
+                // this tile waits for our arrival below.  Warp w rescales O^T lanes of
+                // quadrant w % 4, heads 32 (w / 4) .. +31, in every chunk.
                 mbar_wait(bar(kBarPV), (jj - 1) & 1, abort_flag, P.status, P.wait_ns);
                 tc_fence_after();
                 for (int c = 0; c < 2 * kAtChunks; ++c) {  // 16 heads at a time
                     uint32_t o[16];
-                    const int h0c = hb + 16 * (c & 1);
+                    const int h0c = 32 * half + 16 * (c & 1);
                     const uint32_t ta = tmem + lane_base + kAtOCol + 64 * (c >> 1) + h0c;
                     tmem_ld_32x32b_x16(ta, o);
                     tmem_ld_wait();
@@ -625,15 +658,15 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         if (ok) ok = named_bar_all(1, kAtSoftThreads, mbar_wait(bar(kBarO), 0, abort_flag, P.status, P.wait_ns));
         if (ok) {
             tc_fence_after();
-            // Row sums: add the 8 threads that share my heads (fixed order), then
-            // lanes 0-3 hold the quadrant's sums; the quadrants are added in order below.
+            // Row sums over the warp's 32 tokens (fixed order); the two token
+            // halves are added in order below.  (Every exchange read is done:
+            // the barrier above follows the last tile.)
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
+            for (int k = 0; k < 16; ++k) {
                 float v = lp[k];
-                v += __shfl_xor_sync(0xffffffffu, v, 4);
-                v += __shfl_xor_sync(0xffffffffu, v, 8);
-                v += __shfl_xor_sync(0xffffffffu, v, 16);
-                if (lane < 4) lpart_s[quad * 64 + hb + 8 * (k >> 1) + cp + (k & 1)] = v;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                if (lane == 0) lpart_s[(quad & 1) * 64 + hb + k] = v;
             }
         }
     }
@@ -653,7 +686,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     float *dump = reinterpret_cast<float *>(smem + kOffTile);   // [64 heads][512] f32
     if (warp < kAtSoftWarps) {
         if (tid < kMlaHeads && nt > 0)  // row sums in a fixed order: repeated calls give the same bits
-            lsum_s[tid] = (lpart_s[tid] + lpart_s[64 + tid]) + (lpart_s[128 + tid] + lpart_s[192 + tid]);
+            lsum_s[tid] = lpart_s[tid] + lpart_s[64 + tid];
         if (!aborted && nt > 0) {
             tc_fence_after();
             const int quad = warp & 3, hb = (warp >> 2) * 32;
@@ -663,7 +696,8 @@ __global__ void __launch_bounds__(kAtThreads, 1)
                 const int h0c = hb + 16 * (c & 1);
                 tmem_ld_32x32b_x16(tmem + lane_base + kAtOCol + 64 * (c >> 1) + h0c, o);
                 tmem_ld_wait();
-                const int d = (c >> 1) * 128 + quad * 32 + lane;  // O^T rows are latent columns
+                // O^T lane i of chunk cc is latent column 64 cc + i (i < 64), else 256 + 64 cc + i - 64
+                const int d = 64 * (c >> 1) + 256 * (quad >> 1) + 32 * (quad & 1) + lane;
 #pragma unroll
                 for (int h = 0; h < 16; ++h) dump[(h0c + h) * kNopeDim + d] = __uint_as_float(o[h]);
             }
@@ -691,7 +725,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
                 for (int e = 0; e < 16; e += 2) {
                     const int d = lane * 16 + e;
                     const uint32_t qv =
-                        *reinterpret_cast<const uint32_t *>(smem + kOffQ + (d >> 6) * kAtQBlockBytes +
+                        *reinterpret_cast<const uint32_t *>(smem + kOffQ + at_block_pos(d >> 6) * kAtQBlockBytes +
                                                             sw128_off(h, d & 63));
                     const uint32_t cv = *reinterpret_cast<const uint32_t *>(tail_s + j * kNopeDim + d);
                     acc = fmaf(bf16_lo(qv), bf16_lo(cv), acc);
