@@ -113,11 +113,14 @@ constexpr int kOffQ = 0;
 constexpr int kOffTile = kOffQ + kAtQBytes;               // slots; then this CTA's O^T dump
 constexpr int kOffP = kOffTile + kAtSlots * kAtTileBytes;
 constexpr int kOffMisc = kOffP + 2 * kAtPBytes;
-constexpr int kMiscRed = 0;                               // [4][64] f32 per-quadrant tile maxima
-constexpr int kMiscMUsed = kMiscRed + 4 * 64 * 4;         // [64] f32 running max (log2 units)
+constexpr int kMiscRed = 0;                               // [2][64] f32 per-token-half tile maxima
+constexpr int kMiscMUsed = kMiscRed + 2 * 64 * 4;         // [64] f32 running max (log2 units)
 constexpr int kMiscFac = kMiscMUsed + 64 * 4;             // [64] f32 rescale factors of this tile
 constexpr int kMiscLSum = kMiscFac + 64 * 4;              // [64] f32 row sums
-constexpr int kMiscBars = kMiscLSum + 64 * 4;             // mbarriers
+constexpr int kMiscRecv = kMiscLSum + 64 * 4;             // [2][64] f32 running maxima, row sums of the
+                                                          // heads this CTA merges, [split][head], from
+                                                          // every CTA of the cluster
+constexpr int kMiscBars = kMiscRecv + 2 * 64 * 4;         // mbarriers
 constexpr int kNumBars = 4 * kAtSlots * 2 + 9;
 constexpr int kMiscTmem = kMiscBars + kNumBars * 8;
 constexpr int kMiscAbort = kMiscTmem + 4;
@@ -242,6 +245,8 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     float *mused_s = reinterpret_cast<float *>(misc + kMiscMUsed);
     float *fac_s = reinterpret_cast<float *>(misc + kMiscFac);
     float *lsum_s = reinterpret_cast<float *>(misc + kMiscLSum);
+    float *recv_m = reinterpret_cast<float *>(misc + kMiscRecv);
+    float *recv_l = recv_m + 64;
     using Pool = AtPool<KP>;
     constexpr int kAtMaxTail = Pool::kMaxTail;
     constexpr int kAtPoolsPerTile = Pool::kPoolsPerTile;
@@ -687,6 +692,13 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     if (warp < kAtSoftWarps) {
         if (tid < kMlaHeads && nt > 0)  // row sums in a fixed order: repeated calls give the same bits
             lsum_s[tid] = lpart_s[tid] + lpart_s[64 + tid];
+        if (S > 1 && tid < kMlaHeads) {
+            // Head tid's running max and row sum go to the CTA that merges it, so
+            // the merge weights read local memory after the cluster barrier.
+            const int r = tid / nh, hl = tid % nh;
+            dsmem_st_f32(dsmem_addr(smem_u32(recv_m + split * nh + hl), r), mused_s[tid]);
+            dsmem_st_f32(dsmem_addr(smem_u32(recv_l + split * nh + hl), r), lsum_s[tid]);
+        }
         if (!aborted && nt > 0) {
             tc_fence_after();
             const int quad = warp & 3, hb = (warp >> 2) * 32;
@@ -750,9 +762,9 @@ __global__ void __launch_bounds__(kAtThreads, 1)
             for (int s2 = 0; s2 < kAtMaxSplits; ++s2) {
                 ms[s2] = -INFINITY;
                 ls[s2] = 0.f;
-                if (s2 < S) {
-                    ms[s2] = dsmem_ld_f32(dsmem_addr(smem_u32(mused_s + h), s2));
-                    ls[s2] = dsmem_ld_f32(dsmem_addr(smem_u32(lsum_s + h), s2));
+                if (s2 < S) {   // pushed by every CTA before the cluster barrier
+                    ms[s2] = S > 1 ? recv_m[s2 * nh + tid] : mused_s[h];
+                    ls[s2] = S > 1 ? recv_l[s2 * nh + tid] : lsum_s[h];
                 }
             }
             float M = -INFINITY;
