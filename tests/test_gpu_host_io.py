@@ -157,3 +157,25 @@ def test_run_host_rejects_small_chunks():
     h_out = torch.empty(out_buf.numel(), dtype=torch.uint8).pin_memory()
     with pytest.raises(ValueError):
         step.run_host(h_in, h_out, chunk_queries=64)
+
+
+@pytest.mark.parametrize("mode,page_tokens", [(kp.SELECT_FUSED, None), (kp.SELECT_STAGED, 256)])
+def test_run_host_chunked_fused_select_and_pages(mode, page_tokens):
+    # the selection-only call through the fused score-and-select kernel, and
+    # the chunked attention on paged caches, each against the device-only step
+    wl = KI.make(KI.Spec("hostio", [20000], [600], topk_tokens=2048, seed=87))
+    _, ref = PL.make_gpu(wl, PL.cfg_of(wl, select_mode=mode), page_tokens=page_tokens)
+    ref.run()
+    torch.cuda.synchronize()
+    sess, step = PL.make_gpu(wl, PL.cfg_of(wl, select_mode=mode), page_tokens=page_tokens)
+    in_buf, out_buf = step.pack_io()
+    h_in = torch.empty(in_buf.numel(), dtype=torch.uint8).pin_memory()
+    h_in.copy_(in_buf)
+    h_out = torch.empty(out_buf.numel(), dtype=torch.uint8).pin_memory()
+    in_buf.zero_()
+    step.out.zero_()
+    step.run_host(h_in, h_out, chunk_queries=256)
+    torch.cuda.synchronize()
+    assert int(sess.status.item()) == 0
+    assert len(step._chunked["bounds"]) == 2
+    _same(step, ref, h_out, out_buf)
