@@ -117,10 +117,11 @@ constexpr int kMiscRed = 0;                               // [2][64] f32 per-tok
 constexpr int kMiscMUsed = kMiscRed + 2 * 64 * 4;         // [64] f32 running max (log2 units)
 constexpr int kMiscFac = kMiscMUsed + 64 * 4;             // [64] f32 rescale factors of this tile
 constexpr int kMiscLSum = kMiscFac + 64 * 4;              // [64] f32 row sums
-constexpr int kMiscRecv = kMiscLSum + 64 * 4;             // [2][64] f32 running maxima, row sums of the
-                                                          // heads this CTA merges, [split][head], from
-                                                          // every CTA of the cluster
-constexpr int kMiscBars = kMiscRecv + 2 * 64 * 4;         // mbarriers
+constexpr int kAtRecvSlots = 66;                          // max over splits S != 7 of S x ceil(64 / S)
+constexpr int kMiscRecv = kMiscLSum + 64 * 4;             // [2][kAtRecvSlots] f32 running maxima, row
+                                                          // sums of the heads this CTA merges,
+                                                          // [head][split], from every CTA of the cluster
+constexpr int kMiscBars = kMiscRecv + 2 * kAtRecvSlots * 4;   // mbarriers
 constexpr int kNumBars = 4 * kAtSlots * 2 + 9;
 constexpr int kMiscTmem = kMiscBars + kNumBars * 8;
 constexpr int kMiscAbort = kMiscTmem + 4;
@@ -246,7 +247,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     float *fac_s = reinterpret_cast<float *>(misc + kMiscFac);
     float *lsum_s = reinterpret_cast<float *>(misc + kMiscLSum);
     float *recv_m = reinterpret_cast<float *>(misc + kMiscRecv);
-    float *recv_l = recv_m + 64;
+    float *recv_l = recv_m + kAtRecvSlots;
     using Pool = AtPool<KP>;
     constexpr int kAtMaxTail = Pool::kMaxTail;
     constexpr int kAtPoolsPerTile = Pool::kPoolsPerTile;
@@ -265,8 +266,10 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int S = P.splits;
     const int q = blockIdx.x / S, split = blockIdx.x % S;
-    const int nh = kMlaHeads / S;   // heads this CTA merges (S divides 64)
-    const int h0 = nh * split;
+    // Heads this CTA merges: [64 split / S, 64 (split + 1) / S), 64 / S rounded
+    // either way when S does not divide 64.
+    const int h0 = kMlaHeads * split / S;
+    const int nh = kMlaHeads * (split + 1) / S - h0;
 
     // ---- set-up, and what this query is: inputs no earlier kernel of the step
     // writes, so they are read before the grid dependency resolves.
@@ -695,9 +698,10 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         if (S > 1 && tid < kMlaHeads) {
             // Head tid's running max and row sum go to the CTA that merges it, so
             // the merge weights read local memory after the cluster barrier.
-            const int r = tid / nh, hl = tid % nh;
-            dsmem_st_f32(dsmem_addr(smem_u32(recv_m + split * nh + hl), r), mused_s[tid]);
-            dsmem_st_f32(dsmem_addr(smem_u32(recv_l + split * nh + hl), r), lsum_s[tid]);
+            const int r = (tid * S + S - 1) / kMlaHeads;          // the CTA whose head range holds tid
+            const int hl = tid - kMlaHeads * r / S;
+            dsmem_st_f32(dsmem_addr(smem_u32(recv_m + hl * S + split), r), mused_s[tid]);
+            dsmem_st_f32(dsmem_addr(smem_u32(recv_l + hl * S + split), r), lsum_s[tid]);
         }
         if (!aborted && nt > 0) {
             tc_fence_after();
@@ -763,8 +767,8 @@ __global__ void __launch_bounds__(kAtThreads, 1)
                 ms[s2] = -INFINITY;
                 ls[s2] = 0.f;
                 if (s2 < S) {   // pushed by every CTA before the cluster barrier
-                    ms[s2] = S > 1 ? recv_m[s2 * nh + tid] : mused_s[h];
-                    ls[s2] = S > 1 ? recv_l[s2 * nh + tid] : lsum_s[h];
+                    ms[s2] = S > 1 ? recv_m[tid * S + s2] : mused_s[h];
+                    ls[s2] = S > 1 ? recv_l[tid * S + s2] : lsum_s[h];
                 }
             }
             float M = -INFINITY;
@@ -939,7 +943,7 @@ kp_status launch_attend_kp(const kp_attend_args &a, cudaStream_t s) {
     if (sms <= 0) return KP_ERR_CUDA;
     if (!attend_smem_configured<KP>()) return KP_ERR_CUDA;
     int splits = attend_splits(a.cfg, nq, sms);
-    while (splits > 1 && max_active_clusters<KP>(splits) < nq) splits /= 2;
+    while (splits > 1 && max_active_clusters<KP>(splits) < nq) splits = attend_splits_lower(splits);
 
     // The gather addresses latent rows by a signed 32-bit TMA coordinate
     // (validated: latent_rows <= INT32_MAX).
@@ -979,16 +983,20 @@ kp_status launch_attend_kp(const kp_attend_args &a, cudaStream_t s) {
 
 }  // namespace
 
-// Splits of one query's token list = CTAs of its cluster: a power of two (the
-// merge gives each CTA 64 / splits heads), at most 8, at most one per tile, and
-// no more than keep the grid within the SMs.
+// Splits of one query's token list = CTAs of its cluster: at most 8, at most
+// one per tile, and no more than keep the grid within the SMs; never 7, whose
+// one 10-head CTA would need 70 merge slots (kAtRecvSlots holds 66).  The
+// launch lowers the count further while the clusters do not all fit at once.
 int attend_splits(const kp_config &cfg, int32_t num_queries, int sm_count) {
     if (num_queries <= 0) return 1;
     const int tiles = (cfg.topk_tokens + kAtTok - 1) / kAtTok;
-    int s = 1;
-    while (s * 2 <= kAtMaxSplits && s * 2 <= tiles && static_cast<int64_t>(num_queries) * s * 2 <= sm_count) s *= 2;
+    int s = kAtMaxSplits;
+    while (s > 1 && (s > tiles || static_cast<int64_t>(num_queries) * s > sm_count || s == 7)) --s;
     return s;
 }
+// The next smaller split count the launch tries when the clusters of `s` do
+// not all fit at once.
+int attend_splits_lower(int s) { return s == 8 ? 6 : s - 1; }
 
 size_t attend_ws_bytes(const kp_config &cfg, int32_t num_queries, int splits) {
     (void)cfg;

@@ -79,6 +79,7 @@ kp_status launch_kernel(const char *name, void (*kernel)(KArgs...), const Launch
 // Byte sizes of the step workspaces.
 size_t score_plan_bytes(int32_t num_queries);
 int attend_splits(const kp_config &cfg, int32_t num_queries, int sm_count);
+int attend_splits_lower(int splits);
 size_t attend_ws_bytes(const kp_config &cfg, int32_t num_queries, int splits);
 
 // Inputs of the scorer's work plan, for building it inside another launch.

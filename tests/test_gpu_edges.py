@@ -82,3 +82,15 @@ def test_step_with_new_tokens_and_no_queries():
     torch.cuda.synchronize()
     assert int(sess.status.item()) == 0
     PL.check_pooled(sess, wl)     # the appended pools (and the older ones) against the oracle
+
+
+@pytest.mark.parametrize("nq", [16, 26, 40])
+def test_cluster_sizes_that_do_not_divide_the_heads(nq):
+    # 16, 26 and 40 queries take clusters of 6, 5 and 3 CTAs on a 148-SM B300
+    # (the largest split count whose clusters all fit at once), so the CTAs
+    # merge 10-11, 12-13 and 21-22 of the 64 heads; every stage of every
+    # query against the oracle, through the forward call
+    lens = [6000 + 37 * i for i in range(4)]
+    per = [nq // 4 + (1 if i < nq % 4 else 0) for i in range(4)]
+    wl = KI.make(KI.Spec("edge", lens, per, topk_tokens=2048, seed=90 + nq))
+    PL.full_check(wl, stages=False)
