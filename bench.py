@@ -17,6 +17,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import re
 import os
 import statistics
 import sys
@@ -145,12 +146,22 @@ def measured_peaks():
     return 6400.0, 1800.0, 1400.0, "fallback"
 
 
+def code_of(src: str) -> str:
+    """C++/CUDA source without its comments and with runs of white space
+    collapsed: what a traffic figure depends on.  (String literals in these
+    sources hold no comment markers.)"""
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", " ", src)
+    return " ".join(src.split())
+
+
 def kernel_source_hash(stage: str) -> str:
-    """Hash of the stage's kernel source and its headers: a traffic figure
-    is used only while the sources it was captured on are unchanged."""
+    """Hash of the code of the stage's kernel source and its headers (comments
+    and layout ignored): a traffic figure is used only while the code it was
+    captured on is unchanged."""
     h = hashlib.sha256()
     for f in KERNEL_FILES[stage]:
-        h.update(open(os.path.join(ROOT, "dsa_indexer_sparse_kpool_b300", "csrc", f), "rb").read())
+        h.update(code_of(open(os.path.join(ROOT, "dsa_indexer_sparse_kpool_b300", "csrc", f)).read()).encode())
     return h.hexdigest()[:16]
 
 

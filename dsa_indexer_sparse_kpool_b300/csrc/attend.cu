@@ -45,13 +45,14 @@
 // tile's max exceeds it by 2^8 (then O^T and the row sums are rescaled), so
 // the correction pass almost never runs.
 //
-// A query's token list is split over the CTAs of a thread-block cluster
-// (up to 8).  After its tiles, each CTA dumps its unnormalised O^T, running
-// max and row sums to its own shared memory; after a cluster barrier, CTA r
-// merges heads [64r/S, 64(r+1)/S) across the cluster through distributed
-// shared memory, adds the <= 3 tail tokens (computed on CUDA cores, so the
-// tail never costs a tensor-core tile), normalises and writes bf16 out and
-// fp32 lse.  No global scratch, no second launch.
+// A query's token list is split over the S CTAs of a thread-block cluster
+// (up to 8; any count but 7).  After its tiles, each CTA dumps its
+// unnormalised O^T to its own shared memory and sends each head's running max
+// and row sum to the CTA that merges the head; after a cluster barrier, CTA r
+// merges heads [64r/S, 64(r+1)/S) (rounded down) across the cluster through
+// distributed shared memory, adds the <= kpool - 1 tail tokens (computed on
+// CUDA cores, so the tail never costs a tensor-core tile), normalises and
+// writes bf16 out and fp32 lse.  No global scratch, no second launch.
 //
 // Warp roles (416 threads, one CTA per SM):
 //   warps 0-7  softmax: warp w reads TMEM lane quadrant w % 4 (tokens

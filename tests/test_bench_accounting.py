@@ -42,3 +42,13 @@ def test_flops_closed_form():
     fl = bench.algorithmic_flops(wl)
     assert fl["indexer_score"] == B * (CTX // 4) * 32 * 128 * 2
     assert fl["sparse_mla_attend"] == B * K * 4 * 64 * 512 * 2 * 2
+
+
+def test_source_hash_follows_code_not_comments():
+    a = "int f(int x) {  // doubles x\n    return 2 * x; /* fast */\n}\n"
+    b = "// header comment\nint f(int x) {\n  return 2 * x;\n}\n"
+    c = "int f(int x) { return 3 * x; }\n"
+    assert bench.code_of(a) == bench.code_of(b)
+    assert bench.code_of(a) != bench.code_of(c)
+    for stage in bench.KERNEL_FILES:
+        assert len(bench.kernel_source_hash(stage)) == 16
