@@ -48,7 +48,13 @@ constexpr int kGmNumBars = 2 * kGmMaxStages + 4 + 1;
 // The MMA reads a 128-row A window from each stage; with fewer A rows loaded
 // the window runs past the stage (rows >= m only feed output rows that are never
 // stored), so the ring is followed by one A tile of slack.
-constexpr int kGmSmemBytes = kGmRingBytes + kGmABytes + kGmNumBars * 8 + 1024;
+// Per epilogue warp, a 32-row x 32-column bf16 block staged on its way out, so
+// that the warp writes whole 64-byte row pieces (8 rows per store) instead of
+// 16 bytes in each of 32 rows.
+constexpr int kGmStageWarpBytes = 32 * 64;
+constexpr int kGmOffStage = kGmRingBytes + kGmABytes + (kGmNumBars * 8 + 127) / 128 * 128;
+constexpr int kGmSmemBytes = kGmOffStage + (kGmEpiThreads / 32) * kGmStageWarpBytes + 1024;
+static_assert(kGmSmemBytes <= 232448, "GEMM shared memory over the per-CTA limit");
 
 // One product of a launch.  Its units are unit0 .. unit0 + batch * m_tiles *
 // n_tiles - 1, in the order batch, column tile, row tile (row tiles of one
@@ -283,12 +289,39 @@ __global__ void __launch_bounds__(kGmThreads, 1)
             tc_fence_after();
             const int row = mt * kGmM + quad * 32 + lane;
             const uint32_t tbase = tmem + acc * kGmMaxN + (static_cast<uint32_t>(quad * 32) << 16);
+            const int row0 = mt * kGmM + quad * 32;   // the warp's first row
             for (int ch = half; ch < g.bn / 32; ch += 2) {
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(tbase + ch * 32, r);
                 tmem_ld_wait();
                 const int col0 = nt * g.bn + ch * 32;  // column inside the batch
-                if (row < g.m && col0 < g.n) store_row_chunk(g, b, row, col0, r);
+                uint16_t *c0 = static_cast<uint16_t *>(g.c) + static_cast<int64_t>(row0) * g.ldc +
+                               b * g.c_batch_off + col0;
+                if (!g.c_f32 && col0 + 32 <= g.n && (g.ldc & 7) == 0 &&
+                    (reinterpret_cast<uintptr_t>(c0) & 15) == 0) {
+                    // bf16 rows through the warp's staging block: lane l writes its
+                    // row's four 16-byte pieces (piece slots swizzled by the row, so
+                    // neither side conflicts), then 4 lanes per row store 8 rows at a time
+                    uint32_t *st = reinterpret_cast<uint32_t *>(smem + kGmOffStage) + (warp - 2) * (kGmStageWarpBytes / 4);
+#pragma unroll
+                    for (int pc = 0; pc < 4; ++pc)
+                        *reinterpret_cast<uint4 *>(st + lane * 16 + ((pc ^ ((lane >> 1) & 3)) << 2)) =
+                            make_uint4(pack_bf16x2(__uint_as_float(r[8 * pc]), __uint_as_float(r[8 * pc + 1])),
+                                       pack_bf16x2(__uint_as_float(r[8 * pc + 2]), __uint_as_float(r[8 * pc + 3])),
+                                       pack_bf16x2(__uint_as_float(r[8 * pc + 4]), __uint_as_float(r[8 * pc + 5])),
+                                       pack_bf16x2(__uint_as_float(r[8 * pc + 6]), __uint_as_float(r[8 * pc + 7])));
+                    __syncwarp();
+                    const int part = lane & 3;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int rr = 8 * i + (lane >> 2);
+                        const uint4 v = *reinterpret_cast<const uint4 *>(st + rr * 16 + ((part ^ ((rr >> 1) & 3)) << 2));
+                        if (row0 + rr < g.m) *reinterpret_cast<uint4 *>(c0 + static_cast<int64_t>(rr) * g.ldc + 8 * part) = v;
+                    }
+                    __syncwarp();   // the block is rewritten by the next chunk
+                } else if (row < g.m && col0 < g.n) {
+                    store_row_chunk(g, b, row, col0, r);
+                }
             }
             tc_fence_before();
             mbar_arrive(acce_bar(acc));
